@@ -1,0 +1,104 @@
+// CPU oracle for the asynchronous global->shared streaming path.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
+// definition of what each streaming operation computes. Only the test suite,
+// the smoke check and the benchmark's CPU-baseline leg may load it. The CUDA
+// library never includes, links or calls anything here, and this file shares
+// no header, helper or constant with it.
+//
+// Asynchronous copy changes when bytes move, never which bytes, so each
+// operation's result has a plain definition that is written out below as the
+// simplest loop. Built with -O2 -ffp-contract=off -fno-fast-math so that the
+// compiler neither fuses a*b+c (GCC's default on aarch64) nor reorders
+// floating-point work.
+//
+// Parity status: every function below is pinned by tests that do not call it
+// twice (worked example, library routines, exact rational arithmetic,
+// closed forms and invariants); nothing here is "parity unpinned".
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+extern "C" {
+
+// Elementwise scale y = alpha * x.
+// "CUDA Async Copy and Pipeline Guide", Implementation Comparison (Before and
+// After kernels): every element of a 256-float tile is multiplied by 2.0f and
+// stored; the asynchronous version computes the same product. One fp32
+// multiply, rounded to nearest even.
+void orc_scale(const float* in, float* out, int64_t n, float alpha) {
+    for (int64_t i = 0; i < n; ++i) {
+        out[i] = alpha * in[i];
+    }
+}
+
+// Row shift B[i, :] = A[(i + shift) mod rows, :] of a row-major rows x cols
+// matrix.
+// "Asynchronous Copies" (TVM TIRx), section A Global-to-Shared Copy: each of 64
+// threads copies one 4-float row into shared memory and then reads the next
+// thread's row, (tid + 1) % 64; the page checks the result against
+// torch.roll(a, shifts=-1, dims=0). shift = 1 is that example; any other shift
+// is reduced modulo rows into [0, rows).
+// Returns 0, or -1 for rows < 1 or cols < 1 with a non-empty matrix.
+int orc_row_roll(const float* A, float* B, int64_t rows, int64_t cols, int64_t shift) {
+    if (rows == 0 || cols == 0) return 0;
+    if (rows < 0 || cols < 0) return -1;
+    const int64_t s = ((shift % rows) + rows) % rows;
+    for (int64_t i = 0; i < rows; ++i) {
+        const int64_t src_row = (i + s) % rows;
+        for (int64_t j = 0; j < cols; ++j) {
+            B[i * cols + j] = A[src_row * cols + j];
+        }
+    }
+    return 0;
+}
+
+// Polynomial p(x) = sum_k c[k] x^k of degree K, evaluated by Horner's rule with
+// one fused multiply-add per step:
+//   p = c[K];  for k = K-1 .. 0:  p = fma(p, x, c[k]).
+// The pages leave the per-tile compute open ("compute on tile[cur]" in
+// "Asynchronous Data Movement", section Double buffering) and name "not enough
+// work to hide copy latency" as a pitfall ("CUDA Async Copy and Pipeline
+// Guide", Common Performance Issues); the Horner chain is the library's
+// tunable-intensity stand-in for that compute. Coefficients are in ascending
+// order of power; degree 0 gives the constant c[0].
+int orc_poly(const float* in, float* out, int64_t n, const float* coeffs, int degree) {
+    if (degree < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const float x = in[i];
+        float p = coeffs[degree];
+        for (int k = degree - 1; k >= 0; --k) {
+            p = std::fma(p, x, coeffs[k]);
+        }
+        out[i] = p;
+    }
+    return 0;
+}
+
+// Cluster hand-off: the input is cut into chunks of chunk_bytes, and every run
+// of cluster_size consecutive chunks is one cluster's share. Within a cluster
+// the chunk of rank r is handed to rank (r - 1) mod cluster_size, so that
+//   out chunk (g*cs + r) = in chunk (g*cs + (r + 1) mod cs).
+// "Asynchronous Copies" (TVM TIRx), section Copies between CTAs: a CTA copies
+// a shared-memory chunk into another CTA of its thread-block cluster. The
+// direction follows the same page's row-shift convention, where each thread
+// reads its neighbour (tid + 1).
+// Returns 0, or -1 when the sizes do not form whole clusters of whole chunks.
+int orc_cluster_exchange(const float* in, float* out, int64_t n, int cluster_size,
+                         int64_t chunk_bytes) {
+    if (cluster_size < 1 || chunk_bytes < 4 || chunk_bytes % 4 != 0 || n < 0) return -1;
+    const int64_t E = chunk_bytes / 4;
+    const int64_t cs = cluster_size;
+    if (n % (E * cs) != 0) return -1;
+    const int64_t chunks = n / E;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t group = c / cs;
+        const int64_t r = c % cs;
+        const int64_t src = group * cs + (r + 1) % cs;
+        std::memcpy(out + c * E, in + src * E, (size_t)E * sizeof(float));
+    }
+    return 0;
+}
+
+}  // extern "C"
