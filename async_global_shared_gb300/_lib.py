@@ -1,0 +1,203 @@
+"""ctypes binding of libasyncpipe: argument marshalling only.
+
+Every function has the C entry point's name and arguments. Buffers may be
+given as torch tensors (float32, on the current CUDA device, contiguous) or as
+raw integer device addresses; ``stream`` may be a ``torch.cuda.Stream``, a raw
+``cudaStream_t`` integer, or None for torch's current stream. A status other
+than AP_OK raises :class:`APError`. Nothing here computes: every step runs in
+the library's CUDA kernels, and a missing library raises instead of falling
+back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libasyncpipe.so")
+
+AP_OK = 0
+STATUS_NAMES = {
+    0: "AP_OK",
+    1: "AP_ERR_NULL",
+    2: "AP_ERR_SHAPE",
+    3: "AP_ERR_ALIGN",
+    4: "AP_ERR_ALIAS",
+    5: "AP_ERR_STAGES",
+    6: "AP_ERR_CLUSTER",
+    7: "AP_ERR_SMEM",
+    8: "AP_ERR_CUDA",
+    9: "AP_ERR_DEVICE_TIMEOUT",
+    10: "AP_ERR_UNSUPPORTED_DEVICE",
+    11: "AP_ERR_ARG",
+}
+globals().update({name: code for code, name in STATUS_NAMES.items()})
+
+AP_MIN_STAGES = 2
+AP_MAX_STAGES = 6
+AP_POLY_MAX_DEGREE = 1023
+
+# ap_debug_key
+AP_DBG_FORCE_PATH = 1
+AP_DBG_EXPECT_TX_EXTRA = 2
+AP_DBG_TIMEOUT_NS = 3
+AP_DBG_STAGE_BYTES = 4
+AP_DBG_GRID = 5
+AP_DBG_CTAS_PER_SM = 6
+AP_DBG_ROLL_STAGES = 7
+AP_DBG_LAST_PATH = 100
+AP_DBG_LAST_GRID = 101
+AP_DBG_LAST_STAGE_ELEMS = 102
+AP_DBG_LAST_SMEM = 103
+AP_DBG_LAST_STAGES = 104
+AP_DBG_LAST_FLAGS = 105
+
+# Every symbol the headers under include/ declare.
+EXPORTED = (
+    "ap_scale",
+    "ap_scale_sync",
+    "ap_row_roll",
+    "ap_poly",
+    "ap_cluster_exchange",
+    "ap_check",
+    "ap_status_string",
+    "ap_debug_set",
+    "ap_debug_get",
+    "ap_debug_emulate_ring",
+)
+
+
+class APError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} failed: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+_f32p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libasyncpipe.so (built by ``async_global_shared_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"libasyncpipe is not built ({p} missing); run `python -c \"import __graft_entry__ as g; g.build()\"`"
+        )
+    lib = ctypes.CDLL(p)
+    vp = ctypes.c_void_p
+    lib.ap_scale.argtypes = [vp, vp, _i64, _i64, ctypes.c_float, ctypes.c_int, vp]
+    lib.ap_scale_sync.argtypes = [vp, vp, _i64, _i64, ctypes.c_float, vp]
+    lib.ap_row_roll.argtypes = [vp, vp, _i64, _i64, _i64, vp]
+    lib.ap_poly.argtypes = [vp, vp, _i64, vp, ctypes.c_int, ctypes.c_int, vp]
+    lib.ap_cluster_exchange.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, vp]
+    lib.ap_check.argtypes = [vp]
+    lib.ap_status_string.argtypes = [ctypes.c_int]
+    lib.ap_status_string.restype = ctypes.c_char_p
+    lib.ap_debug_set.argtypes = [ctypes.c_int, _i64]
+    lib.ap_debug_get.argtypes = [ctypes.c_int]
+    lib.ap_debug_get.restype = _i64
+    lib.ap_debug_emulate_ring.argtypes = [vp, vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _i64]
+    for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange", "ap_check",
+                 "ap_debug_set", "ap_debug_emulate_ring"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _addr(buf) -> int | None:
+    """Device address of a tensor (checked: float32, CUDA, contiguous) or an int."""
+    if buf is None:
+        return None
+    if isinstance(buf, int):
+        return buf
+    if hasattr(buf, "data_ptr"):
+        import torch
+
+        if buf.dtype != torch.float32:
+            raise TypeError("libasyncpipe works on float32 tensors")
+        if not buf.is_cuda:
+            raise TypeError("libasyncpipe needs CUDA tensors (device memory)")
+        if not buf.is_contiguous():
+            raise TypeError("libasyncpipe needs contiguous tensors")
+        return buf.data_ptr()
+    raise TypeError(f"cannot take a device address of {type(buf).__name__}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, call: str):
+    if status != AP_OK:
+        raise APError(status, call)
+
+
+def ap_scale(inp, out, n_tiles: int, tile_elems: int, alpha: float, stages: int, stream=None):
+    _check(load().ap_scale(_addr(inp), _addr(out), n_tiles, tile_elems, alpha, stages, _stream(stream)), "ap_scale")
+
+
+def ap_scale_sync(inp, out, n_tiles: int, tile_elems: int, alpha: float, stream=None):
+    _check(load().ap_scale_sync(_addr(inp), _addr(out), n_tiles, tile_elems, alpha, _stream(stream)),
+           "ap_scale_sync")
+
+
+def ap_row_roll(A, B, rows: int, cols: int, shift: int, stream=None):
+    _check(load().ap_row_roll(_addr(A), _addr(B), rows, cols, shift, _stream(stream)), "ap_row_roll")
+
+
+def ap_poly(inp, out, n: int, coeffs, degree: int, stages: int, stream=None):
+    """``coeffs`` is a HOST sequence of degree + 1 floats (copied by the call)."""
+    c = (ctypes.c_float * max(1, len(coeffs)))(*[float(v) for v in coeffs])
+    if len(coeffs) < degree + 1:
+        raise ValueError("ap_poly needs degree + 1 coefficients")
+    _check(load().ap_poly(_addr(inp), _addr(out), n, ctypes.cast(c, ctypes.c_void_p), degree, stages,
+                          _stream(stream)), "ap_poly")
+
+
+def ap_cluster_exchange(inp, out, n: int, cluster_size: int, chunk_bytes: int, stream=None):
+    _check(load().ap_cluster_exchange(_addr(inp), _addr(out), n, cluster_size, chunk_bytes, _stream(stream)),
+           "ap_cluster_exchange")
+
+
+def ap_check(stream=None) -> int:
+    """Wait for the stream and return (not raise) the device status, then clear it."""
+    return load().ap_check(_stream(stream))
+
+
+def ap_status_string(status: int) -> str:
+    return load().ap_status_string(status).decode()
+
+
+def ap_debug_set(key: int, value: int):
+    _check(load().ap_debug_set(key, value), "ap_debug_set")
+
+
+def ap_debug_get(key: int) -> int:
+    return load().ap_debug_get(key)
+
+
+def ap_debug_emulate_ring(in_host, out_host, n: int, off: int, in_mis: int, out_mis: int, stage_elems: int) -> int:
+    """Host emulation (numpy float32 arrays); returns the status code."""
+    import numpy as np
+
+    assert in_host.dtype == np.float32 and out_host.dtype == np.float32
+    return load().ap_debug_emulate_ring(in_host.ctypes.data, out_host.ctypes.data, n, off, in_mis, out_mis,
+                                        stage_elems)

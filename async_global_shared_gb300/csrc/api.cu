@@ -1,0 +1,393 @@
+// C-ABI entry points of libasyncpipe: argument validation (before any CUDA
+// call), per-device set-up, dispatch to the kernel launchers, the device
+// status word, the tuning hooks and the host emulator of the ring's data
+// movement.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace ap {
+
+// One status word per device that loads the library: the first error a
+// kernel records since the last ap_check. Not an allocation: a static
+// device variable of the library's module.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+// ------------------------------------------------------------------ options
+
+std::atomic<int64_t> g_force_path{0};
+std::atomic<int64_t> g_tx_extra{0};
+std::atomic<int64_t> g_timeout_ns{0};
+std::atomic<int64_t> g_stage_bytes{0};
+std::atomic<int64_t> g_grid{0};
+std::atomic<int64_t> g_ctas_per_sm{0};
+std::atomic<int64_t> g_roll_stages{0};
+
+std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
+    g_last_flags{0};
+
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;  // 2 s
+
+int64_t env_timeout() {
+    static const int64_t v = [] {
+        const char* s = std::getenv("AP_WAIT_TIMEOUT_NS");
+        if (s == nullptr || *s == '\0') return int64_t(0);
+        const long long x = std::atoll(s);
+        return x > 0 ? static_cast<int64_t>(x) : int64_t(0);
+    }();
+    return v;
+}
+
+// ------------------------------------------------------------------ devices
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+bool g_dev_ready[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+ap_status g_dev_err[kMaxDevices];
+
+ap_status current_device(DeviceInfo* out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return AP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo di{};
+        di.device = dev;
+        ap_status st = AP_OK;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            st = AP_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            st = AP_ERR_UNSUPPORTED_DEVICE;
+        } else {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+                st = AP_ERR_CUDA;
+            } else {
+                di.status = static_cast<uint32_t*>(p);
+            }
+        }
+        if (st == AP_ERR_CUDA) return st;  // not cached: may succeed later
+        g_dev[dev] = di;
+        g_dev_err[dev] = st;
+        g_dev_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    return g_dev_err[dev];
+}
+
+// ------------------------------------------------------------------ validation
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+// Byte ranges [a, a+na) and [b, b+nb) overlap.
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+}
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;  // keeps every byte offset far from overflow
+
+bool valid_stages(int stages) { return stages >= AP_MIN_STAGES && stages <= AP_MAX_STAGES; }
+
+}  // namespace
+
+Options options() {
+    Options o;
+    o.force_path = g_force_path.load();
+    o.tx_extra = g_tx_extra.load();
+    const int64_t t = g_timeout_ns.load();
+    o.timeout_ns = t > 0 ? t : (env_timeout() > 0 ? env_timeout() : kDefaultTimeoutNs);
+    o.stage_bytes = g_stage_bytes.load();
+    o.grid = g_grid.load();
+    o.ctas_per_sm = g_ctas_per_sm.load();
+    o.roll_stages = g_roll_stages.load();
+    return o;
+}
+
+void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem, int64_t stages, int64_t flags) {
+    g_last_path = path;
+    g_last_grid = grid;
+    g_last_stage_elems = stage_elems;
+    g_last_smem = smem;
+    g_last_stages = stages;
+    g_last_flags = flags;
+}
+
+}  // namespace ap
+
+using namespace ap;
+
+extern "C" {
+
+const char* ap_status_string(ap_status s) {
+    switch (s) {
+        case AP_OK: return "AP_OK";
+        case AP_ERR_NULL: return "AP_ERR_NULL";
+        case AP_ERR_SHAPE: return "AP_ERR_SHAPE";
+        case AP_ERR_ALIGN: return "AP_ERR_ALIGN";
+        case AP_ERR_ALIAS: return "AP_ERR_ALIAS";
+        case AP_ERR_STAGES: return "AP_ERR_STAGES";
+        case AP_ERR_CLUSTER: return "AP_ERR_CLUSTER";
+        case AP_ERR_SMEM: return "AP_ERR_SMEM";
+        case AP_ERR_CUDA: return "AP_ERR_CUDA";
+        case AP_ERR_DEVICE_TIMEOUT: return "AP_ERR_DEVICE_TIMEOUT";
+        case AP_ERR_UNSUPPORTED_DEVICE: return "AP_ERR_UNSUPPORTED_DEVICE";
+        case AP_ERR_ARG: return "AP_ERR_ARG";
+    }
+    return "AP_ERR_UNKNOWN";
+}
+
+ap_status ap_scale(const float* in, float* out, int64_t n_tiles, int64_t tile_elems, float alpha, int stages,
+                   cudaStream_t stream) {
+    if (!valid_stages(stages)) return AP_ERR_STAGES;
+    if (n_tiles < 0 || tile_elems < 1) return AP_ERR_SHAPE;
+    if (n_tiles > 0 && tile_elems > kMaxElems / n_tiles) return AP_ERR_SHAPE;
+    const int64_t n = n_tiles * tile_elems;
+    if (n == 0) return AP_OK;
+    if (in == nullptr || out == nullptr) return AP_ERR_NULL;
+    if (!aligned4(in) || !aligned4(out)) return AP_ERR_ALIGN;
+    if (in != out && overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    OpArgs op{OP_SCALE, alpha, 0, nullptr};
+    return launch_ring(di, options(), in, out, n, 0, tile_elems, stages, op, stream);
+}
+
+ap_status ap_scale_sync(const float* in, float* out, int64_t n_tiles, int64_t tile_elems, float alpha,
+                        cudaStream_t stream) {
+    if (n_tiles < 0 || tile_elems < 1) return AP_ERR_SHAPE;
+    if (n_tiles > 0 && tile_elems > kMaxElems / n_tiles) return AP_ERR_SHAPE;
+    const int64_t n = n_tiles * tile_elems;
+    if (n == 0) return AP_OK;
+    if (in == nullptr || out == nullptr) return AP_ERR_NULL;
+    if (!aligned4(in) || !aligned4(out)) return AP_ERR_ALIGN;
+    if (in != out && overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    if (4 * tile_elems > kSmemOptinGB300) return AP_ERR_SMEM;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    return launch_scale_sync(di, in, out, n_tiles, tile_elems, alpha, stream);
+}
+
+ap_status ap_row_roll(const float* A, float* B, int64_t rows, int64_t cols, int64_t shift, cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return AP_ERR_SHAPE;
+    if (rows > 0 && cols > kMaxElems / rows) return AP_ERR_SHAPE;
+    const int64_t n = rows * cols;
+    if (n == 0) return AP_OK;
+    if (A == nullptr || B == nullptr) return AP_ERR_NULL;
+    if (!aligned4(A) || !aligned4(B)) return AP_ERR_ALIGN;
+    if (overlap(A, 4 * n, B, 4 * n)) return AP_ERR_ALIAS;
+    const Options o = options();
+    const int stages = o.roll_stages > 0 ? static_cast<int>(o.roll_stages) : 4;
+    if (!valid_stages(stages)) return AP_ERR_STAGES;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    const int64_t s = ((shift % rows) + rows) % rows;
+    const bool small = 4 * n <= kRollSmallMaxBytes;
+    if ((small && o.force_path != 1) || (o.force_path == 2 && small)) {
+        return launch_roll_small(di, A, B, rows, cols, s, stream);
+    }
+    OpArgs op{OP_COPY, 1.0f, 0, nullptr};
+    return launch_ring(di, o, A, B, n, s * cols, cols, stages, op, stream);
+}
+
+ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, int degree, int stages,
+                  cudaStream_t stream) {
+    if (!valid_stages(stages)) return AP_ERR_STAGES;
+    if (degree < 0 || degree > AP_POLY_MAX_DEGREE) return AP_ERR_ARG;
+    if (n < 0 || n > kMaxElems) return AP_ERR_SHAPE;
+    if (n == 0) return AP_OK;
+    if (in == nullptr || out == nullptr || coeffs == nullptr) return AP_ERR_NULL;
+    if (!aligned4(in) || !aligned4(out)) return AP_ERR_ALIGN;
+    if (in != out && overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    OpArgs op{OP_POLY, 0.0f, degree, coeffs};
+    return launch_ring(di, options(), in, out, n, 0, 1, stages, op, stream);
+}
+
+ap_status ap_cluster_exchange(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes,
+                              cudaStream_t stream) {
+    if (cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8) return AP_ERR_CLUSTER;
+    if (chunk_bytes < 16 || chunk_bytes % 16 != 0) return AP_ERR_SHAPE;
+    if (2 * chunk_bytes + 256 > kSmemOptinGB300) return AP_ERR_SMEM;
+    if (n < 0 || n > kMaxElems) return AP_ERR_SHAPE;
+    if ((4 * n) % (static_cast<int64_t>(cluster_size) * chunk_bytes) != 0) return AP_ERR_SHAPE;
+    if (n == 0) return AP_OK;
+    if (in == nullptr || out == nullptr) return AP_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return AP_ERR_ALIGN;
+    if (overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    return launch_exchange(di, options(), in, out, n, cluster_size, chunk_bytes, stream);
+}
+
+ap_status ap_check(cudaStream_t stream) {
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return AP_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, di.status, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return AP_ERR_CUDA;
+    if (cudaMemsetAsync(di.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return AP_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return AP_ERR_CUDA;
+    if (word == 0) return AP_OK;
+    return static_cast<ap_status>(word & 0xff);
+}
+
+ap_status ap_debug_set(int key, int64_t value) {
+    if (value < 0) return AP_ERR_ARG;
+    switch (key) {
+        case AP_DBG_FORCE_PATH:
+            if (value > 2) return AP_ERR_ARG;
+            g_force_path = value;
+            return AP_OK;
+        case AP_DBG_EXPECT_TX_EXTRA:
+            if (value > 4096) return AP_ERR_ARG;
+            g_tx_extra = value;
+            return AP_OK;
+        case AP_DBG_TIMEOUT_NS: g_timeout_ns = value; return AP_OK;
+        case AP_DBG_STAGE_BYTES:
+            if (value != 0 && (value < 16 || value > 200 * 1024)) return AP_ERR_ARG;
+            g_stage_bytes = value;
+            return AP_OK;
+        case AP_DBG_GRID: g_grid = value; return AP_OK;
+        case AP_DBG_CTAS_PER_SM:
+            if (value > 8) return AP_ERR_ARG;
+            g_ctas_per_sm = value;
+            return AP_OK;
+        case AP_DBG_ROLL_STAGES:
+            if (value != 0 && !valid_stages(static_cast<int>(value))) return AP_ERR_ARG;
+            g_roll_stages = value;
+            return AP_OK;
+        default: return AP_ERR_ARG;
+    }
+}
+
+int64_t ap_debug_get(int key) {
+    const Options o = options();
+    switch (key) {
+        case AP_DBG_FORCE_PATH: return o.force_path;
+        case AP_DBG_EXPECT_TX_EXTRA: return o.tx_extra;
+        case AP_DBG_TIMEOUT_NS: return o.timeout_ns;
+        case AP_DBG_STAGE_BYTES: return o.stage_bytes;
+        case AP_DBG_GRID: return o.grid;
+        case AP_DBG_CTAS_PER_SM: return o.ctas_per_sm;
+        case AP_DBG_ROLL_STAGES: return o.roll_stages;
+        case AP_DBG_LAST_PATH: return g_last_path.load();
+        case AP_DBG_LAST_GRID: return g_last_grid.load();
+        case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();
+        case AP_DBG_LAST_SMEM: return g_last_smem.load();
+        case AP_DBG_LAST_STAGES: return g_last_stages.load();
+        case AP_DBG_LAST_FLAGS: return g_last_flags.load();
+        default: return -1;
+    }
+}
+
+// Host emulation of the ring's data movement (see asyncpipe_debug.h). It
+// follows the kernel step by step: the producer's copies into a stage slot,
+// then the consumers' reads and stores, using the same planning functions.
+ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n, int64_t off, int in_mis,
+                                int out_mis, int64_t stage_elems) {
+    if (n < 0 || off < 0 || (n > 0 && off >= n)) return AP_ERR_SHAPE;
+    if (in_mis < 0 || in_mis > 12 || in_mis % 4 || out_mis < 0 || out_mis > 12 || out_mis % 4) return AP_ERR_ALIGN;
+    if (stage_elems < 4 || stage_elems % 4) return AP_ERR_SHAPE;
+    if (n == 0) return AP_OK;
+    if (in_host == nullptr || out_host == nullptr) return AP_ERR_NULL;
+    // Pretend device addresses with the requested low bits.
+    const uint64_t in_addr = (uint64_t(1) << 40) + static_cast<uint64_t>(in_mis);
+    const uint64_t out_addr = (uint64_t(3) << 40) + static_cast<uint64_t>(out_mis);
+    StreamGeom g;
+    make_geom(&g, in_addr, out_addr, n, off, stage_elems);
+    const uint64_t in_end = in_addr + 4 * static_cast<uint64_t>(n);
+    unsigned char* slot = static_cast<unsigned char*>(std::malloc(g.slot_bytes));
+    unsigned char* written = static_cast<unsigned char*>(std::malloc(g.slot_bytes));
+    unsigned char* out_done = static_cast<unsigned char*>(std::calloc(static_cast<size_t>(n), 1));
+    if (!slot || !written || !out_done) {
+        std::free(slot);
+        std::free(written);
+        std::free(out_done);
+        return AP_ERR_SHAPE;
+    }
+    const unsigned char* src_bytes = reinterpret_cast<const unsigned char*>(in_host);
+    ap_status result = AP_OK;
+    auto fail = [&]() { result = AP_ERR_SHAPE; };
+    // copy global [ga, ga + bytes) into slot [dst, dst + bytes)
+    auto gcopy = [&](uint32_t dst, uint64_t ga, uint32_t bytes, uint32_t src_valid) {
+        if (ga < in_addr || ga + src_valid > in_end || dst + bytes > g.slot_bytes) return fail();
+        for (uint32_t b = 0; b < bytes; ++b) {
+            slot[dst + b] = b < src_valid ? src_bytes[ga - in_addr + b] : 0;
+            written[dst + b] = 1;
+        }
+    };
+    for (int64_t j = 0; j < g.n_stages && result == AP_OK; ++j) {
+        std::memset(slot, 0xA5, g.slot_bytes);
+        std::memset(written, 0, g.slot_bytes);
+        StagePlan sp;
+        plan_stage(g, j, &sp);
+        for (int k = 0; k < sp.nspans && result == AP_OK; ++k) {
+            const Span& sn = sp.span[k];
+            for (int64_t x = sn.x0; x < sn.head_end; ++x)
+                gcopy(sn.region + sn.lead + static_cast<uint32_t>(4 * (x - sn.x0)), in_addr + 4 * x, 4, 4);
+            if (sn.tail_begin < sn.x1) {
+                if (sn.tail_dst % 16) fail();
+                gcopy(sn.tail_dst, in_addr + 4 * g.t_in, 16, static_cast<uint32_t>(4 * (n - g.t_in)));
+            }
+            if (sn.bulk_bytes) {
+                if (sn.bulk_src % 16 || sn.bulk_dst % 16 || sn.bulk_bytes % 16) fail();
+                gcopy(sn.bulk_dst, sn.bulk_src, sn.bulk_bytes, sn.bulk_bytes);
+            }
+        }
+        if (result != AP_OK) break;
+        auto read = [&](int64_t e) -> float {
+            const uint32_t o = smem_offset_of_output(sp, e);
+            float v = 0.0f;
+            if (o + 4 > g.slot_bytes || !written[o] || !written[o + 3]) {
+                fail();
+                return v;
+            }
+            std::memcpy(&v, slot + o, 4);
+            return v;
+        };
+        auto store = [&](int64_t e, float v) {
+            if (e < 0 || e >= n || out_done[e]) return fail();
+            out_done[e] = 1;
+            out_host[e] = v;
+        };
+        const int64_t ngroups = (sp.e_end - sp.e_al) >> 2;
+        for (int64_t q = 0; q < ngroups && result == AP_OK; ++q) {
+            const int64_t e = sp.e_al + 4 * q;
+            if ((out_addr + 4 * static_cast<uint64_t>(e)) % 16) fail();
+            if (sp.vec) {
+                const uint32_t o = sp.span[0].region + sp.span[0].lead + static_cast<uint32_t>(4 * (e - sp.lo));
+                if (o % 16 || o != smem_offset_of_output(sp, e)) fail();
+            }
+            for (int t = 0; t < 4; ++t) store(e + t, read(e + t));
+        }
+        for (int64_t e = sp.lo; e < sp.e_al; ++e) store(e, read(e));
+        for (int64_t e = sp.e_end; e < sp.hi; ++e) store(e, read(e));
+        if (sp.e_al - sp.lo > 3 || sp.hi - sp.e_end > 3) fail();  // the kernel handles <= 3 + 3 scalars
+    }
+    for (int64_t e = 0; e < n && result == AP_OK; ++e)
+        if (!out_done[e]) fail();
+    std::free(slot);
+    std::free(written);
+    std::free(out_done);
+    return result;
+}
+
+}  // extern "C"

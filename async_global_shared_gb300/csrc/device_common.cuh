@@ -1,0 +1,54 @@
+// Bounded waits and the device status word shared by every kernel.
+//
+// No kernel of this library waits without a limit. A wait that runs past its
+// limit records AP_ERR_DEVICE_TIMEOUT and the site that gave up in the status
+// word (first error wins), raises the CTA's abort flag so the other roles stop
+// too, and returns false; the kernel then drains the copies it issued (again
+// with a limit) and returns normally. No trap, no assert, no endless loop.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace ap {
+
+// Status word layout: bits 0..7 the ap_status code, bits 8..15 the site.
+enum WaitSite : uint32_t {
+    SITE_RING_PRODUCER_EMPTY = 1,
+    SITE_RING_CONSUMER_FULL = 2,
+    SITE_RING_DRAIN = 3,
+    SITE_EX_LOADER_CREDIT = 4,
+    SITE_EX_PUSHER_LOADED = 5,
+    SITE_EX_RECEIVER_FULL = 6,
+    SITE_EX_DRAIN = 7,
+};
+
+constexpr uint32_t kStatusTimeout = 9;  // AP_ERR_DEVICE_TIMEOUT
+
+__device__ __forceinline__ void raise_timeout(uint32_t* status, uint32_t site, volatile int* abort_flag) {
+    atomicCAS(status, 0u, kStatusTimeout | (site << 8));
+    if (abort_flag) *abort_flag = 1;
+}
+
+enum WaitResult : int { WAIT_OK = 0, WAIT_TIMEOUT = 1, WAIT_ABORTED = 2 };
+
+// Wait for the phase with `parity` of the CTA-local barrier `bar`. Gives up
+// with WAIT_TIMEOUT after `timeout_ns`, or with WAIT_ABORTED as soon as the
+// CTA's abort flag is set (pass nullptr to ignore the flag, as drains do).
+template <bool kClusterScope>
+__device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                          volatile int* abort_flag) {
+    auto probe = [&]() {
+        return kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (probe()) return WAIT_OK;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (probe()) return WAIT_OK;
+        if (abort_flag != nullptr && *abort_flag) return WAIT_ABORTED;
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) return WAIT_TIMEOUT;
+    }
+}
+
+}  // namespace ap

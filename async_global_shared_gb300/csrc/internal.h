@@ -1,0 +1,73 @@
+// Host-side interfaces between the C-ABI entry points (api.cu) and the
+// per-kernel launchers (one translation unit per kernel family).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "asyncpipe.h"
+#include "asyncpipe_debug.h"
+#include "stream_plan.h"
+
+namespace ap {
+
+// Per-device facts, looked up once per device.
+struct DeviceInfo {
+    int device;
+    int sms;                 // streaming multiprocessors
+    int smem_optin;          // max dynamic shared memory per CTA (opt-in), bytes
+    uint32_t* status;        // device address of this device's status word
+};
+
+// Snapshot of the process-wide tuning / fault-injection settings.
+struct Options {
+    int64_t force_path;
+    int64_t tx_extra;
+    int64_t timeout_ns;
+    int64_t stage_bytes;
+    int64_t grid;
+    int64_t ctas_per_sm;
+    int64_t roll_stages;
+};
+
+Options options();
+
+// What a launcher reports about the launch it made (AP_DBG_LAST_*).
+void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem, int64_t stages, int64_t flags);
+
+enum Path : int64_t { PATH_RING = 1, PATH_ROLL_SMALL = 2, PATH_SYNC = 3, PATH_EXCHANGE = 4 };
+
+// Arguments of the per-element compute of a ring call.
+enum OpKind { OP_COPY, OP_SCALE, OP_POLY };
+struct OpArgs {
+    OpKind kind;
+    float alpha;
+    int degree;
+    const float* coeffs;  // host, degree + 1
+};
+
+// Ring stage elements for a payload of `payload_bytes`, a multiple of
+// lcm(4, unit) when that fits (so a stage holds whole tiles / rows).
+int64_t stage_elems_for(int64_t payload_bytes, int64_t unit);
+
+// Default stage payload for a ring of `stages` slots.
+int64_t auto_stage_payload(int stages);
+
+ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
+                      int64_t unit, int stages, const OpArgs& op, cudaStream_t stream);
+
+ap_status launch_roll_small(const DeviceInfo& di, const float* A, float* B, int64_t rows, int64_t cols, int64_t s,
+                            cudaStream_t stream);
+
+ap_status launch_scale_sync(const DeviceInfo& di, const float* in, float* out, int64_t n_tiles, int64_t tile,
+                            float alpha, cudaStream_t stream);
+
+ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
+                          int64_t chunk_bytes, cudaStream_t stream);
+
+// Largest chunk accepted by ap_cluster_exchange for this much shared memory.
+constexpr int64_t kSmemOptinGB300 = 232448;  // 227 KiB per CTA on compute capability 10.x
+constexpr int64_t kRollSmallMaxBytes = 32 * 1024;
+
+}  // namespace ap

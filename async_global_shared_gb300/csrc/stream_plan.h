@@ -1,0 +1,177 @@
+// Tile planning for the streaming ring, shared by the kernels, the host
+// launchers and the host emulator (ap_debug_emulate_ring).
+//
+// Every ring call computes out[e] = f(in[(e + off) mod n]) for e in [0, n):
+// off = 0 for scale and polynomial, off = shift * cols for the row shift of a
+// row-major matrix (a shift by whole rows is a rotation of the flat array).
+//
+// Output tiles ("stages"). Output element e belongs to stage j when
+//   j == 0: e in [0, out_head + se)          j >= 1: e in [out_head + j*se, out_head + (j+1)*se)
+// (clipped to n), where out_head (0..3) counts the outputs before the first
+// 16-byte aligned output address and se is a multiple of 4. So every stage
+// after the first starts on a 16-byte boundary of `out`, and a stage's
+// outputs are whole 16-byte groups except the first stage's head and the
+// last stage's tail.
+//
+// Input spans. Stage j reads inputs [a, a + L) with a = (lo + off) mod n; if
+// that runs past n it wraps, and the stage has a second span [0, ...). (For
+// the row shift these are the tile's rows shifted by `shift`: its own rows
+// plus the halo rows of the following tile, wrapping to row 0.)
+//
+// Shared-memory layout of a span. A span is placed in its region of the
+// stage slot so that shared-memory addresses are congruent to global
+// addresses modulo 16: input element x sits at
+//   region + (in_addr + 4x) - floor16(in_addr + 4*x0).
+// The span's elements between the buffer's first and last 16-byte boundaries
+// (I0 = ceil16(in_addr), I1 = floor16(in_addr + 4n)) arrive with ONE bulk
+// copy of their 16-byte-aligned enclosing range, which never leaves
+// [I0, I1) and so never leaves the caller's buffer. Elements before I0 (at
+// most 3, only near element 0) use 4-byte cp.async.ca; elements at or after
+// I1 (at most 3, only near element n-1) use one 16-byte cp.async.cg whose
+// source size is the tail's byte count (the rest of the 16 is zero-filled).
+// If the buffer holds no aligned 16-byte block at all, every element is a
+// 4-byte copy.
+#pragma once
+
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define AP_HD __host__ __device__ __forceinline__
+#else
+#define AP_HD inline
+#endif
+
+namespace ap {
+
+AP_HD uint64_t floor16(uint64_t a) { return a & ~uint64_t(15); }
+AP_HD uint64_t ceil16(uint64_t a) { return (a + 15) & ~uint64_t(15); }
+
+struct StreamGeom {
+    uint64_t in_addr;     // byte address of input element 0 (4-byte aligned)
+    uint64_t out_addr;    // byte address of output element 0 (4-byte aligned)
+    int64_t n;            // elements of each buffer (> 0)
+    int64_t off;          // output e reads input (e + off) mod n, 0 <= off < n
+    int64_t se;           // stage elements, a multiple of 4, >= 4
+    int64_t out_head;     // outputs before the first 16-byte aligned output, min(n, 0..3)
+    int64_t n_stages;     // number of stages covering [0, n)
+    int64_t h_in;         // inputs [0, h_in) lie before I0 (4-byte copies)
+    int64_t t_in;         // inputs [t_in, n) lie at or after I1 (one zero-filling 16-byte copy)
+    uint32_t slot_bytes;  // shared-memory bytes of one stage slot (multiple of 16)
+};
+
+// Bytes of a stage slot for stages of `se` elements: two regions, each the
+// span's bytes plus up to 12 bytes of alignment lead and 15 of trailing
+// rounding, each rounded to 16.
+AP_HD uint32_t slot_bytes_for(int64_t se) { return static_cast<uint32_t>(4 * se + 112); }
+
+AP_HD void make_geom(StreamGeom* g, uint64_t in_addr, uint64_t out_addr, int64_t n, int64_t off, int64_t se) {
+    g->in_addr = in_addr;
+    g->out_addr = out_addr;
+    g->n = n;
+    g->off = off;
+    g->se = se;
+    const int64_t oh = static_cast<int64_t>(((16 - (out_addr & 15)) & 15) >> 2);
+    g->out_head = oh < n ? oh : n;
+    if (n <= 0) {
+        g->n_stages = 0;
+    } else if (n <= g->out_head + se) {
+        g->n_stages = 1;
+    } else {
+        g->n_stages = 1 + (n - g->out_head - se + se - 1) / se;
+    }
+    const uint64_t i0 = ceil16(in_addr);
+    const uint64_t i1 = floor16(in_addr + 4 * static_cast<uint64_t>(n));
+    if (i0 <= i1) {
+        g->h_in = static_cast<int64_t>((i0 - in_addr) >> 2);
+        g->t_in = static_cast<int64_t>((i1 - in_addr) >> 2);
+    } else {
+        g->h_in = n;
+        g->t_in = n;
+    }
+    g->slot_bytes = slot_bytes_for(se);
+}
+
+struct Span {
+    int64_t x0, x1;        // input elements [x0, x1)
+    uint32_t region;       // slot-relative byte offset of the span's region (multiple of 16)
+    uint32_t lead;         // (in_addr + 4*x0) mod 16: byte offset of x0 inside the region
+    int64_t head_end;      // [x0, head_end): 4-byte cp.async.ca copies
+    int64_t tail_begin;    // [tail_begin, x1): covered by the buffer-tail cp.async.cg
+    uint32_t tail_dst;     // slot-relative destination of the tail copy (multiple of 16)
+    uint32_t bulk_dst;     // slot-relative destination of the bulk copy (multiple of 16)
+    uint32_t bulk_bytes;   // multiple of 16; 0 when the span has no bulk part
+    uint64_t bulk_src;     // global source of the bulk copy (multiple of 16)
+};
+
+struct StagePlan {
+    int64_t lo, hi;        // outputs [lo, hi)
+    int64_t len1;          // outputs [lo, lo + len1) read span 0, the rest span 1
+    int nspans;            // 1, or 2 when the input wraps past n
+    Span span[2];
+    int64_t e_al, e_end;   // outputs [e_al, e_end) are whole 16-byte aligned groups
+    bool vec;              // each group's 4 inputs form one aligned 16-byte word in shared memory
+};
+
+AP_HD void plan_span(const StreamGeom& g, int64_t x0, int64_t x1, uint32_t region, Span* s) {
+    s->x0 = x0;
+    s->x1 = x1;
+    s->region = region;
+    const uint64_t g0 = g.in_addr + 4 * static_cast<uint64_t>(x0);
+    const uint64_t a0 = floor16(g0);
+    s->lead = static_cast<uint32_t>(g0 - a0);
+    const int64_t hb = (x0 < g.h_in) ? (x1 < g.h_in ? x1 : g.h_in) : x0;
+    const int64_t tb = (x1 > g.t_in) ? (x0 > g.t_in ? x0 : g.t_in) : x1;
+    s->head_end = hb;
+    s->tail_begin = tb;
+    const uint64_t i1 = g.in_addr + 4 * static_cast<uint64_t>(g.t_in);
+    s->tail_dst = (tb < x1) ? region + static_cast<uint32_t>(i1 - a0) : 0u;
+    if (tb > hb) {
+        const uint64_t b0 = floor16(g.in_addr + 4 * static_cast<uint64_t>(hb));
+        const uint64_t b1 = ceil16(g.in_addr + 4 * static_cast<uint64_t>(tb));
+        s->bulk_src = b0;
+        s->bulk_dst = region + static_cast<uint32_t>(b0 - a0);
+        s->bulk_bytes = static_cast<uint32_t>(b1 - b0);
+    } else {
+        s->bulk_src = 0;
+        s->bulk_dst = 0;
+        s->bulk_bytes = 0;
+    }
+}
+
+AP_HD int64_t stage_lo(const StreamGeom& g, int64_t j) { return j == 0 ? 0 : g.out_head + j * g.se; }
+
+AP_HD void plan_stage(const StreamGeom& g, int64_t j, StagePlan* p) {
+    const int64_t lo = stage_lo(g, j);
+    int64_t hi = g.out_head + (j + 1) * g.se;
+    if (hi > g.n) hi = g.n;
+    p->lo = lo;
+    p->hi = hi;
+    const int64_t L = hi - lo;
+    int64_t a = lo + g.off;
+    if (a >= g.n) a -= g.n;
+    int64_t len1 = g.n - a;
+    if (len1 > L) len1 = L;
+    p->len1 = len1;
+    plan_span(g, a, a + len1, 0u, &p->span[0]);
+    if (len1 < L) {
+        p->nspans = 2;
+        const uint32_t r2 = static_cast<uint32_t>((4 * len1 + 32 + 15) & ~int64_t(15));
+        plan_span(g, 0, L - len1, r2, &p->span[1]);
+    } else {
+        p->nspans = 1;
+    }
+    int64_t e_al = lo > g.out_head ? lo : g.out_head;
+    if (e_al > hi) e_al = hi;
+    p->e_al = e_al;
+    p->e_end = e_al + ((hi - e_al) & ~int64_t(3));
+    p->vec = (p->nspans == 1) && (((p->span[0].lead + 4 * (e_al - lo)) & 15) == 0);
+}
+
+// Slot-relative shared-memory byte offset of the input that output e reads.
+AP_HD uint32_t smem_offset_of_output(const StagePlan& p, int64_t e) {
+    const int64_t q = e - p.lo;
+    if (q < p.len1) return p.span[0].region + p.span[0].lead + static_cast<uint32_t>(4 * q);
+    return p.span[1].region + p.span[1].lead + static_cast<uint32_t>(4 * (q - p.len1));
+}
+
+}  // namespace ap

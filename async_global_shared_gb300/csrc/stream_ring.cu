@@ -1,0 +1,329 @@
+// The streaming ring: a persistent, warp-specialised kernel in which one
+// producer thread keeps up to S stages of input in flight with bulk
+// asynchronous copies while eight consumer warps compute on the oldest
+// landed stage and store it.
+//
+// Protocol per ring slot s (two mbarriers, "Asynchronous Data Movement",
+// section Barriers and pipelines: acquire, commit, wait, release):
+//   producer: wait empty[s]            (acquire: the slot's previous tile is consumed)
+//             cp.async edge copies, cp.async.mbarrier.arrive(full[s])
+//             arrive.expect_tx(full[s], bulk bytes) + cp.async.bulk into the slot
+//                                      (commit: the barrier now tracks the copies)
+//   consumer: wait full[s]             (wait: every byte of the tile has landed)
+//             ld.shared -> compute -> 16-byte st.global
+//             arrive empty[s]          (release)
+// The producer runs up to S tiles ahead, so the load of tile t+1 overlaps the
+// compute and store of tile t ("Asynchronous Data Movement", section Double
+// buffering; "CUDA Async Copy and Pipeline Guide", section Implementation
+// Comparison, "After" kernel).
+//
+// GB300 choices that differ from the pages' 256-float, one-block sketch:
+// a stage holds tens of KiB (many of the pages' tiles) so that each SM keeps
+// enough bytes in flight to cover HBM latency; the grid is persistent (one
+// CTA per SM, CTA b takes tiles b, b + grid, ...); the copy is a single
+// bulk-copy instruction per tile issued by one thread (the TMA engine
+// generates the addresses, "Asynchronous Data Movement", section The Tensor
+// Memory Accelerator) instead of every thread copying a few bytes.
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace ap {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = 32 + kConsumers;
+constexpr int kUnroll = 4;  // 16-byte groups per consumer thread per iteration
+
+struct OpCopyDev {
+    template <int N>
+    __device__ __forceinline__ void apply(float (&)[N]) const {}
+};
+
+struct OpScaleDev {
+    float alpha;
+    template <int N>
+    __device__ __forceinline__ void apply(float (&v)[N]) const {
+#pragma unroll
+        for (int t = 0; t < N; ++t) v[t] = alpha * v[t];
+    }
+};
+
+// Horner's rule, one fmaf per step, N independent chains per thread so the
+// FMA pipe sees N-way instruction-level parallelism.
+struct OpPolyDev {
+    int degree;
+    float c[AP_POLY_MAX_DEGREE + 1];
+    template <int N>
+    __device__ __forceinline__ void apply(float (&v)[N]) const {
+        float p[N];
+        const float top = c[degree];
+#pragma unroll
+        for (int t = 0; t < N; ++t) p[t] = top;
+        for (int k = degree - 1; k >= 0; --k) {
+            const float ck = c[k];
+#pragma unroll
+            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], ck);
+        }
+#pragma unroll
+        for (int t = 0; t < N; ++t) v[t] = p[t];
+    }
+};
+
+template <class Op>
+struct RingParams {
+    const float* in;
+    float* out;
+    StreamGeom g;
+    int stages;
+    uint32_t tx_extra;
+    uint64_t timeout_ns;
+    uint32_t* status;
+    Op op;
+};
+
+__device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off) {
+    return *reinterpret_cast<const float*>(slot + off);
+}
+
+template <class Op>
+__device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const StagePlan& sp, const unsigned char* slot,
+                                              int ct) {
+    const int64_t ngroups = (sp.e_end - sp.e_al) >> 2;
+    float* __restrict__ out = P.out;
+    if (sp.vec) {
+        const float4* src = reinterpret_cast<const float4*>(slot + sp.span[0].region + sp.span[0].lead +
+                                                            4 * (sp.e_al - sp.lo));
+        float4* dst = reinterpret_cast<float4*>(out + sp.e_al);
+        int64_t q = ct;
+        for (; q + (kUnroll - 1) * kConsumers < ngroups; q += kUnroll * kConsumers) {
+            float v[4 * kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const float4 t = src[q + u * kConsumers];
+                v[4 * u + 0] = t.x;
+                v[4 * u + 1] = t.y;
+                v[4 * u + 2] = t.z;
+                v[4 * u + 3] = t.w;
+            }
+            P.op.apply(v);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+        for (; q < ngroups; q += kConsumers) {
+            const float4 t = src[q];
+            float v[4] = {t.x, t.y, t.z, t.w};
+            P.op.apply(v);
+            dst[q] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    } else {
+        for (int64_t q = ct; q < ngroups; q += kConsumers) {
+            const int64_t e = sp.e_al + 4 * q;
+            float v[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) v[t] = lds_f32(slot, smem_offset_of_output(sp, e + t));
+            P.op.apply(v);
+            *reinterpret_cast<float4*>(out + e) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+    // The first stage's unaligned head and the last stage's tail (<= 3 each).
+    const int64_t nh = sp.e_al - sp.lo;
+    const int64_t nt = sp.hi - sp.e_end;
+    if (ct < nh + nt) {
+        const int64_t e = ct < nh ? sp.lo + ct : sp.e_end + (ct - nh);
+        float v[1] = {lds_f32(slot, smem_offset_of_output(sp, e))};
+        P.op.apply(v);
+        out[e] = v[0];
+    }
+}
+
+template <class Op>
+__global__ void __launch_bounds__(kThreads, 1) ring_kernel(const __grid_constant__ RingParams<Op> P) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int S = P.stages;
+    const uint32_t slot_bytes = P.g.slot_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slot_bytes);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S);
+    const uint32_t smem_base = ptx::smem_addr(smem);
+    const uint32_t bar_base = ptx::smem_addr(bars);
+    auto full = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(s); };
+    auto empty = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(S + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(empty(s), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int64_t T = P.g.n_stages;
+    const int64_t G = gridDim.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0) {
+        if (lane != 0) return;
+        // ------------------------------------------------ producer (one thread)
+        int64_t issued = 0;
+        for (int64_t j = blockIdx.x; j < T; j += G, ++issued) {
+            const int s = static_cast<int>(issued % S);
+            const uint32_t ph = static_cast<uint32_t>((issued / S) & 1);
+            const int w = wait_phase<false>(empty(s), ph ^ 1u, P.timeout_ns, abort_flag);
+            if (w != WAIT_OK) {
+                if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_RING_PRODUCER_EMPTY, abort_flag);
+                break;
+            }
+            StagePlan sp;
+            plan_stage(P.g, j, &sp);
+            const uint32_t slot = smem_base + static_cast<uint32_t>(s) * slot_bytes;
+            bool edges = false;
+            uint32_t tx = 0;
+            for (int k = 0; k < sp.nspans; ++k) {
+                const Span& sn = sp.span[k];
+                for (int64_t x = sn.x0; x < sn.head_end; ++x) {
+                    ptx::cp_async_ca4(slot + sn.region + sn.lead + static_cast<uint32_t>(4 * (x - sn.x0)), P.in + x);
+                    edges = true;
+                }
+                if (sn.tail_begin < sn.x1) {
+                    ptx::cp_async_cg16(slot + sn.tail_dst, P.in + P.g.t_in,
+                                       static_cast<uint32_t>(4 * (P.g.n - P.g.t_in)));
+                    edges = true;
+                }
+                tx += sn.bulk_bytes;
+            }
+            if (edges) ptx::cp_async_mbar_arrive(full(s));
+            ptx::mbar_arrive_expect_tx(full(s), tx + P.tx_extra);
+            for (int k = 0; k < sp.nspans; ++k) {
+                const Span& sn = sp.span[k];
+                if (sn.bulk_bytes)
+                    ptx::bulk_g2s(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes,
+                                  full(s));
+            }
+        }
+        // Never leave with copies in flight: wait (bounded) for the last
+        // S tiles issued. Tiles already consumed return at once.
+        for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k) {
+            if (wait_phase<false>(full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1), P.timeout_ns,
+                                  nullptr) != WAIT_OK)
+                raise_timeout(P.status, SITE_RING_DRAIN, abort_flag);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers
+    const int ct = threadIdx.x - 32;
+    int64_t i = 0;
+    for (int64_t j = blockIdx.x; j < T; j += G, ++i) {
+        const int s = static_cast<int>(i % S);
+        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        int w = WAIT_OK;
+        if (lane == 0) {
+            w = wait_phase<false>(full(s), ph, P.timeout_ns, abort_flag);
+            if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_RING_CONSUMER_FULL, abort_flag);
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (w != WAIT_OK) break;
+        __syncwarp();  // orders lane 0's observation of the phase before the other lanes' reads
+        StagePlan sp;
+        plan_stage(P.g, j, &sp);
+        consume_stage(P, sp, smem + static_cast<size_t>(s) * slot_bytes, ct);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty(s));
+    }
+}
+
+template <class Op>
+ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t grid, int64_t smem,
+                         cudaStream_t stream) {
+    // Raise the kernel's dynamic shared-memory limit once per device.
+    static int64_t configured[64] = {0};
+    const int d = di.device;
+    if (d < 0 || d >= 64) return AP_ERR_CUDA;
+    if (configured[d] < smem) {
+        if (cudaFuncSetAttribute(ring_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) !=
+            cudaSuccess)
+            return AP_ERR_CUDA;
+        configured[d] = di.smem_optin;
+    }
+    ring_kernel<Op><<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem), stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
+}
+
+}  // namespace
+
+int64_t stage_elems_for(int64_t payload_bytes, int64_t unit) {
+    int64_t se = payload_bytes / 4;
+    if (se < 4) se = 4;
+    int64_t l = 4;
+    if (unit > 0 && unit <= se) {
+        int64_t a = unit, b = 4;
+        while (b) {
+            const int64_t t = a % b;
+            a = b;
+            b = t;
+        }
+        l = unit / a * 4;  // lcm(unit, 4)
+    }
+    if (l <= se) return se / l * l;
+    return se / 4 * 4;
+}
+
+int64_t auto_stage_payload(int stages) {
+    const int64_t per = (196 * 1024) / stages / 4096 * 4096;
+    return std::min<int64_t>(64 * 1024, per);
+}
+
+ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
+                      int64_t unit, int stages, const OpArgs& op, cudaStream_t stream) {
+    const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : auto_stage_payload(stages);
+    const int64_t se = stage_elems_for(payload, unit);
+    StreamGeom g;
+    make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
+    const int64_t smem = static_cast<int64_t>(stages) * g.slot_bytes + 2 * 8 * stages + 16;
+    if (smem > di.smem_optin) return AP_ERR_SMEM;
+    const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 1;
+    int64_t grid = std::min<int64_t>(g.n_stages, static_cast<int64_t>(di.sms) * cps);
+    if (o.grid > 0) grid = std::min<int64_t>(grid, o.grid);
+    if (grid < 1) grid = 1;
+
+    const uint64_t ia = g.in_addr, oa = g.out_addr;
+    int64_t flags = 0;
+    if (g.h_in > 0 || g.t_in < n) flags |= 1;
+    if (((ia + 4 * static_cast<uint64_t>(off) - oa) & 15) != 0 || off != 0) flags |= 2;
+    record_launch(PATH_RING, grid, se, smem, stages, flags);
+
+    const uint64_t timeout = static_cast<uint64_t>(o.timeout_ns);
+    const uint32_t tx_extra = static_cast<uint32_t>(o.tx_extra);
+    switch (op.kind) {
+        case OP_COPY: {
+            RingParams<OpCopyDev> P{in, out, g, stages, tx_extra, timeout, di.status, OpCopyDev{}};
+            return launch_ring_op(di, P, grid, smem, stream);
+        }
+        case OP_SCALE: {
+            RingParams<OpScaleDev> P{in, out, g, stages, tx_extra, timeout, di.status, OpScaleDev{op.alpha}};
+            return launch_ring_op(di, P, grid, smem, stream);
+        }
+        case OP_POLY: {
+            RingParams<OpPolyDev> P;
+            P.in = in;
+            P.out = out;
+            P.g = g;
+            P.stages = stages;
+            P.tx_extra = tx_extra;
+            P.timeout_ns = timeout;
+            P.status = di.status;
+            P.op.degree = op.degree;
+            for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
+            return launch_ring_op(di, P, grid, smem, stream);
+        }
+    }
+    return AP_ERR_ARG;
+}
+
+}  // namespace ap

@@ -1,0 +1,558 @@
+"""Benchmark of the asynchronous global->shared streaming ring on GB300.
+
+Default workload: the tiled scale y = 2x over 2**20 tiles of 256 float32
+(1 GiB in, 1 GiB out) through the 2-stage ring (ap_scale), the configuration
+the headline metric is quoted on. One step = one ap_scale call over the whole
+input. Prints ONE JSON line (rank 0): achieved HBM GB/s (read + write bytes
+per step / time), the roofline of the ring kernel against the measured copy
+bandwidth, the synchronous baseline kernel on the same input, the oracle timed
+on the host cores, and an end-to-end figure with host buffers.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+    python bench.py --workload all      # one line per workload of the sweep
+
+Under torchrun (N > 1) every rank streams its own 1 GiB shard on its own GPU
+(the operation is elementwise, so shards are independent and no collective
+touches the data); the timing is the max over ranks and the value the bytes
+of all ranks over that time (weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (read+write) and % of GB300 HBM roofline per kernel, 1 GPU"
+GIB = 1 << 30
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1000 * 1000
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def hbm_peak() -> tuple[float, str]:
+    pk = measured_peaks()
+    if "hbm_gbs" in pk:
+        return float(pk["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+RING_SOURCES = ["stream_ring.cu", "stream_plan.h", "ptx.cuh", "device_common.cuh"]
+
+
+def ring_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in RING_SOURCES:
+        with open(os.path.join(ROOT, "async_global_shared_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile: str) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source hash)."""
+    p = os.path.join(ROOT, "profiles", profile)
+    try:
+        text = open(p).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"^source_hash:\s*(\w+)", text, re.M)
+    m_tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not m_hash or not m_tr or m_hash.group(1) != ring_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = (
+        "timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+        "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+    )
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict | None:
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return None
+        lo = self.t0 - datetime.timedelta(seconds=0.06)
+        hi = self.t1 + datetime.timedelta(seconds=0.06)
+        inside = [r for r in rows if lo <= r[0] <= hi]
+        if not inside:  # timed region shorter than the sampling period: nearest sample
+            mid = self.t0 + (self.t1 - self.t0) / 2
+            inside = [min(rows, key=lambda r: abs((r[0] - mid).total_seconds()))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        mhz = sorted(r[1] for r in inside)
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def time_steps(fn, steps: int, warmup: int, stream, dist_ctx=None) -> float:
+    """Milliseconds for `steps` calls of fn(), CUDA events on `stream`, after
+    `warmup` untimed calls; barrier + synchronize on both sides."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist_ctx:
+        dist_ctx.barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist_ctx:
+        dist_ctx.barrier()
+    return start.elapsed_time(end)
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if self.pg.get_backend() == "nccl":
+                import torch
+
+                self.pg.barrier(device_ids=[torch.cuda.current_device()])
+            else:
+                self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU baseline)
+
+
+def oracle_scale_rate(x_host, alpha: float, min_seconds: float, max_passes: int) -> tuple[float, int, float]:
+    """Bytes/s of the oracle's scale over x_host, passes until min_seconds."""
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.load()
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        orc.scale(x_host, alpha)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= max_passes:
+            break
+    return 8.0 * x_host.size * passes / el, passes, el
+
+
+# ----------------------------------------------------------------------------- workloads
+
+SCALE_TILES = 1 << 20
+SCALE_TILE = 256
+
+
+def bench_scale(args, d: Dist) -> dict:
+    import numpy as np
+    import torch
+
+    import async_global_shared_gb300 as ap
+    import synth
+
+    dev = torch.device("cuda", d.local)
+    torch.cuda.set_device(dev)
+    n = SCALE_TILES * SCALE_TILE
+    nbytes = 8 * n
+    x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    assert ap.ap_check() == 0
+
+    ring = lambda: ap.ap_scale(x, y, SCALE_TILES, SCALE_TILE, 2.0, 2, stream)  # noqa: E731
+    sync = lambda: ap.ap_scale_sync(x, y, SCALE_TILES, SCALE_TILE, 2.0, stream)  # noqa: E731
+
+    with ClockSampler(d.local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        for _ in range(args.warmup):
+            ring()
+        torch.cuda.synchronize()
+        clk.mark_start()
+        ms = time_steps(ring, args.steps, 0, stream, d)
+        clk.mark_end()
+    clocks = clk.summary()
+    status = ap.ap_check()
+    if status != 0:
+        raise RuntimeError(f"device status {ap.ap_status_string(status)}")
+    grid = ap.ap_debug_get(ap.AP_DBG_LAST_GRID)
+    stage_elems = ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS)
+    ms = d.max(ms)
+    ms_step = ms / args.steps
+
+    ms_sync = d.max(time_steps(sync, args.steps, args.warmup, stream, d)) / args.steps
+    assert ap.ap_check() == 0
+
+    # end to end: pinned host input -> device -> ap_scale -> pinned host output, every step
+    xh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    xh.copy_(x)
+    yh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    xd = torch.empty_like(x)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        ap.ap_scale(xd, y, SCALE_TILES, SCALE_TILE, 2.0, 2, stream)
+        yh.copy_(y, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    ms_e2e = d.max(time_steps(e2e_step, e2e_steps, args.warmup, stream, d)) / e2e_steps
+    assert ap.ap_check() == 0
+    if not torch.equal(yh[:4096], (xh[:4096] * 2.0)):
+        raise RuntimeError("end-to-end output check failed")
+
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (ms_step * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(d.world * nbytes / (ms_step * 1e-3) / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": d.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "tiled scale y=2.0*x, 2^20 tiles x 256 fp32 (1 GiB in + 1 GiB out), 2-stage ring (ap_scale)",
+            "n_tiles": SCALE_TILES,
+            "tile_elems": SCALE_TILE,
+            "alpha": 2.0,
+            "stages": 2,
+            "stage_elems": stage_elems,
+            "grid": grid,
+            "input": "seeded uniform[-1,1) 24-bit grid, splitmix64",
+            "l2": "inputs larger than L2 (1 GiB read + 1 GiB written per step vs 129 MB L2), no flush",
+            "parallelism": f"{d.world} independent shard(s), no collective",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_kind": f"{peak_kind} copy bandwidth",
+            "traffic": profiled_traffic("ring_scale_2p28.txt"),
+            "kernel": "ring_kernel<OpScaleDev>",
+            "algorithmic_bytes_per_launch": nbytes,
+        },
+        "baseline_sync": {
+            "kernel": "scale_sync_kernel (load -> __syncthreads -> compute -> __syncthreads -> store)",
+            "value": round(nbytes / (ms_sync * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "ms_per_step": round(ms_sync, 5),
+        },
+        "e2e": {
+            "value": round(d.world * nbytes / (ms_e2e * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": 4 * n,
+            "d2h_bytes_per_step": 4 * n,
+            "steps": e2e_steps,
+            "ms_per_step": round(ms_e2e, 4),
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
+        import numpy as np  # noqa: F811
+
+        x_host = x.cpu().numpy()
+        rate, passes, el = oracle_scale_rate(x_host, 2.0, 10.0, 40)
+        res["cpu_baseline"] = {
+            "value": round(rate / 1e9, 3),
+            "unit": "GB/s",
+            "cores": 1,
+            "kind": "oracle",
+            "sample": f"{passes} full passes of the oracle's scale over the 2^28-float input ({el:.1f} s, 1 thread)",
+        }
+    return res
+
+
+def run_reference(args, d: Dist):
+    """The CPU oracle, as it stands, on the same workload and metric."""
+    if d.rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth
+
+    sample = 1 << 24  # 1/16 of the 2^28-float workload per step
+    x = synth.uniform_pm1_np(synth.SEED_SCALE, sample)
+    orc = oracle.load()
+    for _ in range(args.warmup):
+        orc.scale(x, 2.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.scale(x, 2.0)
+    el = time.perf_counter() - t0
+    gbs = 8.0 * sample * args.steps / el / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(gbs, 3),
+        "unit": "GB/s",
+        "n_gpus": d.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "tiled scale y=2.0*x, 2^20 tiles x 256 fp32 (1 GiB in + 1 GiB out), 2-stage ring (ap_scale)",
+            "n_tiles": SCALE_TILES,
+            "tile_elems": SCALE_TILE,
+            "alpha": 2.0,
+        },
+        "cpu_baseline": {
+            "value": round(gbs, 3),
+            "unit": "GB/s",
+            "cores": 1,
+            "kind": "oracle",
+            "sample": "each step: the oracle's scale over the first 2^24 floats (1/16) of the workload, 1 thread",
+        },
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- sweep (per-kernel lines)
+
+
+def _gbs(nbytes: float, ms: float) -> float:
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def sweep(which: str, args):
+    """One line per (kernel, configuration): GB/s from CUDA events over
+    `steps` launches and the fraction of the measured copy bandwidth. Also the
+    FP32 rate of the polynomial for the compute-bound degrees."""
+    import torch
+
+    import async_global_shared_gb300 as ap
+    import synth
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peak, _ = hbm_peak()
+    steps, warm = max(5, min(args.steps, 50)), args.warmup
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = ["scale", "poly", "roll", "exchange", "small"] if which == "all" else which.split(",")
+
+    def line(workload, kernel, nbytes, ms, **extra):
+        gb = _gbs(nbytes, ms)
+        d = {"workload": workload, "kernel": kernel, "ms": round(ms, 5), "GB/s": round(gb, 1),
+             "frac_of_measured_hbm": round(gb / peak, 4)}
+        d.update(extra)
+        if ap.ap_check() != 0:
+            d["device_status"] = "error"
+        return d
+
+    def run(fn):
+        return time_steps(fn, steps, warm, stream) / steps
+
+    if "scale" in groups or "tune" in groups:
+        n_t, t = SCALE_TILES, SCALE_TILE
+        n = n_t * t
+        x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
+        y = torch.empty_like(x)
+        if "scale" in groups:
+            yield line("scale 2^28 f32", "scale_sync", 8 * n, run(lambda: ap.ap_scale_sync(x, y, n_t, t, 2.0)))
+            for S in (2, 3, 4, 5, 6):
+                ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
+                yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
+                           stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
+                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+        if "tune" in groups:
+            for S in (2, 4):
+                for cps in (1, 2):
+                    for kib in (8, 16, 32, 48, 64, 96):
+                        if S * (kib * 1024 + 112) * cps > 228 * 1024:
+                            continue
+                        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                        ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
+                        yield line("scale 2^28 f32", f"ring S={S} stage={kib}KiB ctas/SM={cps}", 8 * n, ms)
+            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
+        del x, y
+    if "poly" in groups:
+        n = 1 << 30
+        x = synth.uniform_pm1_torch(synth.SEED_POLY, n, dev)
+        y = torch.empty_like(x)
+        for K in (0, 8, 32, 128):
+            c = synth.coeffs_np(K).tolist()
+            for S in (2, 3, 4, 6):
+                ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
+                tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
+                yield line("poly 2^30 f32", f"ring S={S} K={K}", 8 * n, ms, fp32_tflops=round(tflops, 2),
+                           fma_per_elem=K)
+        del x, y
+    if "roll" in groups:
+        rows, cols = 1 << 26, 4
+        n = rows * cols
+        abuf = torch.empty(n + 4, dtype=torch.float32, device=dev)
+        bbuf = torch.empty(n + 4, dtype=torch.float32, device=dev)
+        synth.uniform_pm1_torch(synth.SEED_ROLL, n + 4, dev, out=abuf)
+        for name, sa, sb in (("aligned", 0, 0), ("A+4B", 1, 0), ("B+4B", 0, 1), ("A+4B,B+4B", 1, 1)):
+            A, B = abuf[sa:sa + n], bbuf[sb:sb + n]
+            ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
+            yield line("roll 2^26x4 f32", f"ring {name}", 8 * n, ms, flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
+        del abuf, bbuf
+    if "exchange" in groups:
+        n = 1 << 28
+        x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
+        y = torch.empty_like(x)
+        for cs in (1, 2, 4, 8):
+            ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
+            yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster cs={cs}", 8 * n, ms,
+                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        del x, y
+    if "small" in groups:
+        A = torch.arange(256, dtype=torch.float32, device=dev).reshape(64, 4)
+        B = torch.empty_like(A)
+        ms = run(lambda: ap.ap_row_roll(A, B, 64, 4, 1))
+        yield {"workload": "roll 64x4 f32 (one CTA, 64 threads)", "kernel": "roll_small",
+               "us_per_call": round(ms * 1e3, 2), "note": "launch-latency bound; no roofline"}
+    yield {"workload": "device", "sms": sms, "hbm_peak_gbs": peak}
+
+
+def main(argv=None):
+    ap_ = argparse.ArgumentParser()
+    ap_.add_argument("--gpus", type=int, default=1)
+    ap_.add_argument("--steps", type=int, default=1000)
+    ap_.add_argument("--warmup", type=int, default=5)
+    ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap_.add_argument("--workload", default="scale")
+    ap_.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap_.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    d = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, d)
+            return
+        import __graft_entry__
+
+        __graft_entry__.build()
+        if args.workload == "scale":
+            res = bench_scale(args, d)
+            if d.rank == 0:
+                print(json.dumps(res), flush=True)
+        elif d.rank == 0:
+            for line in sweep(args.workload, args):
+                print(json.dumps(line), flush=True)
+    finally:
+        d.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,73 @@
+/*
+ * libasyncpipe tuning, fault-injection and inspection hooks.
+ *
+ * None of these is needed to use the library; they exist for tests and for
+ * measuring the ring at other stage sizes. The pages define no API, so these
+ * calls cite no passage. Settings are process-wide, apply to calls made
+ * after they are set, and are read without locking (set them before
+ * launching work from several threads).
+ */
+#ifndef ASYNCPIPE_DEBUG_H
+#define ASYNCPIPE_DEBUG_H
+
+#include <stdint.h>
+
+#include "asyncpipe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ap_debug_key {
+    /* settable */
+    AP_DBG_FORCE_PATH = 1,      /* 0 auto; 1 always the ring (also for small row shifts);
+                                   2 small one-CTA row shift when it fits */
+    AP_DBG_EXPECT_TX_EXTRA = 2, /* bytes added to every stage's expected transaction count:
+                                   the barrier then never completes and the consumers' bounded
+                                   waits give up (fault injection; 0 = off) */
+    AP_DBG_TIMEOUT_NS = 3,      /* limit of every kernel wait in ns (0 = default 2 s, or the
+                                   AP_WAIT_TIMEOUT_NS environment variable) */
+    AP_DBG_STAGE_BYTES = 4,     /* ring stage payload in bytes (0 = automatic) */
+    AP_DBG_GRID = 5,            /* cap on the number of CTAs of ring kernels (0 = automatic) */
+    AP_DBG_CTAS_PER_SM = 6,     /* resident ring CTAs per SM the grid is sized for (0 = 1) */
+    AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 4) */
+    /* read-only: what the last call on this process launched */
+    AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange */
+    AP_DBG_LAST_GRID = 101,     /* CTAs launched */
+    AP_DBG_LAST_STAGE_ELEMS = 102, /* elements per ring stage (chunk elements for exchange) */
+    AP_DBG_LAST_SMEM = 103,     /* dynamic shared memory per CTA, bytes */
+    AP_DBG_LAST_STAGES = 104,   /* ring depth */
+    AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
+                                   or unaligned tail); bit 1: some stage used the scalar
+                                   shared-memory path (input/output alignments differ or wrap) */
+} ap_debug_key;
+
+/* Set a settable key. AP_ERR_ARG for an unknown key or a negative value. */
+ap_status ap_debug_set(int key, int64_t value);
+
+/* Read any key; -1 for an unknown key. */
+int64_t ap_debug_get(int key);
+
+/*
+ * Host emulation of one ring call's data movement, for checking the
+ * kernel's index arithmetic without a GPU. It runs the same tile planning
+ * code the kernel runs (stage ranges, bulk spans, cp.async edges, shared
+ * memory offsets) on host arrays that stand for device buffers located at
+ * byte addresses whose low four bits are in_mis and out_mis, and performs
+ * out[e] = in[(e + off) mod n]. It checks every bulk copy (16-byte aligned
+ * source and destination, size a multiple of 16, inside the input), every
+ * cp.async edge copy, every shared-memory access (inside its stage slot) and
+ * every vector store (16-byte aligned), and returns AP_ERR_SHAPE at the
+ * first violation, AP_OK otherwise.
+ *  in_host, out_host  n floats each (host memory).
+ *  in_mis, out_mis    0, 4, 8 or 12.
+ *  stage_elems        elements per stage (multiple of 4, >= 4).
+ */
+ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n, int64_t off,
+                                int in_mis, int out_mis, int64_t stage_elems);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASYNCPIPE_DEBUG_H */

@@ -1,0 +1,159 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared
+symbol, rejects bad arguments before touching CUDA, and its tile planning
+(run on the host by ap_debug_emulate_ring) moves every element to the right
+place for any alignment, offset and stage size."""
+
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ap():
+    from async_global_shared_gb300 import build
+
+    build.build()
+    import async_global_shared_gb300 as ap
+
+    ap.load()
+    return ap
+
+
+def _declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ap_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(ap):
+    declared = _declared_symbols()
+    assert {"ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange", "ap_check"} <= declared
+    nm = subprocess.run(["nm", "-D", "--defined-only", ap.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\bT (ap_\w+)$", nm.stdout, flags=re.M))
+    assert declared <= exported, f"declared but not exported: {declared - exported}"
+    assert set(ap.EXPORTED) == declared
+    lib = ap.load()
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_status_strings(ap):
+    for code, name in ap._lib.STATUS_NAMES.items():
+        assert ap.ap_status_string(code) == name
+
+
+FAKE_IN = 0x7F0000000000
+FAKE_OUT = 0x7F0100000000
+
+
+def raw(ap, fn, *args):
+    return getattr(ap.load(), fn)(*args)
+
+
+def test_validation_before_cuda(ap):
+    # Every case below is rejected before any CUDA call (fake addresses are safe).
+    assert raw(ap, "ap_scale", FAKE_IN, FAKE_OUT, 4, 256, 2.0, 1, None) == ap.AP_ERR_STAGES
+    assert raw(ap, "ap_scale", FAKE_IN, FAKE_OUT, 4, 256, 2.0, 7, None) == ap.AP_ERR_STAGES
+    assert raw(ap, "ap_scale", FAKE_IN, FAKE_OUT, -1, 256, 2.0, 2, None) == ap.AP_ERR_SHAPE
+    assert raw(ap, "ap_scale", FAKE_IN, FAKE_OUT, 4, 0, 2.0, 2, None) == ap.AP_ERR_SHAPE
+    assert raw(ap, "ap_scale", FAKE_IN, FAKE_OUT, 1 << 40, 1 << 40, 2.0, 2, None) == ap.AP_ERR_SHAPE
+    assert raw(ap, "ap_scale", None, FAKE_OUT, 4, 256, 2.0, 2, None) == ap.AP_ERR_NULL
+    assert raw(ap, "ap_scale", FAKE_IN + 2, FAKE_OUT, 4, 256, 2.0, 2, None) == ap.AP_ERR_ALIGN
+    assert raw(ap, "ap_scale", FAKE_IN, FAKE_IN + 16, 4, 256, 2.0, 2, None) == ap.AP_ERR_ALIAS
+    assert raw(ap, "ap_scale", None, None, 0, 256, 2.0, 2, None) == ap.AP_OK  # empty: no-op
+    assert raw(ap, "ap_scale_sync", FAKE_IN, FAKE_OUT, 4, 1 << 20, 2.0, None) == ap.AP_ERR_SMEM
+    assert raw(ap, "ap_scale_sync", FAKE_IN, FAKE_IN + 4, 4, 256, 2.0, None) == ap.AP_ERR_ALIAS
+    assert raw(ap, "ap_row_roll", FAKE_IN, FAKE_OUT, -1, 4, 1, None) == ap.AP_ERR_SHAPE
+    assert raw(ap, "ap_row_roll", FAKE_IN, FAKE_OUT, 0, 4, 1, None) == ap.AP_OK
+    assert raw(ap, "ap_row_roll", FAKE_IN, FAKE_IN, 64, 4, 1, None) == ap.AP_ERR_ALIAS  # roll never in place
+    assert raw(ap, "ap_row_roll", FAKE_IN, FAKE_OUT + 1, 64, 4, 1, None) == ap.AP_ERR_ALIGN
+    assert raw(ap, "ap_poly", FAKE_IN, FAKE_OUT, 100, None, 3, 2, None) == ap.AP_ERR_NULL
+    c = (np.zeros(2000, dtype=np.float32)).ctypes.data
+    assert raw(ap, "ap_poly", FAKE_IN, FAKE_OUT, 100, c, -1, 2, None) == ap.AP_ERR_ARG
+    assert raw(ap, "ap_poly", FAKE_IN, FAKE_OUT, 100, c, 1024, 2, None) == ap.AP_ERR_ARG
+    assert raw(ap, "ap_poly", FAKE_IN, FAKE_OUT, 100, c, 8, 9, None) == ap.AP_ERR_STAGES
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1 << 20, 3, 32768, None) == ap.AP_ERR_CLUSTER
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1 << 20, 16, 32768, None) == ap.AP_ERR_CLUSTER
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1 << 20, 2, 24, None) == ap.AP_ERR_SHAPE
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1 << 20, 2, 128 * 1024, None) == ap.AP_ERR_SMEM
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1000, 4, 32768, None) == ap.AP_ERR_SHAPE
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN + 4, FAKE_OUT, 1 << 20, 2, 32768, None) == ap.AP_ERR_ALIGN
+    assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_IN, 1 << 20, 2, 32768, None) == ap.AP_ERR_ALIAS
+
+
+def test_debug_settings_roundtrip(ap):
+    lib = ap.load()
+    assert lib.ap_debug_set(ap.AP_DBG_STAGE_BYTES, -5) == ap.AP_ERR_ARG
+    assert lib.ap_debug_set(999, 1) == ap.AP_ERR_ARG
+    assert lib.ap_debug_get(999) == -1
+    for key, val in ((ap.AP_DBG_STAGE_BYTES, 4096), (ap.AP_DBG_GRID, 7), (ap.AP_DBG_TIMEOUT_NS, 12345)):
+        ap.ap_debug_set(key, val)
+        assert ap.ap_debug_get(key) == val
+        ap.ap_debug_set(key, 0)
+    assert ap.ap_debug_get(ap.AP_DBG_TIMEOUT_NS) > 0  # default limit applies when unset
+
+
+@pytest.mark.skipif(
+    __import__("torch").cuda.is_available(), reason="only meaningful where no CUDA device exists"
+)
+def test_valid_call_without_gpu_reports_cuda_error(ap):
+    # Arguments pass validation; the first CUDA call then fails cleanly.
+    st = raw(ap, "ap_scale", FAKE_IN, FAKE_OUT, 4, 256, 2.0, 2, None)
+    assert st == ap.AP_ERR_CUDA
+
+
+# ----------------------------------------------------------------- host emulation of the ring
+
+
+def _emulate(ap, x, off, in_mis, out_mis, se):
+    y = np.full_like(x, np.nan)
+    st = ap.ap_debug_emulate_ring(x, y, x.size, off, in_mis, out_mis, se)
+    return st, y
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 33, 64, 100, 255, 256, 257, 1000, 4099])
+def test_emulated_ring_matches_oracle(ap, orc, n):
+    x = synth.uniform_pm1_np(n, n)
+    offs = sorted({0, 1, n - 1, n // 2, (7 * n) // 11} & set(range(n)))
+    for se in (4, 8, 12, 64, 256):
+        for off in offs:
+            want = orc.row_roll(x.reshape(n, 1), off).ravel()
+            for in_mis in (0, 4, 8, 12):
+                for out_mis in (0, 4, 8, 12):
+                    st, y = _emulate(ap, x, off, in_mis, out_mis, se)
+                    assert st == ap.AP_OK, (n, off, in_mis, out_mis, se)
+                    assert np.array_equal(y.view(np.uint32), want.view(np.uint32)), (n, off, in_mis, out_mis, se)
+
+
+def test_emulated_ring_row_shift_geometry(ap, orc):
+    # rows x cols matrices as the row shift drives the ring: off = shift * cols
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        rows = int(rng.integers(1, 60))
+        cols = int(rng.integers(1, 9))
+        shift = int(rng.integers(-100, 100))
+        se = int(rng.choice([4, 8, 16, 20, 64]))
+        A = synth.uniform_pm1_np(rows * 100 + cols, rows * cols).reshape(rows, cols)
+        s = shift % rows
+        st, y = _emulate(ap, A.ravel(), s * cols, int(rng.choice([0, 4, 8, 12])), int(rng.choice([0, 4, 8, 12])), se)
+        assert st == ap.AP_OK
+        assert np.array_equal(y.reshape(rows, cols).view(np.uint32), orc.row_roll(A, shift).view(np.uint32))
+
+
+def test_emulator_rejects_bad_arguments(ap):
+    x = np.zeros(16, dtype=np.float32)
+    y = np.zeros(16, dtype=np.float32)
+    assert ap.ap_debug_emulate_ring(x, y, 16, 16, 0, 0, 4) == ap.AP_ERR_SHAPE
+    assert ap.ap_debug_emulate_ring(x, y, 16, 0, 2, 0, 4) == ap.AP_ERR_ALIGN
+    assert ap.ap_debug_emulate_ring(x, y, 16, 0, 0, 0, 6) == ap.AP_ERR_SHAPE

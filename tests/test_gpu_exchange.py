@@ -1,0 +1,61 @@
+"""ap_cluster_exchange against the oracle, bit for bit. Cluster sizes 4 and 8
+tell the hand-off direction apart (for 2 both directions agree)."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def ap():
+    ap = lib()
+    reset_debug(ap)
+    yield ap
+    reset_debug(ap)
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+@pytest.mark.parametrize("chunk_bytes,groups", [(16, 1), (16, 37), (48, 5), (1024, 300), (32768, 3), (100000, 4)])
+def test_exchange_small(ap, orc, cs, chunk_bytes, groups):
+    dev = device()
+    n = groups * cs * chunk_bytes // 4
+    x = synth.uniform_pm1_torch(n + cs, n, dev)
+    want = orc.cluster_exchange(to_np(x), cs, chunk_bytes)
+    for grid in (0, cs):  # cs: a single cluster walks every group through its ring
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_exchange(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 4
+        assert_bits(to_np(out.view), want, f"exchange cs={cs} chunk={chunk_bytes} groups={groups} grid={grid}")
+        assert out.intact()
+
+
+def test_exchange_worked_example(ap, orc):
+    import torch
+
+    dev = device()
+    x = torch.arange(16, dtype=torch.float32, device=dev)
+    # 16-byte chunks, cluster of 4 -> 4 chunks per group, 1 group
+    y = torch.empty_like(x)
+    ap.ap_cluster_exchange(x, y, 16, 4, 16)
+    assert ap.ap_check() == ap.AP_OK
+    assert to_np(y).tolist() == [4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("cs", [2, 4, 8])
+def test_exchange_full_size(ap, orc, cs):
+    """2**28 floats (1 GiB) in 32 KiB chunks: 32768 chunks, 32768/cs groups."""
+    import torch
+
+    dev = device()
+    n = 1 << 28
+    x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
+    y = torch.empty_like(x)
+    ap.ap_cluster_exchange(x, y, n, cs, 32768)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.cluster_exchange(to_np(x), cs, 32768), f"full exchange cs={cs}")

@@ -1,0 +1,76 @@
+"""Bounded waits: a barrier whose expected byte count is inflated never
+completes (every real copy still lands), so the kernel's waits give up after
+a short limit, record AP_ERR_DEVICE_TIMEOUT for ap_check and return. The
+context stays usable: the next normal call is correct. No fault, trap or
+hang is involved."""
+
+import pytest
+
+import synth
+from gpu_util import assert_bits, device, lib, reset_debug, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def ap():
+    ap = lib()
+    reset_debug(ap)
+    yield ap
+    reset_debug(ap)
+
+
+def _inject(ap):
+    ap.ap_debug_set(ap.AP_DBG_TIMEOUT_NS, 20_000_000)  # 20 ms
+    ap.ap_debug_set(ap.AP_DBG_EXPECT_TX_EXTRA, 16)
+
+
+def test_ring_wait_times_out_and_recovers(ap, orc):
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n_tiles, tile = 512, 256
+    x = synth.uniform_pm1_torch(3, n_tiles * tile, dev)
+    y = torch.empty_like(x)
+    _inject(ap)
+    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 4096)
+    ap.ap_scale(x, y, n_tiles, tile, 2.0, 3)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    assert ap.ap_check() == ap.AP_OK  # the check cleared the status word
+    reset_debug(ap)
+    ap.ap_scale(x, y, n_tiles, tile, 2.0, 3)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "after recovery")
+
+
+def test_exchange_wait_times_out_and_recovers(ap, orc):
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n = 4 * 4096 * 16 // 4
+    x = synth.uniform_pm1_torch(4, n, dev)
+    y = torch.empty_like(x)
+    _inject(ap)
+    ap.ap_cluster_exchange(x, y, n, 4, 4096)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    reset_debug(ap)
+    ap.ap_cluster_exchange(x, y, n, 4, 4096)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.cluster_exchange(to_np(x), 4, 4096), "exchange after recovery")
+
+
+def test_bad_arguments_raise(ap):
+    import torch
+
+    dev = device()
+    x = torch.zeros(1024, device=dev)
+    with pytest.raises(ap.APError):
+        ap.ap_scale(x, x[4:], 1, 1000, 2.0, 2)  # partial overlap
+    with pytest.raises(ap.APError):
+        ap.ap_row_roll(x, x, 256, 4, 1)  # roll never in place
+    with pytest.raises(TypeError):
+        ap.ap_scale(x.double(), x, 1, 1024, 2.0, 2)
+    with pytest.raises(TypeError):
+        ap.ap_scale(x.cpu(), x, 1, 1024, 2.0, 2)

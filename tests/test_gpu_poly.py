@@ -1,0 +1,89 @@
+"""ap_poly against the oracle: Horner with fmaf on both sides in the same
+order, so the tolerance is 0 ULP (bit-exact)."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def ap():
+    ap = lib()
+    reset_debug(ap)
+    yield ap
+    reset_debug(ap)
+
+
+@pytest.mark.parametrize("degree", [0, 1, 2, 8, 32, 128, 1023])
+@pytest.mark.parametrize("stages", [2, 3, 4, 6])
+def test_poly_small(ap, orc, degree, stages):
+    dev = device()
+    n = 20011
+    x = synth.uniform_pm1_torch(n + degree, n, dev)
+    c = synth.coeffs_np(degree)
+    want = orc.poly(to_np(x), c)
+    for stage_bytes, grid in ((256, 2), (0, 0)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} stage={stage_bytes}")
+        assert out.intact()
+
+
+@pytest.mark.parametrize("in_shift,out_shift", [(1, 0), (0, 3), (2, 2)])
+def test_poly_misaligned_and_edges(ap, orc, in_shift, out_shift):
+    import torch
+
+    dev = device()
+    c = synth.coeffs_np(8)
+    for n in (1, 2, 3, 5, 17, 4099):
+        src = Guarded(n, in_shift, dev, fill=synth.uniform_pm1_torch(n, n, dev))
+        out = Guarded(n, out_shift, dev)
+        ap.ap_poly(src.view, out.view, n, c.tolist(), 8, 2)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), orc.poly(to_np(src.view), c), f"poly n={n} in+{in_shift} out+{out_shift}")
+        assert out.intact()
+
+
+def test_poly_special_values(ap, orc):
+    import torch
+
+    dev = device()
+    vals = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 1e-40, 65504.0], dtype=np.float32)
+    x = torch.from_numpy(np.tile(vals, 50)).to(dev)
+    for degree in (0, 1, 3):
+        c = synth.coeffs_np(degree)
+        y = torch.empty_like(x)
+        ap.ap_poly(x, y, x.numel(), c.tolist(), degree, 2)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(y), orc.poly(to_np(x), c), f"special K={degree}", nan_equal=True)
+
+
+def test_poly_full_size_sweep_sampled(ap, orc):
+    """2**30 floats (4 GiB), stages {2,3,4,6} x degree {0,8,32,128}; the
+    outputs are checked at the first and last 64 Ki elements and at 256 Ki
+    random positions, each computed one by one by the oracle."""
+    import torch
+
+    dev = device()
+    n = 1 << 30
+    x = synth.uniform_pm1_torch(synth.SEED_POLY, n, dev)
+    y = torch.empty_like(x)
+    rng = np.random.default_rng(1)
+    idx_h = np.concatenate([np.arange(1 << 16), np.arange(n - (1 << 16), n), rng.integers(0, n, 1 << 18)])
+    idx = torch.from_numpy(idx_h).to(dev)
+    xs = to_np(x[idx])
+    for degree in (0, 8, 32, 128):
+        c = synth.coeffs_np(degree)
+        want = orc.poly(xs, c)
+        for stages in (2, 3, 4, 6):
+            y.fill_(float("nan"))
+            ap.ap_poly(x, y, n, c.tolist(), degree, stages)
+            assert ap.ap_check() == ap.AP_OK
+            assert_bits(to_np(y[idx]), want, f"full poly K={degree} S={stages}")

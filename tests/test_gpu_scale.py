@@ -1,0 +1,133 @@
+"""ap_scale (pipelined ring) and ap_scale_sync (synchronous baseline) against
+the oracle, bit for bit (one correctly rounded fp32 multiply per element)."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def ap():
+    ap = lib()
+    reset_debug(ap)
+    yield ap
+    reset_debug(ap)
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("n_tiles,tile", [(1, 1), (1, 3), (3, 5), (37, 256), (101, 7), (64, 256)])
+def test_scale_small_many_stages(ap, orc, stages, n_tiles, tile):
+    import torch
+
+    dev = device()
+    n = n_tiles * tile
+    x = synth.uniform_pm1_torch(n + 17, n, dev)
+    want = orc.scale(to_np(x), 2.0)
+    # tiny stages and few CTAs: every ring slot goes through many phases
+    for stage_bytes, grid in ((64, 1), (256, 3), (1024, 0)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_scale(x, out.view, n_tiles, tile, 2.0, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"scale S={stages} n={n} stage={stage_bytes} grid={grid}")
+        assert out.intact(), "wrote outside the output"
+        assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 1
+
+
+@pytest.mark.parametrize("in_shift,out_shift", [(0, 1), (1, 0), (1, 1), (2, 3), (3, 2), (3, 3)])
+def test_scale_misaligned(ap, orc, in_shift, out_shift):
+    dev = device()
+    n = 10007
+    src = Guarded(n, in_shift, dev, fill=synth.uniform_pm1_torch(99, n, dev))
+    want = orc.scale(to_np(src.view), -1.5)
+    for stage_bytes in (0, 512):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_GRID, 4 if stage_bytes else 0)
+        out = Guarded(n, out_shift, dev)
+        ap.ap_scale(src.view, out.view, n, 1, -1.5, 3)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"misaligned in+{in_shift} out+{out_shift}")
+        assert out.intact()
+        assert src.intact()
+
+
+def test_scale_in_place(ap, orc):
+    import torch
+
+    dev = device()
+    n_tiles, tile = 300, 256
+    x = synth.uniform_pm1_torch(5, n_tiles * tile, dev)
+    want = orc.scale(to_np(x), 0.375)
+    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 2048)
+    ap.ap_scale(x, x, n_tiles, tile, 0.375, 4)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(x), want, "in place")
+
+
+def test_scale_special_values(ap, orc):
+    import torch
+
+    dev = device()
+    vals = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 1.1754942e-38, 3.4e38, -3.4e38, 1.0, -2.5],
+                    dtype=np.float32)
+    x_np = np.tile(vals, 100)
+    x = torch.from_numpy(x_np).to(dev)
+    for alpha in (2.0, 0.5, -3.0, 1e-10):
+        y = torch.empty_like(x)
+        ap.ap_scale(x, y, len(x_np), 1, alpha, 2)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(y), orc.scale(x_np, alpha), f"special alpha={alpha}", nan_equal=True)
+        ys = torch.empty_like(x)
+        ap.ap_scale_sync(x, ys, len(x_np), 1, alpha)
+        assert_bits(to_np(ys), orc.scale(x_np, alpha), f"sync special alpha={alpha}", nan_equal=True)
+
+
+@pytest.mark.parametrize("n_tiles,tile", [(1, 1), (5, 3), (37, 256), (4, 2000), (2, 20000)])
+def test_scale_sync_small(ap, orc, n_tiles, tile):
+    dev = device()
+    n = n_tiles * tile
+    x = synth.uniform_pm1_torch(n, n, dev)
+    out = Guarded(n, 0, dev)
+    ap.ap_scale_sync(x, out.view, n_tiles, tile, 2.0)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(out.view), orc.scale(to_np(x), 2.0), "sync")
+    assert out.intact()
+
+
+def test_scale_full_size_ring_vs_sync_vs_oracle(ap, orc):
+    """The benchmark's workload: 2**20 tiles x 256 floats, alpha 2, 2 stages."""
+    import torch
+
+    dev = device()
+    n_tiles, tile = 1 << 20, 256
+    n = n_tiles * tile
+    x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
+    y = torch.empty_like(x)
+    ap.ap_scale(x, y, n_tiles, tile, 2.0, 2)
+    assert ap.ap_check() == ap.AP_OK
+    x_h = to_np(x)
+    assert_bits(to_np(y), orc.scale(x_h, 2.0), "full-size ring")
+    ys = torch.empty_like(x)
+    ap.ap_scale_sync(x, ys, n_tiles, tile, 2.0)
+    assert ap.ap_check() == ap.AP_OK
+    assert torch.equal(ys.view(torch.int32), y.view(torch.int32)), "sync baseline and ring differ"
+    for stages in (3, 4, 6):
+        ap.ap_scale(x, ys, n_tiles, tile, 2.0, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert torch.equal(ys.view(torch.int32), y.view(torch.int32)), f"stages={stages} differs"
+
+
+def test_device_generator_matches_host(ap):
+    import torch
+
+    dev = device()
+    n = 1 << 22
+    t = synth.uniform_pm1_torch(synth.SEED_POLY, n, dev)
+    idx = np.random.default_rng(0).integers(0, n, 4096)
+    got = to_np(t[torch.from_numpy(idx).to(dev)])
+    assert_bits(got, synth.uniform_pm1_np(synth.SEED_POLY, n)[idx], "device generator")
