@@ -46,6 +46,8 @@ AP_DBG_STAGE_BYTES = 4
 AP_DBG_GRID = 5
 AP_DBG_CTAS_PER_SM = 6
 AP_DBG_ROLL_STAGES = 7
+AP_DBG_CONSUMER_WARPS = 8
+AP_DBG_EXCHANGE_STORE = 9
 AP_DBG_LAST_PATH = 100
 AP_DBG_LAST_GRID = 101
 AP_DBG_LAST_STAGE_ELEMS = 102
@@ -65,6 +67,7 @@ EXPORTED = (
     "ap_debug_set",
     "ap_debug_get",
     "ap_debug_emulate_ring",
+    "ap_debug_fma_probe",
 )
 
 
@@ -103,8 +106,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_get.argtypes = [ctypes.c_int]
     lib.ap_debug_get.restype = _i64
     lib.ap_debug_emulate_ring.argtypes = [vp, vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _i64]
+    lib.ap_debug_fma_probe.argtypes = [vp, _i64, _i64, vp]
     for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange", "ap_check",
-                 "ap_debug_set", "ap_debug_emulate_ring"):
+                 "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_fma_probe"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -201,3 +205,7 @@ def ap_debug_emulate_ring(in_host, out_host, n: int, off: int, in_mis: int, out_
     assert in_host.dtype == np.float32 and out_host.dtype == np.float32
     return load().ap_debug_emulate_ring(in_host.ctypes.data, out_host.ctypes.data, n, off, in_mis, out_mis,
                                         stage_elems)
+
+
+def ap_debug_fma_probe(out, out_elems: int, iters: int, stream=None):
+    _check(load().ap_debug_fma_probe(_addr(out), out_elems, iters, _stream(stream)), "ap_debug_fma_probe")

@@ -27,6 +27,8 @@ std::atomic<int64_t> g_stage_bytes{0};
 std::atomic<int64_t> g_grid{0};
 std::atomic<int64_t> g_ctas_per_sm{0};
 std::atomic<int64_t> g_roll_stages{0};
+std::atomic<int64_t> g_consumer_warps{0};
+std::atomic<int64_t> g_ex_tma_store{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0};
@@ -110,6 +112,8 @@ Options options() {
     o.grid = g_grid.load();
     o.ctas_per_sm = g_ctas_per_sm.load();
     o.roll_stages = g_roll_stages.load();
+    o.consumer_warps = g_consumer_warps.load();
+    o.ex_tma_store = g_ex_tma_store.load();
     return o;
 }
 
@@ -274,6 +278,14 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value != 0 && !valid_stages(static_cast<int>(value))) return AP_ERR_ARG;
             g_roll_stages = value;
             return AP_OK;
+        case AP_DBG_CONSUMER_WARPS:
+            if (value != 0 && value != 8 && value != 16) return AP_ERR_ARG;
+            g_consumer_warps = value;
+            return AP_OK;
+        case AP_DBG_EXCHANGE_STORE:
+            if (value > 2) return AP_ERR_ARG;
+            g_ex_tma_store = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -288,6 +300,8 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_GRID: return o.grid;
         case AP_DBG_CTAS_PER_SM: return o.ctas_per_sm;
         case AP_DBG_ROLL_STAGES: return o.roll_stages;
+        case AP_DBG_CONSUMER_WARPS: return o.consumer_warps;
+        case AP_DBG_EXCHANGE_STORE: return o.ex_tma_store;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();
@@ -296,6 +310,16 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_LAST_FLAGS: return g_last_flags.load();
         default: return -1;
     }
+}
+
+ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaStream_t stream) {
+    if (out == nullptr) return AP_ERR_NULL;
+    if (out_elems < 1 || iters < 1 || iters > (int64_t(1) << 24)) return AP_ERR_SHAPE;
+    if (!aligned4(out)) return AP_ERR_ALIGN;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    return launch_fma_probe(di, out, out_elems, iters, stream);
 }
 
 // Host emulation of the ring's data movement (see asyncpipe_debug.h). It

@@ -9,16 +9,21 @@
 // any of them exits.
 //
 // Each cluster walks a sequence of groups of cluster_size chunks through a
-// ring of S send slots and S receive slots per CTA. CTA rank r has three
-// roles, one warp each for the two single-thread roles:
-//   loader   (warp 0): waits credit[s], loads its chunk of the group from
-//            global memory into send[s] (bulk copy, load_full[s]).
+// ring of S send slots and S receive slots per CTA. A chunk moves as P
+// equal pieces (each a ring item), so the load, the hand-off and the store
+// of one chunk overlap each other; piece q of a chunk lands as piece q of the
+// receiver's output chunk, so the result is the same as moving whole chunks.
+// CTA rank r has three roles, one warp each for the two single-thread roles:
+//   loader   (warp 0): waits credit[s], loads the next piece of its chunk of
+//            the group from global memory into send[s] (bulk copy, load_full[s]).
 //   pusher   (warp 1): waits load_full[s], pushes send[s] into recv[s] of
 //            rank (r-1) mod cs, completing on that CTA's recv_full[s].
-//   receiver (8 warps): registers chunk_bytes on its recv_full[s], waits,
+//   receiver (8 warps): registers the piece's bytes on its recv_full[s], waits,
 //            stores recv[s] to its output chunk with 16-byte stores, then
-//            each warp arrives (remote, release.cluster) on credit[s] of
-//            rank (r+1) mod cs, the CTA that sends to it.
+//            each warp arrives (remote) on credit[s] of rank (r+1) mod cs,
+//            the CTA that sends to it. In the TMA-store form one thread
+//            instead hands recv[s] to a shared->global bulk copy and credits
+//            the slot once that copy has read it.
 // credit[s] therefore tells a sender both that its send[s] has been read
 // (the data reached the receiver) and that the receiver's recv[s] is free,
 // so the loader may refill send[s] and the pusher may overwrite recv[s].
@@ -33,14 +38,18 @@ namespace {
 constexpr int kExConsumerWarps = 8;
 constexpr int kExConsumers = 32 * kExConsumerWarps;
 constexpr int kExThreads = 64 + kExConsumers;
+constexpr int64_t kExMaxSlots = 16;
 
 struct ExParams {
     const float* in;
     float* out;
     int64_t groups;        // whole groups of cluster_size chunks
     uint32_t chunk_bytes;  // multiple of 16
+    uint32_t piece_bytes;  // divides chunk_bytes, multiple of 16
+    int pieces;            // chunk_bytes / piece_bytes
     int cs;                // cluster size
     int stages;            // ring slots per direction
+    int tma_store;         // receiver stores with bulk copies (1) or with 8 warps (0)
     uint32_t tx_extra;
     uint64_t timeout_ns;
     uint32_t* status;
@@ -49,7 +58,8 @@ struct ExParams {
 __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_constant__ ExParams P) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = P.stages;
-    const uint32_t CB = P.chunk_bytes;
+    const uint32_t CB = P.piece_bytes;  // ring slot = one piece
+    const int64_t NP = P.pieces;
     unsigned char* send = smem;
     unsigned char* recv = smem + static_cast<size_t>(S) * CB;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * static_cast<size_t>(S) * CB);
@@ -65,13 +75,19 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
     const uint32_t src_rank = (rank + 1) % cs;       // sends this CTA its chunk
     const int64_t cid = ptx::cluster_id_x();
     const int64_t ncl = ptx::nclusters_x();
-    const int64_t count = cid < P.groups ? (P.groups - cid + ncl - 1) / ncl : 0;
-    const int64_t E = CB / 4;
+    const int64_t count = (cid < P.groups ? (P.groups - cid + ncl - 1) / ncl : 0) * NP;
+    // Byte offset of this CTA's piece for item i: chunk (group * cs + rank), piece i mod NP.
+    auto piece_off = [&](int64_t i) -> int64_t {
+        const int64_t grp = cid + (i / NP) * ncl;
+        return (grp * P.cs + rank) * static_cast<int64_t>(P.chunk_bytes) + (i % NP) * static_cast<int64_t>(CB);
+    };
+    const unsigned char* in_bytes = reinterpret_cast<const unsigned char*>(P.in);
+    unsigned char* out_bytes = reinterpret_cast<unsigned char*>(P.out);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(load_full(s), 1);
-            ptx::mbar_init(credit(s), kExConsumerWarps);
+            ptx::mbar_init(credit(s), P.tma_store ? 1 : kExConsumerWarps);
             ptx::mbar_init(recv_full(s), 1);
         }
         *abort_flag = 0;
@@ -89,15 +105,14 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
             for (; i < count; ++i) {
                 const int s = static_cast<int>(i % S);
                 const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-                const int64_t grp = cid + i * ncl;
                 const int w = wait_phase<true>(credit(s), ph ^ 1u, P.timeout_ns, abort_flag);
                 if (w != WAIT_OK) {
                     if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_LOADER_CREDIT, abort_flag);
                     break;
                 }
                 ptx::mbar_arrive_expect_tx(load_full(s), CB + P.tx_extra);
-                ptx::bulk_g2s(ptx::smem_addr(send + static_cast<size_t>(s) * CB),
-                              P.in + (grp * P.cs + rank) * E, CB, load_full(s));
+                ptx::bulk_g2s(ptx::smem_addr(send + static_cast<size_t>(s) * CB), in_bytes + piece_off(i), CB,
+                              load_full(s));
             }
             for (int64_t k = i > S ? i - S : 0; k < i; ++k) {
                 if (wait_phase<false>(load_full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1),
@@ -122,6 +137,47 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                                       peer_bars + 8u * static_cast<uint32_t>(2 * S + s));
             }
         }
+    } else if (P.tma_store) {
+        // Receiver, TMA-store form: one thread registers, waits and hands each
+        // received piece to the bulk-copy engine (shared -> global); a slot is
+        // credited back once the engine has finished reading it.
+        if (warp == 2 && lane == 0) {
+            const uint32_t peer_credit = ptx::mapa(credit(0), src_rank);
+            const int64_t lag = S > 2 ? 2 : S - 1;  // bulk stores left reading before a slot is credited
+            int64_t i = 0;
+            for (; i < count; ++i) {
+                const int s = static_cast<int>(i % S);
+                ptx::mbar_arrive_expect_tx(recv_full(s), CB);
+                const int w = wait_phase<true>(recv_full(s), static_cast<uint32_t>((i / S) & 1), P.timeout_ns,
+                                               abort_flag);
+                if (w != WAIT_OK) {
+                    if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_RECEIVER_FULL, abort_flag);
+                    // Chunks a peer already sent may still be landing in recv[]:
+                    // wait for them (bounded) before the final cluster barrier.
+                    for (int64_t k = i; k < count && k < i + S; ++k) {
+                        if (k > i) ptx::mbar_arrive_expect_tx(recv_full(static_cast<int>(k % S)), CB);
+                        if (wait_phase<true>(recv_full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1),
+                                             P.timeout_ns, nullptr) != WAIT_OK)
+                            raise_timeout(P.status, SITE_EX_DRAIN, abort_flag);
+                    }
+                    break;
+                }
+                ptx::bulk_s2g(out_bytes + piece_off(i), ptx::smem_addr(recv + static_cast<size_t>(s) * CB), CB);
+                ptx::bulk_commit();
+                if (lag == 2) {
+                    ptx::bulk_wait_read<2>();
+                } else if (lag == 1) {
+                    ptx::bulk_wait_read<1>();
+                } else {
+                    ptx::bulk_wait_read<0>();
+                }
+                if (i >= lag) ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>((i - lag) % S));
+            }
+            ptx::bulk_wait_read<0>();
+            for (int64_t k = i > lag ? i - lag : 0; k < i; ++k)
+                ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>(k % S));
+            ptx::bulk_wait_all();
+        }
     } else {
         const int cw = warp - 2;
         const int ct = threadIdx.x - 64;
@@ -132,7 +188,6 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
         for (; i < count; ++i) {
             const int s = static_cast<int>(i % S);
             const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-            const int64_t grp = cid + i * ncl;
             if (leader) {
                 ptx::mbar_arrive_expect_tx(recv_full(s), CB);
                 armed = i + 1;
@@ -146,7 +201,7 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
             if (w != WAIT_OK) break;
             __syncwarp();
             const float4* src = reinterpret_cast<const float4*>(recv + static_cast<size_t>(s) * CB);
-            float4* dst = reinterpret_cast<float4*>(P.out + (grp * P.cs + rank) * E);
+            float4* dst = reinterpret_cast<float4*>(out_bytes + piece_off(i));
             const int64_t nq = CB / 16;
             int64_t q = ct;
             for (; q + 3 * kExConsumers < nq; q += 4 * kExConsumers) {
@@ -161,7 +216,9 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
             }
             for (; q < nq; q += kExConsumers) dst[q] = src[q];
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_remote(peer_credit + 8u * static_cast<uint32_t>(s));
+            // The slot's values are in registers (the stores used them), so a
+            // relaxed arrive suffices: it does not wait for the global stores.
+            if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>(s));
         }
         if (leader && i < count) {
             // Gave up early: chunks a peer already sent may still be landing in
@@ -183,11 +240,23 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
 
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
                           int64_t chunk_bytes, cudaStream_t stream) {
-    const int64_t budget = di.smem_optin - 256;
-    int64_t S = budget / (2 * chunk_bytes);
+    // Piece: the largest multiple of 16 dividing chunk_bytes that is at most
+    // the target (8 KiB, or the stage-bytes setting).
+    const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 8192;
+    const int64_t units = chunk_bytes / 16;
+    int64_t piece_units = 1;
+    for (int64_t d = 1; d * d <= units; ++d) {
+        if (units % d) continue;
+        const int64_t a = d, b = units / d;
+        if (16 * a <= target && a > piece_units) piece_units = a;
+        if (16 * b <= target && b > piece_units) piece_units = b;
+    }
+    const int64_t piece = 16 * piece_units;
+    const int64_t budget = di.smem_optin - 512;
+    int64_t S = budget / (2 * piece);
     if (S < 1) return AP_ERR_SMEM;
-    if (S > 4) S = 4;
-    const int64_t smem = 2 * S * chunk_bytes + 3 * 8 * S + 16;
+    if (S > kExMaxSlots) S = kExMaxSlots;
+    const int64_t smem = 2 * S * piece + 3 * 8 * S + 16;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
 
     static bool configured[64] = {false};
@@ -200,8 +269,18 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     }
 
     const int64_t groups = (4 * n) / (static_cast<int64_t>(cs) * chunk_bytes);
-    ExParams P{in, out, groups, static_cast<uint32_t>(chunk_bytes), cs, static_cast<int>(S),
-               static_cast<uint32_t>(o.tx_extra), static_cast<uint64_t>(o.timeout_ns), di.status};
+    ExParams P{in,
+               out,
+               groups,
+               static_cast<uint32_t>(chunk_bytes),
+               static_cast<uint32_t>(piece),
+               static_cast<int>(chunk_bytes / piece),
+               cs,
+               static_cast<int>(S),
+               o.ex_tma_store == 1 ? 1 : 0,
+               static_cast<uint32_t>(o.tx_extra),
+               static_cast<uint64_t>(o.timeout_ns),
+               di.status};
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -221,7 +300,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     int64_t ncl = std::min<int64_t>(groups, max_clusters);
     if (o.grid > 0) ncl = std::max<int64_t>(1, std::min<int64_t>(ncl, o.grid / cs));
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs), 1, 1);
-    record_launch(PATH_EXCHANGE, ncl * cs, chunk_bytes / 4, smem, S, 0);
+    record_launch(PATH_EXCHANGE, ncl * cs, piece / 4, smem, S, 0);
     if (cudaLaunchKernelEx(&cfg, exchange_kernel, P) != cudaSuccess) return AP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
 }

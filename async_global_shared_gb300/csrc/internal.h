@@ -29,6 +29,8 @@ struct Options {
     int64_t grid;
     int64_t ctas_per_sm;
     int64_t roll_stages;
+    int64_t consumer_warps;
+    int64_t ex_tma_store;
 };
 
 Options options();
@@ -62,6 +64,8 @@ ap_status launch_roll_small(const DeviceInfo& di, const float* A, float* B, int6
 
 ap_status launch_scale_sync(const DeviceInfo& di, const float* in, float* out, int64_t n_tiles, int64_t tile,
                             float alpha, cudaStream_t stream);
+
+ap_status launch_fma_probe(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
 
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
                           int64_t chunk_bytes, cudaStream_t stream);

@@ -48,6 +48,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Remote arrive without release ordering: for a signal that only says "my
+// shared-memory reads of the slot are done" (the values are already in
+// registers), so it need not wait for this thread's global stores.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // Non-blocking probe of phase completion (the hardware may suspend the thread
 // for a short, bounded time before answering false).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -105,6 +112,23 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uin
         "r"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+
+// Shared (this CTA) -> global bulk copy, tracked by the thread's bulk async-group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // L2 policy: lines touched once, evict them first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

@@ -1,7 +1,7 @@
 // The streaming ring: a persistent, warp-specialised kernel in which one
 // producer thread keeps up to S stages of input in flight with bulk
-// asynchronous copies while eight consumer warps compute on the oldest
-// landed stage and store it.
+// asynchronous copies while the consumer warps (8, or 16 on request) compute
+// on the oldest landed stage and store it.
 //
 // Protocol per ring slot s (two mbarriers, "Asynchronous Data Movement",
 // section Barriers and pipelines: acquire, commit, wait, release):
@@ -32,40 +32,59 @@
 namespace ap {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kThreads = 32 + kConsumers;
 constexpr int kUnroll = 4;  // 16-byte groups per consumer thread per iteration
 
+// Each op: stage() copies whatever the op reads from shared memory (only
+// the polynomial's coefficients) before the ring starts; apply() transforms
+// N values held in registers.
 struct OpCopyDev {
+    __device__ __forceinline__ void stage(float*, int, int) const {}
     template <int N>
-    __device__ __forceinline__ void apply(float (&)[N]) const {}
+    __device__ __forceinline__ void apply(float (&)[N], const float*) const {}
 };
 
 struct OpScaleDev {
     float alpha;
+    __device__ __forceinline__ void stage(float*, int, int) const {}
     template <int N>
-    __device__ __forceinline__ void apply(float (&v)[N]) const {
+    __device__ __forceinline__ void apply(float (&v)[N], const float*) const {
 #pragma unroll
         for (int t = 0; t < N; ++t) v[t] = alpha * v[t];
     }
 };
 
 // Horner's rule, one fmaf per step, N independent chains per thread so the
-// FMA pipe sees N-way instruction-level parallelism.
+// FMA pipe sees N-way instruction-level parallelism. The coefficients are
+// read from shared memory four at a time (one 16-byte broadcast load per four
+// fma steps per chain), highest power first.
 struct OpPolyDev {
     int degree;
     float c[AP_POLY_MAX_DEGREE + 1];
+    __device__ __forceinline__ void stage(float* cs, int tid, int nthreads) const {
+        for (int k = tid; k <= degree; k += nthreads) cs[k] = c[k];
+    }
     template <int N>
-    __device__ __forceinline__ void apply(float (&v)[N]) const {
+    __device__ __forceinline__ void apply(float (&v)[N], const float* cs) const {
         float p[N];
-        const float top = c[degree];
+        const float top = cs[degree];
 #pragma unroll
         for (int t = 0; t < N; ++t) p[t] = top;
-        for (int k = degree - 1; k >= 0; --k) {
-            const float ck = c[k];
+        int k = degree - 1;
+        for (; k >= 0 && ((k + 1) & 3) != 0; --k) {  // until k + 1 is a multiple of 4
+            const float ck = cs[k];
 #pragma unroll
             for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], ck);
+        }
+        for (; k >= 3; k -= 4) {  // steps k, k-1, k-2, k-3 from one aligned 16-byte word
+            const float4 q = *reinterpret_cast<const float4*>(cs + k - 3);
+#pragma unroll
+            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.w);
+#pragma unroll
+            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.z);
+#pragma unroll
+            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.y);
+#pragma unroll
+            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.x);
         }
 #pragma unroll
         for (int t = 0; t < N; ++t) v[t] = p[t];
@@ -81,6 +100,7 @@ struct RingParams {
     uint32_t tx_extra;
     uint64_t timeout_ns;
     uint32_t* status;
+    uint32_t coef_off;  // byte offset of the op's staged data in dynamic shared memory
     Op op;
 };
 
@@ -88,9 +108,9 @@ __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off
     return *reinterpret_cast<const float*>(slot + off);
 }
 
-template <class Op>
+template <int kConsumers, class Op>
 __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const StagePlan& sp, const unsigned char* slot,
-                                              int ct) {
+                                              const float* cs, int ct) {
     const int64_t ngroups = (sp.e_end - sp.e_al) >> 2;
     float* __restrict__ out = P.out;
     if (sp.vec) {
@@ -108,7 +128,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Sta
                 v[4 * u + 2] = t.z;
                 v[4 * u + 3] = t.w;
             }
-            P.op.apply(v);
+            P.op.apply(v, cs);
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u)
                 dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
@@ -116,7 +136,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Sta
         for (; q < ngroups; q += kConsumers) {
             const float4 t = src[q];
             float v[4] = {t.x, t.y, t.z, t.w};
-            P.op.apply(v);
+            P.op.apply(v, cs);
             dst[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
     } else {
@@ -125,7 +145,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Sta
             float v[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) v[t] = lds_f32(slot, smem_offset_of_output(sp, e + t));
-            P.op.apply(v);
+            P.op.apply(v, cs);
             *reinterpret_cast<float4*>(out + e) = make_float4(v[0], v[1], v[2], v[3]);
         }
     }
@@ -135,13 +155,15 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Sta
     if (ct < nh + nt) {
         const int64_t e = ct < nh ? sp.lo + ct : sp.e_end + (ct - nh);
         float v[1] = {lds_f32(slot, smem_offset_of_output(sp, e))};
-        P.op.apply(v);
+        P.op.apply(v, cs);
         out[e] = v[0];
     }
 }
 
-template <class Op>
-__global__ void __launch_bounds__(kThreads, 1) ring_kernel(const __grid_constant__ RingParams<Op> P) {
+// kConsumerWarps consumer warps plus one producer warp per CTA.
+template <class Op, int kConsumerWarps>
+__global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(const __grid_constant__ RingParams<Op> P) {
+    constexpr int kConsumers = 32 * kConsumerWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = P.stages;
     const uint32_t slot_bytes = P.g.slot_bytes;
@@ -152,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_kernel(const __grid_constant
     auto full = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(s); };
     auto empty = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(S + s); };
 
+    float* cs = reinterpret_cast<float*>(smem + P.coef_off);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full(s), 1);
@@ -160,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_kernel(const __grid_constant
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    P.op.stage(cs, threadIdx.x, blockDim.x);
     __syncthreads();
 
     const int64_t T = P.g.n_stages;
@@ -232,27 +256,34 @@ __global__ void __launch_bounds__(kThreads, 1) ring_kernel(const __grid_constant
         __syncwarp();  // orders lane 0's observation of the phase before the other lanes' reads
         StagePlan sp;
         plan_stage(P.g, j, &sp);
-        consume_stage(P, sp, smem + static_cast<size_t>(s) * slot_bytes, ct);
+        consume_stage<kConsumers>(P, sp, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty(s));
     }
 }
 
-template <class Op>
+template <class Op, int kConsumerWarps>
 ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t grid, int64_t smem,
                          cudaStream_t stream) {
     // Raise the kernel's dynamic shared-memory limit once per device.
     static int64_t configured[64] = {0};
     const int d = di.device;
     if (d < 0 || d >= 64) return AP_ERR_CUDA;
+    auto kernel = ring_kernel<Op, kConsumerWarps>;
     if (configured[d] < smem) {
-        if (cudaFuncSetAttribute(ring_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
             return AP_ERR_CUDA;
         configured[d] = di.smem_optin;
     }
-    ring_kernel<Op><<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem), stream>>>(P);
+    kernel<<<static_cast<unsigned>(grid), 32 * (kConsumerWarps + 1), static_cast<size_t>(smem), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
+}
+
+template <class Op>
+ap_status launch_ring_warps(const DeviceInfo& di, int64_t warps, const RingParams<Op>& P, int64_t grid, int64_t smem,
+                            cudaStream_t stream) {
+    if (warps == 16) return launch_ring_op<Op, 16>(di, P, grid, smem, stream);
+    return launch_ring_op<Op, 8>(di, P, grid, smem, stream);
 }
 
 }  // namespace
@@ -285,7 +316,9 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     const int64_t se = stage_elems_for(payload, unit);
     StreamGeom g;
     make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
-    const int64_t smem = static_cast<int64_t>(stages) * g.slot_bytes + 2 * 8 * stages + 16;
+    const int64_t coef_off = static_cast<int64_t>(stages) * g.slot_bytes + 2 * 8 * stages + 16;
+    const int64_t coef_bytes = op.kind == OP_POLY ? (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
+    const int64_t smem = coef_off + coef_bytes;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
     const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 1;
     int64_t grid = std::min<int64_t>(g.n_stages, static_cast<int64_t>(di.sms) * cps);
@@ -302,12 +335,14 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     const uint32_t tx_extra = static_cast<uint32_t>(o.tx_extra);
     switch (op.kind) {
         case OP_COPY: {
-            RingParams<OpCopyDev> P{in, out, g, stages, tx_extra, timeout, di.status, OpCopyDev{}};
-            return launch_ring_op(di, P, grid, smem, stream);
+            RingParams<OpCopyDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
+                                    static_cast<uint32_t>(coef_off), OpCopyDev{}};
+            return launch_ring_warps(di, o.consumer_warps, P, grid, smem, stream);
         }
         case OP_SCALE: {
-            RingParams<OpScaleDev> P{in, out, g, stages, tx_extra, timeout, di.status, OpScaleDev{op.alpha}};
-            return launch_ring_op(di, P, grid, smem, stream);
+            RingParams<OpScaleDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
+                                     static_cast<uint32_t>(coef_off), OpScaleDev{op.alpha}};
+            return launch_ring_warps(di, o.consumer_warps, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
@@ -318,9 +353,10 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             P.tx_extra = tx_extra;
             P.timeout_ns = timeout;
             P.status = di.status;
+            P.coef_off = static_cast<uint32_t>(coef_off);
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
-            return launch_ring_op(di, P, grid, smem, stream);
+            return launch_ring_warps(di, o.consumer_warps, P, grid, smem, stream);
         }
     }
     return AP_ERR_ARG;

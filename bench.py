@@ -127,9 +127,9 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self) -> dict | None:
+    def _rows(self):
         if self.proc is None or self.path is None:
-            return None
+            return []
         rows = []
         try:
             for line in open(self.path):
@@ -141,21 +141,34 @@ class ClockSampler:
                     rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
-        finally:
-            os.unlink(self.path)
+        except OSError:
+            pass
+        return rows
+
+    def window(self, t0, t1, rows=None) -> dict | None:
+        """Median SM clock and active throttle reasons of the samples taken
+        between t0 and t1 (the nearest sample if the window is shorter than
+        the sampling period)."""
+        rows = self._rows() if rows is None else rows
         if not rows:
             return None
-        lo = self.t0 - datetime.timedelta(seconds=0.06)
-        hi = self.t1 + datetime.timedelta(seconds=0.06)
+        lo = t0 - datetime.timedelta(seconds=0.06)
+        hi = t1 + datetime.timedelta(seconds=0.06)
         inside = [r for r in rows if lo <= r[0] <= hi]
-        if not inside:  # timed region shorter than the sampling period: nearest sample
-            mid = self.t0 + (self.t1 - self.t0) / 2
+        if not inside:
+            mid = t0 + (t1 - t0) / 2
             inside = [min(rows, key=lambda r: abs((r[0] - mid).total_seconds()))]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower().startswith("active")})
         mhz = sorted(r[1] for r in inside)
         return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
                 "samples": len(inside)}
+
+    def summary(self) -> dict | None:
+        out = self.window(self.t0, self.t1)
+        if self.path is not None and os.path.exists(self.path):
+            os.unlink(self.path)
+        return out
 
 
 def time_steps(fn, steps: int, warmup: int, stream, dist_ctx=None) -> float:
@@ -247,6 +260,44 @@ SCALE_TILES = 1 << 20
 SCALE_TILE = 256
 
 
+E2E_CHUNKS = 16
+
+
+def pipelined_host_step(ap, xh, yh, xd, yd, n_tiles, tile, alpha, stages, chunks, main):
+    """A step that copies pinned host xh to the device, scales it with
+    ap_scale and copies the result to pinned host yh, chunk by chunk on three
+    streams (copy in, compute, copy out) so transfers overlap the kernel."""
+    import torch
+
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    per = n_tiles // chunks
+    bounds = [(c * per, (c + 1) * per if c < chunks - 1 else n_tiles) for c in range(chunks)]
+
+    def step():
+        start = torch.cuda.Event()
+        start.record(main)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for t0, t1 in bounds:
+            a, b = t0 * tile, t1 * tile
+            with torch.cuda.stream(s_in):
+                xd[a:b].copy_(xh[a:b], non_blocking=True)
+            e1 = torch.cuda.Event()
+            e1.record(s_in)
+            s_c.wait_event(e1)
+            ap.ap_scale(xd[a:b], yd[a:b], t1 - t0, tile, alpha, stages, s_c)
+            e2 = torch.cuda.Event()
+            e2.record(s_c)
+            s_out.wait_event(e2)
+            with torch.cuda.stream(s_out):
+                yh[a:b].copy_(yd[a:b], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        main.wait_event(done)
+
+    return step
+
+
 def bench_scale(args, d: Dist) -> dict:
     import numpy as np
     import torch
@@ -285,21 +336,19 @@ def bench_scale(args, d: Dist) -> dict:
     ms_sync = d.max(time_steps(sync, args.steps, args.warmup, stream, d)) / args.steps
     assert ap.ap_check() == 0
 
-    # end to end: pinned host input -> device -> ap_scale -> pinned host output, every step
+    # end to end: pinned host input -> device -> ap_scale -> pinned host output,
+    # every step, in E2E_CHUNKS chunks so the two copy directions and the
+    # kernel overlap (copy-in stream, compute stream, copy-out stream)
     xh = torch.empty(n, dtype=torch.float32, pin_memory=True)
     xh.copy_(x)
     yh = torch.empty(n, dtype=torch.float32, pin_memory=True)
     xd = torch.empty_like(x)
-
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        ap.ap_scale(xd, y, SCALE_TILES, SCALE_TILE, 2.0, 2, stream)
-        yh.copy_(y, non_blocking=True)
+    e2e_step = pipelined_host_step(ap, xh, yh, xd, y, SCALE_TILES, SCALE_TILE, 2.0, 2, E2E_CHUNKS, stream)
 
     e2e_steps = max(3, min(args.steps, 20))
     ms_e2e = d.max(time_steps(e2e_step, e2e_steps, args.warmup, stream, d)) / e2e_steps
     assert ap.ap_check() == 0
-    if not torch.equal(yh[:4096], (xh[:4096] * 2.0)):
+    if not (torch.equal(yh[:4096], (xh[:4096] * 2.0)) and torch.equal(yh[-4096:], (xh[-4096:] * 2.0))):
         raise RuntimeError("end-to-end output check failed")
 
     peak, peak_kind = hbm_peak()
@@ -352,6 +401,7 @@ def bench_scale(args, d: Dist) -> dict:
             "h2d_bytes_per_step": 4 * n,
             "d2h_bytes_per_step": 4 * n,
             "steps": e2e_steps,
+            "pipeline": f"{E2E_CHUNKS} chunks; H2D, ap_scale and D2H on three streams",
             "ms_per_step": round(ms_e2e, 4),
         },
         "gpu_launches": args.steps,
@@ -446,6 +496,8 @@ def sweep(which: str, args):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     groups = ["scale", "poly", "roll", "exchange", "small"] if which == "all" else which.split(",")
 
+    window = {}
+
     def line(workload, kernel, nbytes, ms, **extra):
         gb = _gbs(nbytes, ms)
         d = {"workload": workload, "kernel": kernel, "ms": round(ms, 5), "GB/s": round(gb, 1),
@@ -453,10 +505,17 @@ def sweep(which: str, args):
         d.update(extra)
         if ap.ap_check() != 0:
             d["device_status"] = "error"
+        d["_window"] = (window["t0"], window["t1"])
         return d
 
     def run(fn):
-        return time_steps(fn, steps, warm, stream) / steps
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        window["t0"] = datetime.datetime.now()
+        ms = time_steps(fn, steps, 0, stream) / steps
+        window["t1"] = datetime.datetime.now()
+        return ms
 
     if "scale" in groups or "tune" in groups:
         n_t, t = SCALE_TILES, SCALE_TILE
@@ -464,37 +523,57 @@ def sweep(which: str, args):
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
         y = torch.empty_like(x)
         if "scale" in groups:
-            yield line("scale 2^28 f32", "scale_sync", 8 * n, run(lambda: ap.ap_scale_sync(x, y, n_t, t, 2.0)))
+            ms = run(lambda: ap.ap_scale_sync(x, y, n_t, t, 2.0))
+            yield line("scale 2^28 f32", "scale_sync", 8 * n, ms)
             for S in (2, 3, 4, 5, 6):
                 ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
                 yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
                            grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
         if "tune" in groups:
-            for S in (2, 4):
-                for cps in (1, 2):
-                    for kib in (8, 16, 32, 48, 64, 96):
-                        if S * (kib * 1024 + 112) * cps > 228 * 1024:
-                            continue
-                        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                        ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
-                        yield line("scale 2^28 f32", f"ring S={S} stage={kib}KiB ctas/SM={cps}", 8 * n, ms)
+            cands = [(2, 16, 2), (2, 12, 3), (2, 32, 1), (2, 48, 1), (2, 24, 2), (2, 8, 4), (2, 16, 3),
+                     (3, 24, 1), (3, 8, 3), (3, 12, 2), (3, 16, 2), (3, 32, 1), (3, 64, 1),
+                     (4, 16, 1), (4, 8, 2), (4, 12, 2), (4, 24, 1), (4, 48, 1),
+                     (5, 12, 1), (5, 16, 1), (5, 8, 2), (5, 36, 1),
+                     (6, 8, 2), (6, 12, 1), (6, 16, 1), (6, 32, 1)]
+            reps = {c: [] for c in cands}
+            for _ in range(5):  # interleaved repetitions: drift hits every candidate alike
+                for S, kib, cps in cands:
+                    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                    ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                    reps[(S, kib, cps)].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S)))
             ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
             ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
+            for (S, kib, cps), v in reps.items():
+                v = sorted(v)
+                yield line("scale 2^28 f32", f"ring S={S} stage={kib}KiB ctas/SM={cps} (median of 5)", 8 * n,
+                           v[len(v) // 2], min_ms=round(v[0], 5), max_ms=round(v[-1], 5),
+                           ring_kib_per_sm=S * kib * cps)
         del x, y
     if "poly" in groups:
         n = 1 << 30
         x = synth.uniform_pm1_torch(synth.SEED_POLY, n, dev)
         y = torch.empty_like(x)
-        for K in (0, 8, 32, 128):
-            c = synth.coeffs_np(K).tolist()
-            for S in (2, 3, 4, 6):
-                ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
-                tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
-                yield line("poly 2^30 f32", f"ring S={S} K={K}", 8 * n, ms, fp32_tflops=round(tflops, 2),
-                           fma_per_elem=K)
-        del x, y
+        for warps in (8, 16):
+            ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+            for K in (0, 8, 32, 128):
+                c = synth.coeffs_np(K).tolist()
+                for S in (2, 3, 4, 6):
+                    ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
+                    tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
+                    yield line("poly 2^30 f32", f"ring S={S} K={K} warps={warps}", 8 * n, ms,
+                               fp32_tflops=round(tflops, 2), fma_per_elem=K)
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 0)
+        # the FP32 roof measured under the same conditions: register-only fma chains
+        probe = torch.empty(sms * 1024, dtype=torch.float32, device=dev)
+        iters = 1 << 16
+        ms = run(lambda: ap.ap_debug_fma_probe(probe, probe.numel(), iters))
+        tfma = sms * 1024 * 16 * iters / (ms * 1e-3) / 1e12
+        d = line("fp32 fma probe (registers only)", "fma_probe_kernel", 0, ms, fp32_tflops=round(2 * tfma, 2))
+        d.pop("GB/s")
+        d.pop("frac_of_measured_hbm")
+        yield d
+        del x, y, probe
     if "roll" in groups:
         rows, cols = 1 << 26, 4
         n = rows * cols
@@ -510,18 +589,115 @@ def sweep(which: str, args):
         n = 1 << 28
         x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
         y = torch.empty_like(x)
-        for cs in (1, 2, 4, 8):
-            ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
-            yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster cs={cs}", 8 * n, ms,
-                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        for store in (2, 1):
+            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+            for piece_kib in (4, 8, 16, 32):
+                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
+                for cs in (1, 2, 4, 8):
+                    ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
+                    yield line("exchange 2^28 f32, 32 KiB chunks",
+                               f"cluster cs={cs} piece={piece_kib}KiB store={'tma' if store == 1 else 'warps'}",
+                               8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
+                               slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         del x, y
+    if "e2e" in groups:
+        n_t, t = SCALE_TILES, SCALE_TILE
+        n = n_t * t
+        x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
+        xh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        xh.copy_(x)
+        yh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        xd = torch.empty_like(x)
+        yd = torch.empty_like(x)
+        main = torch.cuda.current_stream()
+        for chunks in (1, 4, 8, 16, 32):
+            for n_in in (1, 2):
+                s_in = [torch.cuda.Stream() for _ in range(n_in)]
+                s_out = [torch.cuda.Stream() for _ in range(n_in)]
+                s_c = torch.cuda.Stream()
+                per = n_t // chunks
+
+                def step():
+                    ev0 = torch.cuda.Event()
+                    ev0.record(main)
+                    done = []
+                    for c in range(chunks):
+                        a, b = c * per * t, (c + 1) * per * t
+                        si, so = s_in[c % n_in], s_out[c % n_in]
+                        si.wait_event(ev0)
+                        with torch.cuda.stream(si):
+                            xd[a:b].copy_(xh[a:b], non_blocking=True)
+                        e1 = torch.cuda.Event()
+                        e1.record(si)
+                        s_c.wait_event(e1)
+                        ap.ap_scale(xd[a:b], yd[a:b], per, t, 2.0, 2, s_c)
+                        e2 = torch.cuda.Event()
+                        e2.record(s_c)
+                        so.wait_event(e2)
+                        with torch.cuda.stream(so):
+                            yh[a:b].copy_(yd[a:b], non_blocking=True)
+                        e3 = torch.cuda.Event()
+                        e3.record(so)
+                        done.append(e3)
+                    for e in done:
+                        main.wait_event(e)
+
+                for _ in range(3):
+                    step()
+                torch.cuda.synchronize()
+                window["t0"] = datetime.datetime.now()
+                ms = time_steps(step, 10, 0, main)
+                window["t1"] = datetime.datetime.now()
+                ok = torch.equal(yh[-4096:], xh[-4096:] * 2.0)
+                yield line("e2e scale 2^28 f32 pinned host", f"chunks={chunks} copy_streams={n_in}", 8 * n, ms / 10,
+                           output_ok=ok)
+        del x, xd, yd
     if "small" in groups:
         A = torch.arange(256, dtype=torch.float32, device=dev).reshape(64, 4)
         B = torch.empty_like(A)
         ms = run(lambda: ap.ap_row_roll(A, B, 64, 4, 1))
         yield {"workload": "roll 64x4 f32 (one CTA, 64 threads)", "kernel": "roll_small",
-               "us_per_call": round(ms * 1e3, 2), "note": "launch-latency bound; no roofline"}
+               "us_per_call": round(ms * 1e3, 2), "note": "launch-latency bound; no roofline",
+               "_window": (window["t0"], window["t1"])}
     yield {"workload": "device", "sms": sms, "hbm_peak_gbs": peak}
+
+
+# ----------------------------------------------------------------------------- profiling cases
+
+PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "exchange4")
+
+
+def profile_case(name: str, args):
+    """Run one kernel on a small case (inputs still larger than L2, a few
+    hundred MiB on the device) `warmup + steps` times, for ncu captures."""
+    import torch
+
+    import async_global_shared_gb300 as ap
+    import synth
+
+    dev = torch.device("cuda", 0)
+    n = 1 << 26  # 256 MiB in + 256 MiB out
+    x = synth.uniform_pm1_torch(synth.SEED_SCALE, n + 4, dev)
+    y = torch.empty_like(x)
+    calls = {
+        "scale": lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, 2),
+        "sync": lambda: ap.ap_scale_sync(x[:n], y[:n], n // 256, 256, 2.0),
+        "poly32": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 3),
+        "poly128": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(128).tolist(), 128, 3),
+        "roll": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
+        "roll_mis": lambda: ap.ap_row_roll(x[1:n + 1], y[:n], n // 4, 4, 1),
+        "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
+    }
+    fn = calls[name]
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    st = ap.ap_check()
+    print(json.dumps({"profile_case": name, "launches": args.warmup + args.steps, "status": st}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
 
 
 def main(argv=None):
@@ -532,6 +708,7 @@ def main(argv=None):
     ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap_.add_argument("--workload", default="scale")
     ap_.add_argument("--no-cpu-baseline", action="store_true")
+    ap_.add_argument("--profile-case", choices=PROFILE_CASES, default=None)
     args = ap_.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -543,12 +720,23 @@ def main(argv=None):
         import __graft_entry__
 
         __graft_entry__.build()
-        if args.workload == "scale":
+        if args.profile_case:
+            if d.rank == 0:
+                profile_case(args.profile_case, args)
+        elif args.workload == "scale":
             res = bench_scale(args, d)
             if d.rank == 0:
                 print(json.dumps(res), flush=True)
         elif d.rank == 0:
-            for line in sweep(args.workload, args):
+            with ClockSampler(0) as clk:
+                lines = list(sweep(args.workload, args))
+            rows = clk._rows()
+            if clk.path and os.path.exists(clk.path):
+                os.unlink(clk.path)
+            for line in lines:
+                w = line.pop("_window", None)
+                if w is not None:
+                    line["clocks"] = clk.window(w[0], w[1], rows)
                 print(json.dumps(line), flush=True)
     finally:
         d.close()

@@ -31,6 +31,9 @@ typedef enum ap_debug_key {
     AP_DBG_GRID = 5,            /* cap on the number of CTAs of ring kernels (0 = automatic) */
     AP_DBG_CTAS_PER_SM = 6,     /* resident ring CTAs per SM the grid is sized for (0 = 1) */
     AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 4) */
+    AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8 or 16 (0 = 8) */
+    AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
+                                   piece to a shared->global bulk copy, 2 eight warps of 16-byte stores */
     /* read-only: what the last call on this process launched */
     AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange */
     AP_DBG_LAST_GRID = 101,     /* CTAs launched */
@@ -47,6 +50,16 @@ ap_status ap_debug_set(int key, int64_t value);
 
 /* Read any key; -1 for an unknown key. */
 int64_t ap_debug_get(int key);
+
+/*
+ * FP32 FMA throughput probe: each thread of a grid sized to the device runs
+ * 16 independent fmaf chains of `iters` steps on registers only and writes
+ * one float (the chains' sum) to out[thread]; the number of threads launched
+ * is min(out_elems, SMs * 1024) rounded down to whole CTAs of 512. Timing a
+ * call gives the achievable fma rate that bounds ap_poly at high degree.
+ * out is a device array of out_elems floats.
+ */
+ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
 
 /*
  * Host emulation of one ring call's data movement, for checking the

@@ -37,6 +37,8 @@ def reset_debug(ap):
         ap.AP_DBG_GRID,
         ap.AP_DBG_CTAS_PER_SM,
         ap.AP_DBG_ROLL_STAGES,
+        ap.AP_DBG_CONSUMER_WARPS,
+        ap.AP_DBG_EXCHANGE_STORE,
     ):
         ap.ap_debug_set(key, 0)
 

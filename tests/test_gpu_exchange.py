@@ -18,20 +18,24 @@ def ap():
     reset_debug(ap)
 
 
+@pytest.mark.parametrize("store", [1, 2])
 @pytest.mark.parametrize("cs", [1, 2, 4, 8])
 @pytest.mark.parametrize("chunk_bytes,groups", [(16, 1), (16, 37), (48, 5), (1024, 300), (32768, 3), (100000, 4)])
-def test_exchange_small(ap, orc, cs, chunk_bytes, groups):
+def test_exchange_small(ap, orc, cs, chunk_bytes, groups, store):
     dev = device()
     n = groups * cs * chunk_bytes // 4
     x = synth.uniform_pm1_torch(n + cs, n, dev)
     want = orc.cluster_exchange(to_np(x), cs, chunk_bytes)
-    for grid in (0, cs):  # cs: a single cluster walks every group through its ring
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+    for grid, piece in ((0, 0), (cs, 0), (cs, 16), (0, 4096)):  # grid cs: one cluster walks every group
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece)
         out = Guarded(n, 0, dev)
         ap.ap_cluster_exchange(x, out.view, n, cs, chunk_bytes)
         assert ap.ap_check() == ap.AP_OK
         assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 4
-        assert_bits(to_np(out.view), want, f"exchange cs={cs} chunk={chunk_bytes} groups={groups} grid={grid}")
+        assert_bits(to_np(out.view), want,
+                    f"exchange cs={cs} chunk={chunk_bytes} groups={groups} grid={grid} piece={piece} store={store}")
         assert out.intact()
 
 
@@ -55,7 +59,10 @@ def test_exchange_full_size(ap, orc, cs):
     dev = device()
     n = 1 << 28
     x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
-    y = torch.empty_like(x)
-    ap.ap_cluster_exchange(x, y, n, cs, 32768)
-    assert ap.ap_check() == ap.AP_OK
-    assert_bits(to_np(y), orc.cluster_exchange(to_np(x), cs, 32768), f"full exchange cs={cs}")
+    want = orc.cluster_exchange(to_np(x), cs, 32768)
+    for store in (0, 1, 2):
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+        y = torch.full_like(x, float("nan"))
+        ap.ap_cluster_exchange(x, y, n, cs, 32768)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(y), want, f"full exchange cs={cs} store={store}")

@@ -44,7 +44,8 @@ def test_ring_wait_times_out_and_recovers(ap, orc):
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "after recovery")
 
 
-def test_exchange_wait_times_out_and_recovers(ap, orc):
+@pytest.mark.parametrize("store", [1, 2])
+def test_exchange_wait_times_out_and_recovers(ap, orc, store):
     import torch
 
     dev = device()
@@ -53,6 +54,7 @@ def test_exchange_wait_times_out_and_recovers(ap, orc):
     x = synth.uniform_pm1_torch(4, n, dev)
     y = torch.empty_like(x)
     _inject(ap)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
     ap.ap_cluster_exchange(x, y, n, 4, 4096)
     assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
     reset_debug(ap)

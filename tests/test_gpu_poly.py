@@ -18,7 +18,7 @@ def ap():
     reset_debug(ap)
 
 
-@pytest.mark.parametrize("degree", [0, 1, 2, 8, 32, 128, 1023])
+@pytest.mark.parametrize("degree", [0, 1, 2, 3, 4, 5, 7, 8, 32, 127, 128, 1023])
 @pytest.mark.parametrize("stages", [2, 3, 4, 6])
 def test_poly_small(ap, orc, degree, stages):
     dev = device()
@@ -26,13 +26,14 @@ def test_poly_small(ap, orc, degree, stages):
     x = synth.uniform_pm1_torch(n + degree, n, dev)
     c = synth.coeffs_np(degree)
     want = orc.poly(to_np(x), c)
-    for stage_bytes, grid in ((256, 2), (0, 0)):
+    for stage_bytes, grid, warps in ((256, 2, 8), (0, 0, 0), (1024, 3, 16), (0, 0, 16)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
         out = Guarded(n, 0, dev)
         ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
         assert ap.ap_check() == ap.AP_OK
-        assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} stage={stage_bytes}")
+        assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} stage={stage_bytes} warps={warps}")
         assert out.intact()
 
 

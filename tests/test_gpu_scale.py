@@ -28,9 +28,11 @@ def test_scale_small_many_stages(ap, orc, stages, n_tiles, tile):
     x = synth.uniform_pm1_torch(n + 17, n, dev)
     want = orc.scale(to_np(x), 2.0)
     # tiny stages and few CTAs: every ring slot goes through many phases
-    for stage_bytes, grid in ((64, 1), (256, 3), (1024, 0)):
+    for stage_bytes, grid, warps, cps in ((64, 1, 8, 0), (256, 3, 16, 0), (1024, 0, 0, 3), (0, 0, 0, 0)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
         out = Guarded(n, 0, dev)
         ap.ap_scale(x, out.view, n_tiles, tile, 2.0, stages)
         assert ap.ap_check() == ap.AP_OK
