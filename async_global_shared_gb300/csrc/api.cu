@@ -400,6 +400,22 @@ ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n
                 const uint32_t o = sp.span[0].region + sp.span[0].lead + static_cast<uint32_t>(4 * (e - sp.lo));
                 if (o % 16 || o != smem_offset_of_output(sp, e)) fail();
             }
+            if (shifted_words(sp)) {
+                // the kernel reads two aligned words per group and picks the
+                // four inputs out of them: check the words and the picks
+                const uint32_t o0 = group_input_offset(sp);
+                const uint32_t d = o0 & 15u;
+                const uint32_t w = o0 - d + static_cast<uint32_t>(16 * q);
+                const uint32_t region_end = sp.span[0].region + static_cast<uint32_t>((4 * sp.len1 + 32 + 15) & ~int64_t(15));
+                if (d == 0 || d % 4 || w + 32 > region_end || w + 32 > g.slot_bytes) {
+                    fail();
+                    break;
+                }
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t pick = w + d + 4u * static_cast<uint32_t>(t);
+                    if (pick != smem_offset_of_output(sp, e + t)) fail();
+                }
+            }
             for (int t = 0; t < 4; ++t) store(e + t, read(e + t));
         }
         for (int64_t e = sp.lo; e < sp.e_al; ++e) store(e, read(e));

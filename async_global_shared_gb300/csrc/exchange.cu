@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
                           int64_t chunk_bytes, cudaStream_t stream) {
     // Piece: the largest multiple of 16 dividing chunk_bytes that is at most
-    // the target (8 KiB, or the stage-bytes setting).
-    const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 8192;
+    // the target (16 KiB, or the stage-bytes setting). Measured on GB300 with
+    // 32 KiB chunks: 16 KiB pieces beat whole chunks (more slots in flight)
+    // and beat 4-8 KiB pieces (the single-thread roles' per-piece cost).
+    const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 16384;
     const int64_t units = chunk_bytes / 16;
     int64_t piece_units = 1;
     for (int64_t d = 1; d * d <= units; ++d) {
@@ -252,7 +254,10 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
         if (16 * b <= target && b > piece_units) piece_units = b;
     }
     const int64_t piece = 16 * piece_units;
-    const int64_t budget = di.smem_optin - 512;
+    // Shared memory per CTA when `cps` CTAs share an SM (228 KiB per SM, 1 KiB
+    // reserved per CTA): more resident CTAs let clusters of 8 fill more SMs.
+    const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 1;
+    const int64_t budget = std::min<int64_t>(di.smem_optin, kSmemPerSM / cps - 1024) - 512;
     int64_t S = budget / (2 * piece);
     if (S < 1) return AP_ERR_SMEM;
     if (S > kExMaxSlots) S = kExMaxSlots;

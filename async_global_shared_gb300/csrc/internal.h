@@ -53,8 +53,14 @@ struct OpArgs {
 // lcm(4, unit) when that fits (so a stage holds whole tiles / rows).
 int64_t stage_elems_for(int64_t payload_bytes, int64_t unit);
 
-// Default stage payload for a ring of `stages` slots.
-int64_t auto_stage_payload(int stages);
+// Default ring shape for an op and ring depth: stage payload bytes, CTAs
+// per SM the grid is sized for, consumer warps per CTA.
+struct RingShape {
+    int64_t payload;
+    int64_t ctas_per_sm;
+    int64_t consumer_warps;
+};
+RingShape auto_ring_shape(OpKind kind, int stages);
 
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
                       int64_t unit, int stages, const OpArgs& op, cudaStream_t stream);
@@ -72,6 +78,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
 
 // Largest chunk accepted by ap_cluster_exchange for this much shared memory.
 constexpr int64_t kSmemOptinGB300 = 232448;  // 227 KiB per CTA on compute capability 10.x
+constexpr int64_t kSmemPerSM = 233472;       // 228 KiB per SM
 constexpr int64_t kRollSmallMaxBytes = 32 * 1024;
 
 }  // namespace ap

@@ -167,6 +167,20 @@ AP_HD void plan_stage(const StreamGeom& g, int64_t j, StagePlan* p) {
     p->vec = (p->nspans == 1) && (((p->span[0].lead + 4 * (e_al - lo)) & 15) == 0);
 }
 
+// Slot-relative shared-memory byte offset of the input of the first aligned
+// output group (output e_al).
+AP_HD uint32_t group_input_offset(const StagePlan& p) {
+    return p.span[0].region + p.span[0].lead + static_cast<uint32_t>(4 * (p.e_al - p.lo));
+}
+
+// Stages whose inputs lie in one span but 4, 8 or 12 bytes off the 16-byte
+// grid relative to the output: group q's four inputs are the last 16 - d
+// bytes of the aligned word at w0 + 16q and the first d bytes of the next
+// word (w0 = group_input_offset - d). Both words lie inside the span's
+// region: the next word of the last group ends at most lead + 4L + 16 bytes
+// into a region of at least 4L + 32 bytes.
+AP_HD bool shifted_words(const StagePlan& p) { return !p.vec && p.nspans == 1; }
+
 // Slot-relative shared-memory byte offset of the input that output e reads.
 AP_HD uint32_t smem_offset_of_output(const StagePlan& p, int64_t e) {
     const int64_t q = e - p.lo;

@@ -139,6 +139,27 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Sta
             P.op.apply(v, cs);
             dst[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
+    } else if (shifted_words(sp)) {
+        // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
+        // 16-byte shared loads per group (bank-conflict free) instead of four
+        // 4-byte loads that conflict four ways across the warp.
+        const uint32_t o0 = group_input_offset(sp);
+        const uint32_t d = o0 & 15u;
+        const unsigned char* wbase = slot + (o0 - d);
+        for (int64_t q = ct; q < ngroups; q += kConsumers) {
+            const float4 a = *reinterpret_cast<const float4*>(wbase + 16 * q);
+            const float4 b = *reinterpret_cast<const float4*>(wbase + 16 * q + 16);
+            float v[4];
+            if (d == 4) {
+                v[0] = a.y, v[1] = a.z, v[2] = a.w, v[3] = b.x;
+            } else if (d == 8) {
+                v[0] = a.z, v[1] = a.w, v[2] = b.x, v[3] = b.y;
+            } else {
+                v[0] = a.w, v[1] = b.x, v[2] = b.y, v[3] = b.z;
+            }
+            P.op.apply(v, cs);
+            *reinterpret_cast<float4*>(out + sp.e_al + 4 * q) = make_float4(v[0], v[1], v[2], v[3]);
+        }
     } else {
         for (int64_t q = ct; q < ngroups; q += kConsumers) {
             const int64_t e = sp.e_al + 4 * q;
@@ -305,14 +326,26 @@ int64_t stage_elems_for(int64_t payload_bytes, int64_t unit) {
     return se / 4 * 4;
 }
 
-int64_t auto_stage_payload(int stages) {
-    const int64_t per = (196 * 1024) / stages / 4096 * 4096;
-    return std::min<int64_t>(64 * 1024, per);
+RingShape auto_ring_shape(OpKind kind, int stages) {
+    // Measured on GB300 (2^28-float scale and 2^30-float polynomial, median of
+    // interleaved repetitions): data movement peaks with about 64-96 KiB of
+    // ring per SM in 8-24 KiB stages; larger rings lose bandwidth. The
+    // fma-heavy polynomial wants 16 consumer warps and large stages.
+    if (kind == OP_POLY) return RingShape{stages <= 3 ? 64 * 1024 : 32 * 1024, 1, 16};
+    switch (stages) {
+        case 2: return RingShape{16 * 1024, 2, 8};
+        case 3: return RingShape{24 * 1024, 1, 8};
+        case 4: return RingShape{16 * 1024, 1, 8};
+        default: return RingShape{8 * 1024, 2, 8};
+    }
 }
 
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
                       int64_t unit, int stages, const OpArgs& op, cudaStream_t stream) {
-    const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : auto_stage_payload(stages);
+    const RingShape shape = auto_ring_shape(op.kind, stages);
+    const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : shape.payload;
+    const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : shape.ctas_per_sm;
+    const int64_t warps = o.consumer_warps > 0 ? o.consumer_warps : shape.consumer_warps;
     const int64_t se = stage_elems_for(payload, unit);
     StreamGeom g;
     make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
@@ -320,7 +353,6 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     const int64_t coef_bytes = op.kind == OP_POLY ? (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
     const int64_t smem = coef_off + coef_bytes;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
-    const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 1;
     int64_t grid = std::min<int64_t>(g.n_stages, static_cast<int64_t>(di.sms) * cps);
     if (o.grid > 0) grid = std::min<int64_t>(grid, o.grid);
     if (grid < 1) grid = 1;
@@ -337,12 +369,12 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
         case OP_COPY: {
             RingParams<OpCopyDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
                                     static_cast<uint32_t>(coef_off), OpCopyDev{}};
-            return launch_ring_warps(di, o.consumer_warps, P, grid, smem, stream);
+            return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
         case OP_SCALE: {
             RingParams<OpScaleDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
                                      static_cast<uint32_t>(coef_off), OpScaleDev{op.alpha}};
-            return launch_ring_warps(di, o.consumer_warps, P, grid, smem, stream);
+            return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
@@ -356,7 +388,7 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             P.coef_off = static_cast<uint32_t>(coef_off);
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
-            return launch_ring_warps(di, o.consumer_warps, P, grid, smem, stream);
+            return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
     }
     return AP_ERR_ARG;

@@ -554,15 +554,27 @@ def sweep(which: str, args):
         n = 1 << 30
         x = synth.uniform_pm1_torch(synth.SEED_POLY, n, dev)
         y = torch.empty_like(x)
-        for warps in (8, 16):
-            ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
-            for K in (0, 8, 32, 128):
+        for K in (0, 8, 32, 128):
+            c = synth.coeffs_np(K).tolist()
+            for S in (2, 3, 4, 6):
+                ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
+                tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
+                yield line("poly 2^30 f32", f"ring S={S} K={K} (defaults)", 8 * n, ms,
+                           fp32_tflops=round(tflops, 2), fma_per_elem=K,
+                           stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+        if "polytune" in groups:
+            for K in (32, 128):
                 c = synth.coeffs_np(K).tolist()
-                for S in (2, 3, 4, 6):
-                    ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
-                    tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
-                    yield line("poly 2^30 f32", f"ring S={S} K={K} warps={warps}", 8 * n, ms,
-                               fp32_tflops=round(tflops, 2), fma_per_elem=K)
+                for S in (2, 4, 6):
+                    for kib in (16, 24, 32, 48):
+                        if S * kib > 200:
+                            continue
+                        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                        ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
+                        tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
+                        yield line("poly 2^30 f32", f"ring S={S} K={K} stage={kib}KiB", 8 * n, ms,
+                                   fp32_tflops=round(tflops, 2), fma_per_elem=K)
+                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 0)
         # the FP32 roof measured under the same conditions: register-only fma chains
         probe = torch.empty(sms * 1024, dtype=torch.float32, device=dev)
@@ -580,25 +592,35 @@ def sweep(which: str, args):
         abuf = torch.empty(n + 4, dtype=torch.float32, device=dev)
         bbuf = torch.empty(n + 4, dtype=torch.float32, device=dev)
         synth.uniform_pm1_torch(synth.SEED_ROLL, n + 4, dev, out=abuf)
-        for name, sa, sb in (("aligned", 0, 0), ("A+4B", 1, 0), ("B+4B", 0, 1), ("A+4B,B+4B", 1, 1)):
-            A, B = abuf[sa:sa + n], bbuf[sb:sb + n]
-            ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
-            yield line("roll 2^26x4 f32", f"ring {name}", 8 * n, ms, flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
+        for S in (0, 2, 3, 6) if "rolltune" in groups else (0,):
+            ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
+            for name, sa, sb in (("aligned", 0, 0), ("A+4B", 1, 0), ("B+4B", 0, 1), ("A+4B,B+4B", 1, 1)):
+                A, B = abuf[sa:sa + n], bbuf[sb:sb + n]
+                ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
+                yield line("roll 2^26x4 f32", f"ring {name} S={S or 'default'}", 8 * n, ms,
+                           flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
         del abuf, bbuf
     if "exchange" in groups:
         n = 1 << 28
         x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
         y = torch.empty_like(x)
-        for store in (2, 1):
+        for store, piece_kib, cps in ((2, 16, 1), (2, 16, 2), (2, 16, 3), (2, 12, 2), (2, 32, 2), (1, 16, 2)):
             ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
-            for piece_kib in (4, 8, 16, 32):
-                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
-                for cs in (1, 2, 4, 8):
-                    ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
-                    yield line("exchange 2^28 f32, 32 KiB chunks",
-                               f"cluster cs={cs} piece={piece_kib}KiB store={'tma' if store == 1 else 'warps'}",
-                               8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
-                               slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
+            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+            for cs in (1, 2, 4, 8):
+                ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
+                yield line("exchange 2^28 f32, 32 KiB chunks",
+                           f"cluster cs={cs} piece={piece_kib}KiB ctas/SM={cps} store={'tma' if store == 1 else 'warps'}",
+                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
+                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+        for cs in (1, 2, 4, 8):
+            ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
+            yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster cs={cs} (defaults)", 8 * n, ms,
+                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         del x, y
