@@ -241,10 +241,12 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
                           int64_t chunk_bytes, cudaStream_t stream) {
     // Piece: the largest multiple of 16 dividing chunk_bytes that is at most
-    // the target (16 KiB, or the stage-bytes setting). Measured on GB300 with
-    // 32 KiB chunks: 16 KiB pieces beat whole chunks (more slots in flight)
-    // and beat 4-8 KiB pieces (the single-thread roles' per-piece cost).
-    const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 16384;
+    // the target (8 KiB, or the stage-bytes setting), and two CTAs per SM.
+    // Measured on GB300 with 32 KiB chunks: the loader and pusher are single
+    // threads with a fixed cost per piece, so pieces much below 8 KiB starve
+    // them, and a second CTA per SM doubles those threads; whole 32 KiB chunks
+    // leave too few slots in flight.
+    const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 8192;
     const int64_t units = chunk_bytes / 16;
     int64_t piece_units = 1;
     for (int64_t d = 1; d * d <= units; ++d) {
@@ -256,7 +258,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     const int64_t piece = 16 * piece_units;
     // Shared memory per CTA when `cps` CTAs share an SM (228 KiB per SM, 1 KiB
     // reserved per CTA): more resident CTAs let clusters of 8 fill more SMs.
-    const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 1;
+    const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
     const int64_t budget = std::min<int64_t>(di.smem_optin, kSmemPerSM / cps - 1024) - 512;
     int64_t S = budget / (2 * piece);
     if (S < 1) return AP_ERR_SMEM;

@@ -181,6 +181,40 @@ AP_HD uint32_t group_input_offset(const StagePlan& p) {
 // into a region of at least 4L + 32 bytes.
 AP_HD bool shifted_words(const StagePlan& p) { return !p.vec && p.nspans == 1; }
 
+// What the consumers of a stage need, computed once by the producer and
+// stored beside the stage's slot (so consumer threads spend their issue
+// slots on the stage's data, not on re-planning it).
+enum SlotMode : uint32_t { MODE_VEC = 0, MODE_SHIFTED = 1, MODE_SCALAR = 2 };
+
+struct SlotDesc {
+    int64_t lo, hi;        // outputs [lo, hi)
+    int64_t e_al, e_end;   // whole aligned 16-byte output groups [e_al, e_end)
+    int64_t len1;          // outputs [lo, lo + len1) read span 0
+    uint32_t off0, off1;   // slot offsets of span 0's and span 1's first input (region + lead)
+    uint32_t mode;         // SlotMode
+    uint32_t pad_[3];
+};
+static_assert(sizeof(SlotDesc) == 64, "slot descriptor is 64 bytes");
+
+AP_HD void make_slot_desc(const StagePlan& p, SlotDesc* d) {
+    d->lo = p.lo;
+    d->hi = p.hi;
+    d->e_al = p.e_al;
+    d->e_end = p.e_end;
+    d->len1 = p.len1;
+    d->off0 = p.span[0].region + p.span[0].lead;
+    d->off1 = p.nspans == 2 ? p.span[1].region + p.span[1].lead : 0u;
+    d->mode = p.vec ? MODE_VEC : (p.nspans == 1 ? MODE_SHIFTED : MODE_SCALAR);
+    d->pad_[0] = d->pad_[1] = d->pad_[2] = 0;
+}
+
+// Slot offset of the input that output e reads, from a descriptor.
+AP_HD uint32_t desc_offset_of_output(const SlotDesc& d, int64_t e) {
+    const int64_t q = e - d.lo;
+    if (q < d.len1) return d.off0 + static_cast<uint32_t>(4 * q);
+    return d.off1 + static_cast<uint32_t>(4 * (q - d.len1));
+}
+
 // Slot-relative shared-memory byte offset of the input that output e reads.
 AP_HD uint32_t smem_offset_of_output(const StagePlan& p, int64_t e) {
     const int64_t q = e - p.lo;

@@ -109,14 +109,14 @@ __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off
 }
 
 template <int kConsumers, class Op>
-__device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const StagePlan& sp, const unsigned char* slot,
+__device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const SlotDesc& d, const unsigned char* slot,
                                               const float* cs, int ct) {
-    const int64_t ngroups = (sp.e_end - sp.e_al) >> 2;
+    const int64_t ngroups = (d.e_end - d.e_al) >> 2;
     float* __restrict__ out = P.out;
-    if (sp.vec) {
-        const float4* src = reinterpret_cast<const float4*>(slot + sp.span[0].region + sp.span[0].lead +
-                                                            4 * (sp.e_al - sp.lo));
-        float4* dst = reinterpret_cast<float4*>(out + sp.e_al);
+    const uint32_t o0 = d.off0 + static_cast<uint32_t>(4 * (d.e_al - d.lo));  // input of the first group
+    if (d.mode == MODE_VEC) {
+        const float4* src = reinterpret_cast<const float4*>(slot + o0);
+        float4* dst = reinterpret_cast<float4*>(out + d.e_al);
         int64_t q = ct;
         for (; q + (kUnroll - 1) * kConsumers < ngroups; q += kUnroll * kConsumers) {
             float v[4 * kUnroll];
@@ -139,43 +139,42 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Sta
             P.op.apply(v, cs);
             dst[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
-    } else if (shifted_words(sp)) {
+    } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
         // 16-byte shared loads per group (bank-conflict free) instead of four
         // 4-byte loads that conflict four ways across the warp.
-        const uint32_t o0 = group_input_offset(sp);
-        const uint32_t d = o0 & 15u;
-        const unsigned char* wbase = slot + (o0 - d);
+        const uint32_t sh = o0 & 15u;
+        const unsigned char* wbase = slot + (o0 - sh);
         for (int64_t q = ct; q < ngroups; q += kConsumers) {
             const float4 a = *reinterpret_cast<const float4*>(wbase + 16 * q);
             const float4 b = *reinterpret_cast<const float4*>(wbase + 16 * q + 16);
             float v[4];
-            if (d == 4) {
+            if (sh == 4) {
                 v[0] = a.y, v[1] = a.z, v[2] = a.w, v[3] = b.x;
-            } else if (d == 8) {
+            } else if (sh == 8) {
                 v[0] = a.z, v[1] = a.w, v[2] = b.x, v[3] = b.y;
             } else {
                 v[0] = a.w, v[1] = b.x, v[2] = b.y, v[3] = b.z;
             }
             P.op.apply(v, cs);
-            *reinterpret_cast<float4*>(out + sp.e_al + 4 * q) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(out + d.e_al + 4 * q) = make_float4(v[0], v[1], v[2], v[3]);
         }
     } else {
         for (int64_t q = ct; q < ngroups; q += kConsumers) {
-            const int64_t e = sp.e_al + 4 * q;
+            const int64_t e = d.e_al + 4 * q;
             float v[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) v[t] = lds_f32(slot, smem_offset_of_output(sp, e + t));
+            for (int t = 0; t < 4; ++t) v[t] = lds_f32(slot, desc_offset_of_output(d, e + t));
             P.op.apply(v, cs);
             *reinterpret_cast<float4*>(out + e) = make_float4(v[0], v[1], v[2], v[3]);
         }
     }
     // The first stage's unaligned head and the last stage's tail (<= 3 each).
-    const int64_t nh = sp.e_al - sp.lo;
-    const int64_t nt = sp.hi - sp.e_end;
+    const int64_t nh = d.e_al - d.lo;
+    const int64_t nt = d.hi - d.e_end;
     if (ct < nh + nt) {
-        const int64_t e = ct < nh ? sp.lo + ct : sp.e_end + (ct - nh);
-        float v[1] = {lds_f32(slot, smem_offset_of_output(sp, e))};
+        const int64_t e = ct < nh ? d.lo + ct : d.e_end + (ct - nh);
+        float v[1] = {lds_f32(slot, desc_offset_of_output(d, e))};
         P.op.apply(v, cs);
         out[e] = v[0];
     }
@@ -188,7 +187,8 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = P.stages;
     const uint32_t slot_bytes = P.g.slot_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slot_bytes);
+    SlotDesc* descs = reinterpret_cast<SlotDesc*>(smem + static_cast<size_t>(S) * slot_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(descs + S);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S);
     const uint32_t smem_base = ptx::smem_addr(smem);
     const uint32_t bar_base = ptx::smem_addr(bars);
@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             }
             StagePlan sp;
             plan_stage(P.g, j, &sp);
+            make_slot_desc(sp, &descs[s]);  // published to the consumers by the arrive below
             const uint32_t slot = smem_base + static_cast<uint32_t>(s) * slot_bytes;
             bool edges = false;
             uint32_t tx = 0;
@@ -275,9 +276,8 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
         w = __shfl_sync(0xffffffffu, w, 0);
         if (w != WAIT_OK) break;
         __syncwarp();  // orders lane 0's observation of the phase before the other lanes' reads
-        StagePlan sp;
-        plan_stage(P.g, j, &sp);
-        consume_stage<kConsumers>(P, sp, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
+        const SlotDesc d = descs[s];
+        consume_stage<kConsumers>(P, d, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty(s));
     }
@@ -349,7 +349,8 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     const int64_t se = stage_elems_for(payload, unit);
     StreamGeom g;
     make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
-    const int64_t coef_off = static_cast<int64_t>(stages) * g.slot_bytes + 2 * 8 * stages + 16;
+    const int64_t coef_off =
+        static_cast<int64_t>(stages) * (g.slot_bytes + static_cast<int64_t>(sizeof(SlotDesc))) + 2 * 8 * stages + 16;
     const int64_t coef_bytes = op.kind == OP_POLY ? (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
     const int64_t smem = coef_off + coef_bytes;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
