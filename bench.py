@@ -634,8 +634,31 @@ def sweep(which: str, args):
         xd = torch.empty_like(x)
         yd = torch.empty_like(x)
         main = torch.cuda.current_stream()
-        for chunks in (1, 4, 8, 16, 32):
-            for n_in in (1, 2):
+        # the host link alone: one direction at a time, then both at once
+        s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+        ms = run(lambda: xd.copy_(xh, non_blocking=True))
+        yield line("host link", "H2D 1 GiB pinned", 4 * n, ms)
+        ms = run(lambda: yh.copy_(yd, non_blocking=True))
+        yield line("host link", "D2H 1 GiB pinned", 4 * n, ms)
+
+        def both():
+            ev = torch.cuda.Event()
+            ev.record(main)
+            s_a.wait_event(ev)
+            s_b.wait_event(ev)
+            with torch.cuda.stream(s_a):
+                xd.copy_(xh, non_blocking=True)
+            with torch.cuda.stream(s_b):
+                yh.copy_(yd, non_blocking=True)
+            for st in (s_a, s_b):
+                e = torch.cuda.Event()
+                e.record(st)
+                main.wait_event(e)
+
+        ms = run(both)
+        yield line("host link", "H2D + D2H 1 GiB each, concurrent", 8 * n, ms)
+        for chunks in (16,):
+            for n_in in (1,):
                 s_in = [torch.cuda.Stream() for _ in range(n_in)]
                 s_out = [torch.cuda.Stream() for _ in range(n_in)]
                 s_c = torch.cuda.Stream()
