@@ -32,18 +32,22 @@
 namespace ap {
 namespace {
 
-constexpr int kUnroll = 4;  // 16-byte groups per consumer thread per iteration
 
 // Each op: stage() copies whatever the op reads from shared memory (only
 // the polynomial's coefficients) before the ring starts; apply() transforms
 // N values held in registers.
+// kGroups: 16-byte groups a consumer thread keeps in flight per iteration
+// (4 for data movement; 8 for the polynomial, i.e. 32 independent Horner
+// chains per thread).
 struct OpCopyDev {
+    static constexpr int kGroups = 4;
     __device__ __forceinline__ void stage(float*, int, int) const {}
     template <int N>
     __device__ __forceinline__ void apply(float (&)[N], const float*) const {}
 };
 
 struct OpScaleDev {
+    static constexpr int kGroups = 4;
     float alpha;
     __device__ __forceinline__ void stage(float*, int, int) const {}
     template <int N>
@@ -58,6 +62,7 @@ struct OpScaleDev {
 // read from shared memory four at a time (one 16-byte broadcast load per four
 // fma steps per chain), highest power first.
 struct OpPolyDev {
+    static constexpr int kGroups = 8;
     int degree;
     float c[AP_POLY_MAX_DEGREE + 1];
     __device__ __forceinline__ void stage(float* cs, int tid, int nthreads) const {
@@ -108,6 +113,28 @@ __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off
     return *reinterpret_cast<const float*>(slot + off);
 }
 
+// Groups q, q + kConsumers, ..., U at a time while U whole groups remain;
+// advances q past them.
+template <int U, int kConsumers, class Op>
+__device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4* src, float4* dst, int64_t& q,
+                                           int64_t ngroups, const float* cs) {
+    for (; q + (U - 1) * kConsumers < ngroups; q += U * kConsumers) {
+        float v[4 * U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float4 t = src[q + u * kConsumers];
+            v[4 * u + 0] = t.x;
+            v[4 * u + 1] = t.y;
+            v[4 * u + 2] = t.z;
+            v[4 * u + 3] = t.w;
+        }
+        P.op.apply(v, cs);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    }
+}
+
 template <int kConsumers, class Op>
 __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const SlotDesc& d, const unsigned char* slot,
                                               const float* cs, int ct) {
@@ -118,27 +145,11 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         const float4* src = reinterpret_cast<const float4*>(slot + o0);
         float4* dst = reinterpret_cast<float4*>(out + d.e_al);
         int64_t q = ct;
-        for (; q + (kUnroll - 1) * kConsumers < ngroups; q += kUnroll * kConsumers) {
-            float v[4 * kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const float4 t = src[q + u * kConsumers];
-                v[4 * u + 0] = t.x;
-                v[4 * u + 1] = t.y;
-                v[4 * u + 2] = t.z;
-                v[4 * u + 3] = t.w;
-            }
-            P.op.apply(v, cs);
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        }
-        for (; q < ngroups; q += kConsumers) {
-            const float4 t = src[q];
-            float v[4] = {t.x, t.y, t.z, t.w};
-            P.op.apply(v, cs);
-            dst[q] = make_float4(v[0], v[1], v[2], v[3]);
-        }
+        // 16 consumer warps get at most 120 registers a thread: 4 groups then
+        constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
+        vec_groups<kG, kConsumers>(P, src, dst, q, ngroups, cs);
+        if (kG > 4) vec_groups<4, kConsumers>(P, src, dst, q, ngroups, cs);
+        vec_groups<1, kConsumers>(P, src, dst, q, ngroups, cs);
     } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
         // 16-byte shared loads per group (bank-conflict free) instead of four

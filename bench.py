@@ -531,11 +531,9 @@ def sweep(which: str, args):
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
                            grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
         if "tune" in groups:
-            cands = [(2, 16, 2), (2, 12, 3), (2, 32, 1), (2, 48, 1), (2, 24, 2), (2, 8, 4), (2, 16, 3),
-                     (3, 24, 1), (3, 8, 3), (3, 12, 2), (3, 16, 2), (3, 32, 1), (3, 64, 1),
-                     (4, 16, 1), (4, 8, 2), (4, 12, 2), (4, 24, 1), (4, 48, 1),
-                     (5, 12, 1), (5, 16, 1), (5, 8, 2), (5, 36, 1),
-                     (6, 8, 2), (6, 12, 1), (6, 16, 1), (6, 32, 1)]
+            cands = [(2, 16, 2), (2, 12, 3), (3, 24, 1), (3, 8, 3), (4, 16, 1), (4, 8, 2),
+                     (5, 12, 1), (5, 16, 1), (5, 8, 2), (5, 36, 1), (5, 24, 1), (5, 6, 3), (5, 4, 4),
+                     (6, 8, 2), (6, 12, 1), (6, 16, 1), (6, 32, 1), (6, 4, 3), (6, 6, 2), (6, 24, 1)]
             reps = {c: [] for c in cands}
             for _ in range(5):  # interleaved repetitions: drift hits every candidate alike
                 for S, kib, cps in cands:
@@ -562,6 +560,19 @@ def sweep(which: str, args):
                 yield line("poly 2^30 f32", f"ring S={S} K={K} (defaults)", 8 * n, ms,
                            fp32_tflops=round(tflops, 2), fma_per_elem=K,
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+        if "polywarps" in groups:
+            for K in (8, 32, 128):
+                c = synth.coeffs_np(K).tolist()
+                for warps in (8, 16):
+                    ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+                    for S, kib in ((2, 64), (3, 64), (4, 48), (4, 32), (6, 32), (2, 96), (3, 48)):
+                        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                        ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
+                        tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
+                        yield line("poly 2^30 f32", f"ring S={S} K={K} warps={warps} stage={kib}KiB", 8 * n, ms,
+                                   fp32_tflops=round(tflops, 2), fma_per_elem=K)
+            ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 0)
+            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         if "polytune" in groups:
             for K in (32, 128):
                 c = synth.coeffs_np(K).tolist()
