@@ -37,8 +37,7 @@ namespace {
 // the polynomial's coefficients) before the ring starts; apply() transforms
 // N values held in registers.
 // kGroups: 16-byte groups a consumer thread keeps in flight per iteration
-// (4 for data movement; 8 for the polynomial, i.e. 32 independent Horner
-// chains per thread).
+// (4 groups = 16 values; for the polynomial, 16 independent Horner chains).
 struct OpCopyDev {
     static constexpr int kGroups = 4;
     __device__ __forceinline__ void stage(float*, int, int) const {}
@@ -62,7 +61,7 @@ struct OpScaleDev {
 // read from shared memory four at a time (one 16-byte broadcast load per four
 // fma steps per chain), highest power first.
 struct OpPolyDev {
-    static constexpr int kGroups = 8;
+    static constexpr int kGroups = 4;
     int degree;
     float c[AP_POLY_MAX_DEGREE + 1];
     __device__ __forceinline__ void stage(float* cs, int tid, int nthreads) const {
@@ -145,10 +144,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         const float4* src = reinterpret_cast<const float4*>(slot + o0);
         float4* dst = reinterpret_cast<float4*>(out + d.e_al);
         int64_t q = ct;
-        // 16 consumer warps get at most 120 registers a thread: 4 groups then
-        constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
-        vec_groups<kG, kConsumers>(P, src, dst, q, ngroups, cs);
-        if (kG > 4) vec_groups<4, kConsumers>(P, src, dst, q, ngroups, cs);
+        vec_groups<Op::kGroups, kConsumers>(P, src, dst, q, ngroups, cs);
         vec_groups<1, kConsumers>(P, src, dst, q, ngroups, cs);
     } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
@@ -338,16 +334,22 @@ int64_t stage_elems_for(int64_t payload_bytes, int64_t unit) {
 }
 
 RingShape auto_ring_shape(OpKind kind, int stages) {
-    // Measured on GB300 (2^28-float scale and 2^30-float polynomial, median of
+    // Measured on GB300 (2^28-float scale and 2^30-float polynomial, medians of
     // interleaved repetitions): data movement peaks with about 64-96 KiB of
-    // ring per SM in 8-24 KiB stages; larger rings lose bandwidth. The
-    // fma-heavy polynomial wants 16 consumer warps and large stages.
-    if (kind == OP_POLY) return RingShape{stages <= 3 ? 64 * 1024 : 32 * 1024, 1, 16};
+    // ring per SM in 16-24 KiB stages for depths 2-4; larger rings lose
+    // bandwidth. The fma-heavy polynomial wants 16 consumer warps and the
+    // largest stages that fit, since every stage costs each consumer warp a
+    // barrier wait, a descriptor read and a release.
+    if (kind == OP_POLY) {
+        const int64_t per = (196 * 1024) / stages / 4096 * 4096;
+        return RingShape{std::min<int64_t>(96 * 1024, per), 1, 16};
+    }
     switch (stages) {
         case 2: return RingShape{16 * 1024, 2, 8};
         case 3: return RingShape{24 * 1024, 1, 8};
         case 4: return RingShape{16 * 1024, 1, 8};
-        default: return RingShape{8 * 1024, 2, 8};
+        case 5: return RingShape{36 * 1024, 1, 8};
+        default: return RingShape{32 * 1024, 1, 8};
     }
 }
 
