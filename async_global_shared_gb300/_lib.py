@@ -48,6 +48,7 @@ AP_DBG_CTAS_PER_SM = 6
 AP_DBG_ROLL_STAGES = 7
 AP_DBG_CONSUMER_WARPS = 8
 AP_DBG_EXCHANGE_STORE = 9
+AP_DBG_CACHE_HINTS = 10
 AP_DBG_LAST_PATH = 100
 AP_DBG_LAST_GRID = 101
 AP_DBG_LAST_STAGE_ELEMS = 102

@@ -29,6 +29,7 @@ std::atomic<int64_t> g_ctas_per_sm{0};
 std::atomic<int64_t> g_roll_stages{0};
 std::atomic<int64_t> g_consumer_warps{0};
 std::atomic<int64_t> g_ex_tma_store{0};
+std::atomic<int64_t> g_cache_hints{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0};
@@ -114,6 +115,7 @@ Options options() {
     o.roll_stages = g_roll_stages.load();
     o.consumer_warps = g_consumer_warps.load();
     o.ex_tma_store = g_ex_tma_store.load();
+    o.cache_hints = g_cache_hints.load();
     return o;
 }
 
@@ -288,6 +290,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 2) return AP_ERR_ARG;
             g_ex_tma_store = value;
             return AP_OK;
+        case AP_DBG_CACHE_HINTS:
+            if (value > 3) return AP_ERR_ARG;
+            g_cache_hints = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -304,6 +310,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_ROLL_STAGES: return o.roll_stages;
         case AP_DBG_CONSUMER_WARPS: return o.consumer_warps;
         case AP_DBG_EXCHANGE_STORE: return o.ex_tma_store;
+        case AP_DBG_CACHE_HINTS: return o.cache_hints;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

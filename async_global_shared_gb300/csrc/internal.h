@@ -31,6 +31,7 @@ struct Options {
     int64_t roll_stages;
     int64_t consumer_warps;
     int64_t ex_tma_store;
+    int64_t cache_hints;
 };
 
 Options options();

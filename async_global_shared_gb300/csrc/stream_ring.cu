@@ -105,8 +105,17 @@ struct RingParams {
     uint64_t timeout_ns;
     uint32_t* status;
     uint32_t coef_off;  // byte offset of the op's staged data in dynamic shared memory
+    uint32_t hints;     // bit 0: loads marked L2 evict-first; bit 1: streaming (.cs) stores
     Op op;
 };
+
+__device__ __forceinline__ void store4(float4* p, float4 v, uint32_t hints) {
+    if (hints & 2u) {
+        __stcs(p, v);
+    } else {
+        *p = v;
+    }
+}
 
 __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off) {
     return *reinterpret_cast<const float*>(slot + off);
@@ -130,7 +139,8 @@ __device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4
         P.op.apply(v, cs);
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            store4(&dst[q + u * kConsumers], make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]),
+                   P.hints);
     }
 }
 
@@ -164,7 +174,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
                 v[0] = a.w, v[1] = b.x, v[2] = b.y, v[3] = b.z;
             }
             P.op.apply(v, cs);
-            *reinterpret_cast<float4*>(out + d.e_al + 4 * q) = make_float4(v[0], v[1], v[2], v[3]);
+            store4(reinterpret_cast<float4*>(out + d.e_al + 4 * q), make_float4(v[0], v[1], v[2], v[3]), P.hints);
         }
     } else {
         for (int64_t q = ct; q < ngroups; q += kConsumers) {
@@ -222,6 +232,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     if (warp == 0) {
         if (lane != 0) return;
         // ------------------------------------------------ producer (one thread)
+        const uint64_t l2_policy = (P.hints & 1u) ? ptx::l2_evict_first_policy() : 0;
         int64_t issued = 0;
         for (int64_t j = blockIdx.x; j < T; j += G, ++issued) {
             const int s = static_cast<int>(issued % S);
@@ -254,9 +265,14 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             ptx::mbar_arrive_expect_tx(full(s), tx + P.tx_extra);
             for (int k = 0; k < sp.nspans; ++k) {
                 const Span& sn = sp.span[k];
-                if (sn.bulk_bytes)
+                if (sn.bulk_bytes == 0) continue;
+                if (P.hints & 1u) {
+                    ptx::bulk_g2s_hint(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes,
+                                       full(s), l2_policy);
+                } else {
                     ptx::bulk_g2s(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes,
                                   full(s));
+                }
             }
         }
         // Never leave with copies in flight: wait (bounded) for the last
@@ -378,16 +394,17 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     record_launch(PATH_RING, grid, se, smem, stages, flags);
 
     const uint64_t timeout = static_cast<uint64_t>(o.timeout_ns);
+    const uint32_t hints = static_cast<uint32_t>(o.cache_hints);
     const uint32_t tx_extra = static_cast<uint32_t>(o.tx_extra);
     switch (op.kind) {
         case OP_COPY: {
             RingParams<OpCopyDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
-                                    static_cast<uint32_t>(coef_off), OpCopyDev{}};
+                                    static_cast<uint32_t>(coef_off), hints, OpCopyDev{}};
             return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
         case OP_SCALE: {
             RingParams<OpScaleDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
-                                     static_cast<uint32_t>(coef_off), OpScaleDev{op.alpha}};
+                                     static_cast<uint32_t>(coef_off), hints, OpScaleDev{op.alpha}};
             return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
         case OP_POLY: {
@@ -400,6 +417,7 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             P.timeout_ns = timeout;
             P.status = di.status;
             P.coef_off = static_cast<uint32_t>(coef_off);
+            P.hints = hints;
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, P, grid, smem, stream);

@@ -517,7 +517,7 @@ def sweep(which: str, args):
         window["t1"] = datetime.datetime.now()
         return ms
 
-    if "scale" in groups or "tune" in groups:
+    if "scale" in groups or "tune" in groups or "hints" in groups:
         n_t, t = SCALE_TILES, SCALE_TILE
         n = n_t * t
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
@@ -530,6 +530,17 @@ def sweep(which: str, args):
                 yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
                            grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+        if "hints" in groups:
+            reps = {h: [] for h in (0, 1, 2, 3)}
+            for _ in range(5):
+                for h in reps:
+                    ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, h)
+                    reps[h].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, 2)))
+            ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, 0)
+            for h, v in reps.items():
+                v = sorted(v)
+                yield line("scale 2^28 f32", f"ring S=2 cache_hints={h} (median of 5)", 8 * n, v[2],
+                           min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
         if "tune" in groups:
             cands = [(2, 16, 2), (2, 12, 3), (3, 24, 1), (3, 8, 3), (4, 16, 1), (4, 8, 2),
                      (5, 12, 1), (5, 16, 1), (5, 8, 2), (5, 36, 1), (5, 24, 1), (5, 6, 3), (5, 4, 4),

@@ -34,6 +34,8 @@ typedef enum ap_debug_key {
     AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8 or 16 (0 = 8) */
     AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
                                    piece to a shared->global bulk copy, 2 eight warps of 16-byte stores */
+    AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: bit 0 bulk loads carry an L2 evict-first policy,
+                                   bit 1 consumer stores are streaming (st.global.cs); 0 = none */
     /* read-only: what the last call on this process launched */
     AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange */
     AP_DBG_LAST_GRID = 101,     /* CTAs launched */

@@ -39,6 +39,7 @@ def reset_debug(ap):
         ap.AP_DBG_ROLL_STAGES,
         ap.AP_DBG_CONSUMER_WARPS,
         ap.AP_DBG_EXCHANGE_STORE,
+        ap.AP_DBG_CACHE_HINTS,
     ):
         ap.ap_debug_set(key, 0)
 

@@ -133,3 +133,20 @@ def test_device_generator_matches_host(ap):
     idx = np.random.default_rng(0).integers(0, n, 4096)
     got = to_np(t[torch.from_numpy(idx).to(dev)])
     assert_bits(got, synth.uniform_pm1_np(synth.SEED_POLY, n)[idx], "device generator")
+
+
+@pytest.mark.parametrize("hints", [1, 2, 3])
+def test_scale_cache_hints(ap, orc, hints):
+    """L2 evict-first loads and streaming stores change no result."""
+    import torch
+
+    dev = device()
+    n_tiles, tile = 4099, 256
+    x = synth.uniform_pm1_torch(hints, n_tiles * tile, dev)
+    ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, hints)
+    for stages in (2, 5):
+        out = Guarded(n_tiles * tile, 1, dev)
+        ap.ap_scale(x, out.view, n_tiles, tile, 2.0, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), orc.scale(to_np(x), 2.0), f"hints={hints} S={stages}")
+        assert out.intact()
