@@ -48,6 +48,9 @@ class Oracle:
         lib.orc_poly.restype = ctypes.c_int
         lib.orc_cluster_exchange.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64]
         lib.orc_cluster_exchange.restype = ctypes.c_int
+        lib.orc_cluster_exchange_ex.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                                ctypes.c_int64]
+        lib.orc_cluster_exchange_ex.restype = ctypes.c_int
         self._lib = lib
 
     def scale(self, x, alpha: float) -> np.ndarray:
@@ -84,6 +87,16 @@ class Oracle:
         rc = self._lib.orc_cluster_exchange(_ptr(x), _ptr(y), x.size, int(cluster_size), int(chunk_bytes))
         if rc != 0:
             raise ValueError("orc_cluster_exchange rejected the sizes")
+        return y
+
+
+    def cluster_exchange_ex(self, x, cluster_size: int, chunk_bytes: int, shift: int) -> np.ndarray:
+        x = _f32(x).ravel()
+        y = np.empty_like(x)
+        rc = self._lib.orc_cluster_exchange_ex(_ptr(x), _ptr(y), x.size, int(cluster_size), int(chunk_bytes),
+                                               int(shift))
+        if rc != 0:
+            raise ValueError("orc_cluster_exchange_ex rejected the sizes")
         return y
 
 

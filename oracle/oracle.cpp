@@ -101,4 +101,35 @@ int orc_cluster_exchange(const float* in, float* out, int64_t n, int cluster_siz
     return 0;
 }
 
+// Generalised cluster hand-off: clusters of any size, any shift within the
+// cluster, and a last group with fewer chunks. The input is cut into chunks of
+// chunk_bytes; consecutive runs of cluster_size chunks form groups, the last
+// group holding the m = chunks mod cluster_size leftover chunks when that is
+// not zero. Within a group of m members, member r receives member
+// (r + shift) mod m:
+//   out chunk (g*cs + r) = in chunk (g*cs + (r + shift) mod m).
+// shift = 1 with whole groups is orc_cluster_exchange. Same page and section
+// as above: a CTA copies a chunk into another CTA of its cluster; the library
+// extends the fixed neighbour to any distance and to a short last cluster.
+// Returns 0, or -1 for sizes that are not whole chunks.
+int orc_cluster_exchange_ex(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes,
+                            int64_t shift) {
+    if (cluster_size < 1 || chunk_bytes < 4 || chunk_bytes % 4 != 0 || n < 0) return -1;
+    const int64_t E = chunk_bytes / 4;
+    if (n % E != 0) return -1;
+    const int64_t chunks = n / E;
+    const int64_t cs = cluster_size;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t group = c / cs;
+        const int64_t first = group * cs;
+        const int64_t left = chunks - first;
+        const int64_t m = left < cs ? left : cs;  // members of this group
+        const int64_t r = c - first;
+        const int64_t s = ((shift % m) + m) % m;
+        const int64_t src = first + (r + s) % m;
+        std::memcpy(out + c * E, in + src * E, (size_t)E * sizeof(float));
+    }
+    return 0;
+}
+
 }  // extern "C"

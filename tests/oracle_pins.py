@@ -278,6 +278,59 @@ def pin_exchange_invariants(orc):
         raise AssertionError(f"partial cluster or chunk accepted: n={bad[0].size} cs={bad[1]} chunk={bad[2]}")
 
 
+def _load_exchange_ex_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "exchange_ex_small.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, tail = line.split(":")
+            n, cs, cb, sh = (int(t) for t in head.split())
+            cases.append((n, cs, cb, sh, [float(t) for t in tail.split()]))
+    return cases
+
+
+def pin_exchange_ex_worked_examples(orc):
+    for n, cs, cb, sh, want in _load_exchange_ex_golden():
+        got = orc.cluster_exchange_ex(np.arange(n, dtype=np.float32), cs, cb, sh)
+        assert got.tolist() == want, f"n={n} cs={cs} chunk={cb} shift={sh}: {got.tolist()} != {want}"
+
+
+def pin_exchange_ex_library(orc):
+    """Against numpy: whole groups as a (groups, cs, E) view rolled by -shift on
+    the rank axis, the short last group as an (m, E) view rolled alike."""
+    for cs in (1, 2, 3, 4, 5, 8, 16):
+        for E in (1, 3):
+            for chunks in (cs, 3 * cs, 3 * cs + 1, 2 * cs + cs // 2 + 1):
+                n = chunks * E
+                x = synth.uniform_pm1_np(7000 + n + cs, n)
+                G, m = divmod(chunks, cs)
+                for shift in (0, 1, 2, -1, cs - 1, 7, -13):
+                    full = np.roll(x[: G * cs * E].reshape(G, cs, E), -shift, axis=1).reshape(-1)
+                    tail = np.roll(x[G * cs * E:].reshape(m, E), -shift, axis=0).reshape(-1) if m else x[:0]
+                    want = np.concatenate([full, tail])
+                    got = orc.cluster_exchange_ex(x, cs, 4 * E, shift)
+                    assert_bits_equal(got, want, f"cs={cs} E={E} chunks={chunks} shift={shift}")
+
+
+def pin_exchange_ex_invariants(orc):
+    x = synth.uniform_pm1_np(4242, 38 * 4)  # 38 chunks of 4 floats: a short last group for cs 3, 4, 6
+    for cs in (2, 3, 4, 6):
+        assert_bits_equal(orc.cluster_exchange_ex(x, cs, 16, 0), x, f"cs={cs} shift 0 is the identity")
+        for a, b in ((1, 2), (3, -1), (5, 5)):
+            once = orc.cluster_exchange_ex(orc.cluster_exchange_ex(x, cs, 16, a), cs, 16, b)
+            assert_bits_equal(once, orc.cluster_exchange_ex(x, cs, 16, a + b), f"cs={cs} compose {a}+{b}")
+        y = orc.cluster_exchange_ex(x, cs, 16, 1)
+        assert sorted(map(tuple, y.reshape(-1, 4).tolist())) == sorted(map(tuple, x.reshape(-1, 4).tolist()))
+    try:
+        orc.cluster_exchange_ex(x[:-1], 4, 16, 1)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a partial chunk was accepted")
+
+
 ALL_PINS = [
     pin_roll_worked_example,
     pin_roll_brute_force,
@@ -290,6 +343,9 @@ ALL_PINS = [
     pin_exchange_worked_examples,
     pin_exchange_library,
     pin_exchange_invariants,
+    pin_exchange_ex_worked_examples,
+    pin_exchange_ex_library,
+    pin_exchange_ex_invariants,
 ]
 
 

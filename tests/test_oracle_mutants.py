@@ -30,6 +30,9 @@ MUTANTS = {
     "exchange_wrong_direction": ("(r + 1) % cs", "(r + cs - 1) % cs"),
     "exchange_drops_group": ("group * cs + (r + 1) % cs", "(r + 1) % cs"),
     "exchange_accepts_partial": ("if (n % (E * cs) != 0) return -1;", ""),
+    "exchange_ex_last_group_uses_cs": ("const int64_t m = left < cs ? left : cs;", "const int64_t m = cs;"),
+    "exchange_ex_shift_sign": ("const int64_t s = ((shift % m) + m) % m;", "const int64_t s = ((-shift % m) + m) % m;"),
+    "exchange_ex_ignores_shift": ("const int64_t src = first + (r + s) % m;", "const int64_t src = first + (r + 1) % m;"),
 }
 
 
