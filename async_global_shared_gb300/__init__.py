@@ -17,6 +17,7 @@ __all__ = [
     "ap_row_roll",
     "ap_poly",
     "ap_cluster_exchange",
+    "ap_cluster_exchange_ex",
     "ap_check",
     "ap_status_string",
     "ap_debug_set",

@@ -63,6 +63,7 @@ EXPORTED = (
     "ap_row_roll",
     "ap_poly",
     "ap_cluster_exchange",
+    "ap_cluster_exchange_ex",
     "ap_check",
     "ap_status_string",
     "ap_debug_set",
@@ -100,6 +101,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_row_roll.argtypes = [vp, vp, _i64, _i64, _i64, vp]
     lib.ap_poly.argtypes = [vp, vp, _i64, vp, ctypes.c_int, ctypes.c_int, vp]
     lib.ap_cluster_exchange.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, vp]
+    lib.ap_cluster_exchange_ex.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, _i64, vp]
     lib.ap_check.argtypes = [vp]
     lib.ap_status_string.argtypes = [ctypes.c_int]
     lib.ap_status_string.restype = ctypes.c_char_p
@@ -108,7 +110,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_get.restype = _i64
     lib.ap_debug_emulate_ring.argtypes = [vp, vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _i64]
     lib.ap_debug_fma_probe.argtypes = [vp, _i64, _i64, vp]
-    for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange", "ap_check",
+    for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange",
+                 "ap_cluster_exchange_ex", "ap_check",
                  "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_fma_probe"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
@@ -180,6 +183,11 @@ def ap_poly(inp, out, n: int, coeffs, degree: int, stages: int, stream=None):
 def ap_cluster_exchange(inp, out, n: int, cluster_size: int, chunk_bytes: int, stream=None):
     _check(load().ap_cluster_exchange(_addr(inp), _addr(out), n, cluster_size, chunk_bytes, _stream(stream)),
            "ap_cluster_exchange")
+
+
+def ap_cluster_exchange_ex(inp, out, n: int, cluster_size: int, chunk_bytes: int, shift: int, stream=None):
+    _check(load().ap_cluster_exchange_ex(_addr(inp), _addr(out), n, cluster_size, chunk_bytes, shift,
+                                         _stream(stream)), "ap_cluster_exchange_ex")
 
 
 def ap_check(stream=None) -> int:

@@ -48,6 +48,7 @@ struct ExParams {
     uint32_t piece_bytes;  // divides chunk_bytes, multiple of 16
     int pieces;            // chunk_bytes / piece_bytes
     int cs;                // cluster size
+    int shift;             // rank r receives from rank (r + shift) mod cs, 0 <= shift < cs
     int stages;            // ring slots per direction
     int tma_store;         // receiver stores with bulk copies (1) or with 8 warps (0)
     uint32_t tx_extra;
@@ -71,8 +72,9 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
 
     const uint32_t cs = static_cast<uint32_t>(P.cs);
     const uint32_t rank = ptx::cluster_ctarank();
-    const uint32_t dst_rank = (rank + cs - 1) % cs;  // receives this CTA's chunk
-    const uint32_t src_rank = (rank + 1) % cs;       // sends this CTA its chunk
+    const uint32_t sh = static_cast<uint32_t>(P.shift);
+    const uint32_t dst_rank = (rank + cs - sh) % cs;  // receives this CTA's chunk
+    const uint32_t src_rank = (rank + sh) % cs;       // sends this CTA its chunk
     const int64_t cid = ptx::cluster_id_x();
     const int64_t ncl = ptx::nclusters_x();
     const int64_t count = (cid < P.groups ? (P.groups - cid + ncl - 1) / ncl : 0) * NP;
@@ -238,8 +240,8 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
 
 }  // namespace
 
-ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
-                          int64_t chunk_bytes, cudaStream_t stream) {
+ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t groups, int cs,
+                          int64_t chunk_bytes, int64_t shift, cudaStream_t stream) {
     // Piece: the largest multiple of 16 dividing chunk_bytes that is at most
     // the target (8 KiB, or the stage-bytes setting), and two CTAs per SM.
     // Measured on GB300 with 32 KiB chunks: the loader and pusher are single
@@ -270,12 +272,12 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     if (di.device < 0 || di.device >= 64) return AP_ERR_CUDA;
     if (!configured[di.device]) {
         if (cudaFuncSetAttribute(exchange_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(exchange_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return AP_ERR_CUDA;
         configured[di.device] = true;
     }
 
-    const int64_t groups = (4 * n) / (static_cast<int64_t>(cs) * chunk_bytes);
     ExParams P{in,
                out,
                groups,
@@ -283,6 +285,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
                static_cast<uint32_t>(piece),
                static_cast<int>(chunk_bytes / piece),
                cs,
+               static_cast<int>(((shift % cs) + cs) % cs),
                static_cast<int>(S),
                o.ex_tma_store == 1 ? 1 : 0,
                static_cast<uint32_t>(o.tx_extra),
@@ -302,8 +305,11 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
     int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, exchange_kernel, &cfg) != cudaSuccess || max_clusters < 1)
-        return AP_ERR_CUDA;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, exchange_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // clear: an unsupported cluster shape is an argument error, not a sticky one
+        return cs > AP_MAX_CLUSTER ? AP_ERR_CLUSTER : AP_ERR_CUDA;
+    }
+    if (max_clusters < 1) return AP_ERR_CLUSTER;
     int64_t ncl = std::min<int64_t>(groups, max_clusters);
     if (o.grid > 0) ncl = std::max<int64_t>(1, std::min<int64_t>(ncl, o.grid / cs));
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs), 1, 1);

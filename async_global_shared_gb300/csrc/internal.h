@@ -74,8 +74,10 @@ ap_status launch_scale_sync(const DeviceInfo& di, const float* in, float* out, i
 
 ap_status launch_fma_probe(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
 
-ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int cs,
-                          int64_t chunk_bytes, cudaStream_t stream);
+// `groups` whole groups of cs chunks starting at in/out; rank r receives
+// rank (r + shift) mod cs.
+ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t groups, int cs,
+                          int64_t chunk_bytes, int64_t shift, cudaStream_t stream);
 
 // Largest chunk accepted by ap_cluster_exchange for this much shared memory.
 constexpr int64_t kSmemOptinGB300 = 232448;  // 227 KiB per CTA on compute capability 10.x

@@ -50,7 +50,7 @@ typedef enum ap_status {
     AP_ERR_ALIGN = 3,              /* pointer not aligned as the call requires */
     AP_ERR_ALIAS = 4,              /* input and output overlap in a way the call forbids */
     AP_ERR_STAGES = 5,             /* ring depth outside [AP_MIN_STAGES, AP_MAX_STAGES] */
-    AP_ERR_CLUSTER = 6,            /* cluster size not in {1, 2, 4, 8} */
+    AP_ERR_CLUSTER = 6,            /* cluster size not supported by the call */
     AP_ERR_SMEM = 7,               /* the requested tiles do not fit in shared memory */
     AP_ERR_CUDA = 8,               /* a CUDA runtime call failed (launch, sync, attribute) */
     AP_ERR_DEVICE_TIMEOUT = 9,     /* a kernel wait gave up (reported by ap_check) */
@@ -62,6 +62,7 @@ typedef enum ap_status {
 #define AP_MAX_STAGES 6
 #define AP_POLY_MAX_DEGREE 1023
 #define AP_MAX_CLUSTER 8
+#define AP_MAX_CLUSTER_NONPORTABLE 16
 
 /*
  * ap_scale: out[i] = alpha * in[i] for i < n_tiles * tile_elems.
@@ -152,6 +153,31 @@ ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, i
  */
 ap_status ap_cluster_exchange(const float* in, float* out, int64_t n, int cluster_size,
                               int64_t chunk_bytes, cudaStream_t stream);
+
+/*
+ * ap_cluster_exchange_ex: the cluster hand-off generalised to any cluster
+ * size from 1 to 16, any distance within the cluster, and a short last group.
+ * The input is cut into chunks of chunk_bytes; consecutive runs of
+ * cluster_size chunks form groups, the last group holding the
+ * m = chunks mod cluster_size leftover chunks when that is not zero. Within a
+ * group of m members (m = cluster_size for whole groups) member r receives
+ * member (r + shift) mod m:
+ *     out chunk (g * cs + r) = in chunk (g * cs + (r + shift) mod m).
+ * shift = 1 with whole groups is ap_cluster_exchange. Source: "Asynchronous
+ * Copies" (TVM TIRx guide), section Copies between CTAs, a CTA copying a
+ * chunk into another CTA of its cluster; the pages fix neither the distance
+ * nor how a short last cluster behaves, and this call defines both.
+ *  in, out       as ap_cluster_exchange (16-byte aligned, not overlapping).
+ *  n             >= 0; n * 4 must be a multiple of chunk_bytes (AP_ERR_SHAPE).
+ *  cluster_size  1..16 (AP_ERR_CLUSTER otherwise; sizes above 8 use the
+ *                non-portable cluster attribute and return AP_ERR_CLUSTER if
+ *                the device cannot place such a cluster).
+ *  chunk_bytes   as ap_cluster_exchange.
+ *  shift         any value, reduced modulo the group's member count.
+ * A short last group runs as a second launch with a cluster of m CTAs.
+ */
+ap_status ap_cluster_exchange_ex(const float* in, float* out, int64_t n, int cluster_size,
+                                 int64_t chunk_bytes, int64_t shift, cudaStream_t stream);
 
 /*
  * ap_check: waits for `stream`, then returns and clears the device status

@@ -90,6 +90,14 @@ def test_validation_before_cuda(ap):
     assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1000, 4, 32768, None) == ap.AP_ERR_SHAPE
     assert raw(ap, "ap_cluster_exchange", FAKE_IN + 4, FAKE_OUT, 1 << 20, 2, 32768, None) == ap.AP_ERR_ALIGN
     assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_IN, 1 << 20, 2, 32768, None) == ap.AP_ERR_ALIAS
+    ex = "ap_cluster_exchange_ex"
+    assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1 << 20, 0, 32768, 1, None) == ap.AP_ERR_CLUSTER
+    assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1 << 20, 17, 32768, 1, None) == ap.AP_ERR_CLUSTER
+    assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1000, 3, 32768, 1, None) == ap.AP_ERR_SHAPE  # not whole chunks
+    assert raw(ap, ex, FAKE_IN, FAKE_OUT, 12, 3, 24, 1, None) == ap.AP_ERR_SHAPE  # chunk not a multiple of 16
+    assert raw(ap, ex, FAKE_IN, FAKE_OUT, 0, 5, 32768, 7, None) == ap.AP_OK
+    assert raw(ap, ex, FAKE_IN + 8, FAKE_OUT, 1 << 20, 5, 32768, 7, None) == ap.AP_ERR_ALIGN
+    assert raw(ap, ex, FAKE_IN, FAKE_IN + 16, 1 << 20, 5, 32768, 7, None) == ap.AP_ERR_ALIAS
 
 
 def test_debug_settings_roundtrip(ap):
