@@ -69,6 +69,7 @@ EXPORTED = (
     "ap_debug_set",
     "ap_debug_get",
     "ap_debug_emulate_ring",
+    "ap_debug_emulate_ring_tensor",
     "ap_debug_fma_probe",
 )
 
@@ -110,9 +111,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_get.restype = _i64
     lib.ap_debug_emulate_ring.argtypes = [vp, vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _i64]
     lib.ap_debug_fma_probe.argtypes = [vp, _i64, _i64, vp]
+    lib.ap_debug_emulate_ring_tensor.argtypes = [vp, vp, _i64, _i64, _i64, _i64, _i64]
     for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange",
                  "ap_cluster_exchange_ex", "ap_check",
-                 "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_fma_probe"):
+                 "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_emulate_ring_tensor", "ap_debug_fma_probe"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -214,6 +216,16 @@ def ap_debug_emulate_ring(in_host, out_host, n: int, off: int, in_mis: int, out_
     assert in_host.dtype == np.float32 and out_host.dtype == np.float32
     return load().ap_debug_emulate_ring(in_host.ctypes.data, out_host.ctypes.data, n, off, in_mis, out_mis,
                                         stage_elems)
+
+
+def ap_debug_emulate_ring_tensor(in_host, out_host, rows: int, cols: int, shift: int, box_rows: int,
+                                 stage_elems: int) -> int:
+    """Host emulation of the tensor-map row shift (numpy float32 arrays); returns the status code."""
+    import numpy as np
+
+    assert in_host.dtype == np.float32 and out_host.dtype == np.float32
+    return load().ap_debug_emulate_ring_tensor(in_host.ctypes.data, out_host.ctypes.data, rows, cols, shift,
+                                               box_rows, stage_elems)
 
 
 def ap_debug_fma_probe(out, out_elems: int, iters: int, stream=None):

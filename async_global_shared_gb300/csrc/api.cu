@@ -166,7 +166,7 @@ ap_status ap_scale(const float* in, float* out, int64_t n_tiles, int64_t tile_el
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     OpArgs op{OP_SCALE, alpha, 0, nullptr};
-    return launch_ring(di, options(), in, out, n, 0, tile_elems, stages, op, stream);
+    return launch_ring(di, options(), in, out, n, 0, tile_elems, stages, op, 0, stream);
 }
 
 ap_status ap_scale_sync(const float* in, float* out, int64_t n_tiles, int64_t tile_elems, float alpha,
@@ -203,11 +203,16 @@ ap_status ap_row_roll(const float* A, float* B, int64_t rows, int64_t cols, int6
     if (st != AP_OK) return st;
     const int64_t s = ((shift % rows) + rows) % rows;
     const bool small = 4 * n <= kRollSmallMaxBytes;
-    if ((small && o.force_path != 1) || (o.force_path == 2 && small)) {
+    if (small && (o.force_path == 0 || o.force_path == 2)) {
         return launch_roll_small(di, A, B, rows, cols, s, stream);
     }
     OpArgs op{OP_COPY, 1.0f, 0, nullptr};
-    return launch_ring(di, o, A, B, n, s * cols, cols, stages, op, stream);
+    // The tensor-map producer (2-D boxes of whole rows) on request, where the
+    // matrix meets its alignment rules; the 1-D bulk producer otherwise.
+    const bool tensor_ok = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0 &&
+                           cols % 4 == 0 && cols <= 256 && rows < (int64_t(1) << 30);
+    const int64_t tensor_cols = (o.force_path == 3 && tensor_ok) ? cols : 0;
+    return launch_ring(di, o, A, B, n, s * cols, cols, stages, op, tensor_cols, stream);
 }
 
 ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, int degree, int stages,
@@ -223,7 +228,7 @@ ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, i
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     OpArgs op{OP_POLY, 0.0f, degree, coeffs};
-    return launch_ring(di, options(), in, out, n, 0, 1, stages, op, stream);
+    return launch_ring(di, options(), in, out, n, 0, 1, stages, op, 0, stream);
 }
 
 ap_status ap_cluster_exchange(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes,
@@ -292,7 +297,7 @@ ap_status ap_debug_set(int key, int64_t value) {
     if (value < 0) return AP_ERR_ARG;
     switch (key) {
         case AP_DBG_FORCE_PATH:
-            if (value > 2) return AP_ERR_ARG;
+            if (value > 3) return AP_ERR_ARG;
             g_force_path = value;
             return AP_OK;
         case AP_DBG_EXPECT_TX_EXTRA:
@@ -362,21 +367,17 @@ ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaS
     return launch_fma_probe(di, out, out_elems, iters, stream);
 }
 
-// Host emulation of the ring's data movement (see asyncpipe_debug.h). It
+}  // extern "C"
+
+namespace {
+
+// Host emulation of one ring call's data movement (see asyncpipe_debug.h). It
 // follows the kernel step by step: the producer's copies into a stage slot,
-// then the consumers' reads and stores, using the same planning functions.
-ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n, int64_t off, int in_mis,
-                                int out_mis, int64_t stage_elems) {
-    if (n < 0 || off < 0 || (n > 0 && off >= n)) return AP_ERR_SHAPE;
-    if (in_mis < 0 || in_mis > 12 || in_mis % 4 || out_mis < 0 || out_mis > 12 || out_mis % 4) return AP_ERR_ALIGN;
-    if (stage_elems < 4 || stage_elems % 4) return AP_ERR_SHAPE;
-    if (n == 0) return AP_OK;
-    if (in_host == nullptr || out_host == nullptr) return AP_ERR_NULL;
-    // Pretend device addresses with the requested low bits.
-    const uint64_t in_addr = (uint64_t(1) << 40) + static_cast<uint64_t>(in_mis);
-    const uint64_t out_addr = (uint64_t(3) << 40) + static_cast<uint64_t>(out_mis);
-    StreamGeom g;
-    make_geom(&g, in_addr, out_addr, n, off, stage_elems);
+// then the consumers' reads and stores through the slot descriptor, using the
+// same planning functions.
+ap_status emulate_ring(const StreamGeom& g, const float* in_host, float* out_host) {
+    const int64_t n = g.n;
+    const uint64_t in_addr = g.in_addr, out_addr = g.out_addr;
     const uint64_t in_end = in_addr + 4 * static_cast<uint64_t>(n);
     unsigned char* slot = static_cast<unsigned char*>(std::malloc(g.slot_bytes));
     unsigned char* written = static_cast<unsigned char*>(std::malloc(g.slot_bytes));
@@ -390,7 +391,8 @@ ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n
     const unsigned char* src_bytes = reinterpret_cast<const unsigned char*>(in_host);
     ap_status result = AP_OK;
     auto fail = [&]() { result = AP_ERR_SHAPE; };
-    // copy global [ga, ga + bytes) into slot [dst, dst + bytes)
+    // copy global [ga, ga + bytes) into slot [dst, dst + bytes); bytes past
+    // src_valid are zero (the zero-filling copies)
     auto gcopy = [&](uint32_t dst, uint64_t ga, uint32_t bytes, uint32_t src_valid) {
         if (ga < in_addr || ga + src_valid > in_end || dst + bytes > g.slot_bytes) return fail();
         for (uint32_t b = 0; b < bytes; ++b) {
@@ -405,6 +407,29 @@ ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n
         plan_stage(g, j, &sp);
         for (int k = 0; k < sp.nspans && result == AP_OK; ++k) {
             const Span& sn = sp.span[k];
+            if (g.box_bytes != 0) {
+                // tensor-map boxes: whole rows, rows past the matrix arrive as zeros
+                if (sn.bulk_dst % 128 || sn.x0 % g.cols || sn.bulk_bytes % g.box_bytes) {
+                    fail();
+                    break;
+                }
+                const int64_t box_rows = g.box_elems / g.cols;
+                const int64_t rows = n / g.cols;
+                const uint32_t nbox = sn.bulk_bytes / g.box_bytes;
+                const uint32_t row_bytes = static_cast<uint32_t>(4 * g.cols);
+                for (uint32_t b = 0; b < nbox && result == AP_OK; ++b) {
+                    for (int64_t r = 0; r < box_rows; ++r) {
+                        const int64_t row = sn.x0 / g.cols + b * box_rows + r;
+                        const uint32_t dst = sn.bulk_dst + b * g.box_bytes + static_cast<uint32_t>(r) * row_bytes;
+                        if (row < rows) {
+                            gcopy(dst, in_addr + static_cast<uint64_t>(row) * row_bytes, row_bytes, row_bytes);
+                        } else {
+                            gcopy(dst, in_addr, row_bytes, 0);
+                        }
+                    }
+                }
+                continue;
+            }
             for (int64_t x = sn.x0; x < sn.head_end; ++x)
                 gcopy(sn.region + sn.lead + static_cast<uint32_t>(4 * (x - sn.x0)), in_addr + 4 * x, 4, 4);
             if (sn.tail_begin < sn.x1) {
@@ -473,6 +498,36 @@ ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n
     std::free(written);
     std::free(out_done);
     return result;
+}
+
+}  // namespace
+
+extern "C" {
+
+ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n, int64_t off, int in_mis,
+                                int out_mis, int64_t stage_elems) {
+    if (n < 0 || off < 0 || (n > 0 && off >= n)) return AP_ERR_SHAPE;
+    if (in_mis < 0 || in_mis > 12 || in_mis % 4 || out_mis < 0 || out_mis > 12 || out_mis % 4) return AP_ERR_ALIGN;
+    if (stage_elems < 4 || stage_elems % 4) return AP_ERR_SHAPE;
+    if (n == 0) return AP_OK;
+    if (in_host == nullptr || out_host == nullptr) return AP_ERR_NULL;
+    // Pretend device addresses with the requested low bits.
+    StreamGeom g;
+    make_geom(&g, (uint64_t(1) << 40) + static_cast<uint64_t>(in_mis), (uint64_t(3) << 40) + static_cast<uint64_t>(out_mis),
+              n, off, stage_elems);
+    return emulate_ring(g, in_host, out_host);
+}
+
+ap_status ap_debug_emulate_ring_tensor(const float* in_host, float* out_host, int64_t rows, int64_t cols,
+                                       int64_t shift, int64_t box_rows, int64_t stage_elems) {
+    if (rows < 1 || cols < 4 || cols % 4 || cols > 256) return AP_ERR_SHAPE;
+    if (box_rows < 8 || box_rows % 8 || box_rows > 256) return AP_ERR_SHAPE;
+    if (stage_elems < box_rows * cols || stage_elems % (box_rows * cols)) return AP_ERR_SHAPE;
+    if (in_host == nullptr || out_host == nullptr) return AP_ERR_NULL;
+    const int64_t s = ((shift % rows) + rows) % rows;
+    StreamGeom g;
+    make_geom_tensor(&g, uint64_t(1) << 40, uint64_t(3) << 40, rows * cols, s * cols, stage_elems, cols, box_rows);
+    return emulate_ring(g, in_host, out_host);
 }
 
 }  // extern "C"

@@ -22,9 +22,11 @@ enum WaitSite : uint32_t {
     SITE_EX_PUSHER_LOADED = 5,
     SITE_EX_RECEIVER_FULL = 6,
     SITE_EX_DRAIN = 7,
+    SITE_RING_TENSOR_ALIGN = 8,
 };
 
 constexpr uint32_t kStatusTimeout = 9;  // AP_ERR_DEVICE_TIMEOUT
+constexpr uint32_t kStatusAlign = 3;    // AP_ERR_ALIGN
 
 __device__ __forceinline__ void raise_timeout(uint32_t* status, uint32_t site, volatile int* abort_flag) {
     atomicCAS(status, 0u, kStatusTimeout | (site << 8));

@@ -63,8 +63,10 @@ struct RingShape {
 };
 RingShape auto_ring_shape(OpKind kind, int stages);
 
+// tensor_cols > 0 selects the tensor-map producer for a rows x cols row shift
+// (in and out 16-byte aligned, cols a multiple of 4 and at most 256).
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
-                      int64_t unit, int stages, const OpArgs& op, cudaStream_t stream);
+                      int64_t unit, int stages, const OpArgs& op, int64_t tensor_cols, cudaStream_t stream);
 
 ap_status launch_roll_small(const DeviceInfo& di, const float* A, float* B, int64_t rows, int64_t cols, int64_t s,
                             cudaStream_t stream);

@@ -104,6 +104,22 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
         : "memory");
 }
 
+// Global -> shared copy of one 2-D box described by a tensor map (the TMA
+// engine's descriptor form): box at {c0 = column, c1 = row}; rows past the
+// tensor's end arrive as zeros. completes `box bytes` of transactions on bar.
+// dst 128-byte aligned; the map lives in kernel parameter space.
+__device__ __forceinline__ void tensor_g2s_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // Shared (this CTA) -> shared (a CTA of the cluster) bulk copy, completed on
 // the destination CTA's barrier. dst and bar are shared::cluster addresses.
 __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {

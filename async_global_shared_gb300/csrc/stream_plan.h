@@ -57,6 +57,11 @@ struct StreamGeom {
     int64_t h_in;         // inputs [0, h_in) lie before I0 (4-byte copies)
     int64_t t_in;         // inputs [t_in, n) lie at or after I1 (one zero-filling 16-byte copy)
     uint32_t slot_bytes;  // shared-memory bytes of one stage slot (multiple of 16)
+    // Tensor-map mode (row shift only; 0 = 1-D bulk copies): spans are whole
+    // rows and load as 2-D boxes of box_rows x cols floats.
+    uint32_t box_bytes;   // bytes of one box (multiple of 128), 0 in 1-D mode
+    int64_t box_elems;    // box_rows * cols
+    int64_t cols;         // row length of the tensor
 };
 
 // Bytes of a stage slot for stages of `se` elements: two regions, each the
@@ -89,7 +94,27 @@ AP_HD void make_geom(StreamGeom* g, uint64_t in_addr, uint64_t out_addr, int64_t
         g->t_in = n;
     }
     g->slot_bytes = slot_bytes_for(se);
+    g->box_bytes = 0;
+    g->box_elems = 0;
+    g->cols = 0;
 }
+
+// Tensor-map geometry for the row shift of a rows x cols matrix whose input and
+// output are 16-byte aligned and cols a multiple of 4: off = shift * cols and
+// the stage a whole number of boxes, so every span starts on a row. A span
+// loads ceil(len / box_elems) whole boxes (the last may run past the span, or
+// past the last row, where the engine writes zeros), so each region is sized
+// for whole boxes: slot = 4 se + 2 box_bytes + 256, regions 128-byte aligned.
+AP_HD void make_geom_tensor(StreamGeom* g, uint64_t in_addr, uint64_t out_addr, int64_t n, int64_t off, int64_t se,
+                            int64_t cols, int64_t box_rows) {
+    make_geom(g, in_addr, out_addr, n, off, se);
+    g->cols = cols;
+    g->box_elems = box_rows * cols;
+    g->box_bytes = static_cast<uint32_t>(4 * g->box_elems);
+    g->slot_bytes = static_cast<uint32_t>(4 * se + 2 * static_cast<int64_t>(g->box_bytes) + 256);
+}
+
+AP_HD int64_t boxes_for(const StreamGeom& g, int64_t len) { return (len + g.box_elems - 1) / g.box_elems; }
 
 struct Span {
     int64_t x0, x1;        // input elements [x0, x1)
@@ -116,6 +141,16 @@ AP_HD void plan_span(const StreamGeom& g, int64_t x0, int64_t x1, uint32_t regio
     s->x0 = x0;
     s->x1 = x1;
     s->region = region;
+    if (g.box_bytes != 0) {  // whole rows, aligned: boxes only, no edges
+        s->lead = 0;
+        s->head_end = x0;
+        s->tail_begin = x1;
+        s->tail_dst = 0;
+        s->bulk_src = 0;
+        s->bulk_dst = region;
+        s->bulk_bytes = static_cast<uint32_t>(boxes_for(g, x1 - x0) * g.box_bytes);
+        return;
+    }
     const uint64_t g0 = g.in_addr + 4 * static_cast<uint64_t>(x0);
     const uint64_t a0 = floor16(g0);
     s->lead = static_cast<uint32_t>(g0 - a0);
@@ -155,7 +190,9 @@ AP_HD void plan_stage(const StreamGeom& g, int64_t j, StagePlan* p) {
     plan_span(g, a, a + len1, 0u, &p->span[0]);
     if (len1 < L) {
         p->nspans = 2;
-        const uint32_t r2 = static_cast<uint32_t>((4 * len1 + 32 + 15) & ~int64_t(15));
+        const uint32_t r2 = g.box_bytes != 0
+                                ? static_cast<uint32_t>(boxes_for(g, len1) * g.box_bytes)
+                                : static_cast<uint32_t>((4 * len1 + 32 + 15) & ~int64_t(15));
         plan_span(g, 0, L - len1, r2, &p->span[1]);
     } else {
         p->nspans = 1;

@@ -24,7 +24,11 @@
 // bulk-copy instruction per tile issued by one thread (the TMA engine
 // generates the addresses, "Asynchronous Data Movement", section The Tensor
 // Memory Accelerator) instead of every thread copying a few bytes.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <cstring>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -97,6 +101,7 @@ struct OpPolyDev {
 
 template <class Op>
 struct RingParams {
+    CUtensorMap tmap;   // the row shift's input as a rows x cols tensor (tensor-map mode only)
     const float* in;
     float* out;
     StreamGeom g;
@@ -233,6 +238,15 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
         if (lane != 0) return;
         // ------------------------------------------------ producer (one thread)
         const uint64_t l2_policy = (P.hints & 1u) ? ptx::l2_evict_first_policy() : 0;
+        if (P.g.box_bytes != 0) {
+            // box destinations must be 128-byte aligned: refuse (status, no copy) otherwise
+            if (smem_base & 127u) {
+                atomicCAS(P.status, 0u, kStatusAlign | (SITE_RING_TENSOR_ALIGN << 8));
+                *abort_flag = 1;
+                return;
+            }
+            ptx::prefetch_tensormap(&P.tmap);
+        }
         int64_t issued = 0;
         for (int64_t j = blockIdx.x; j < T; j += G, ++issued) {
             const int s = static_cast<int>(issued % S);
@@ -266,6 +280,16 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             for (int k = 0; k < sp.nspans; ++k) {
                 const Span& sn = sp.span[k];
                 if (sn.bulk_bytes == 0) continue;
+                if (P.g.box_bytes != 0) {
+                    // tensor-map mode: whole boxes of box_rows rows from the span's first row
+                    const int32_t box_rows = static_cast<int32_t>(P.g.box_elems / P.g.cols);
+                    const int32_t row0 = static_cast<int32_t>(sn.x0 / P.g.cols);
+                    const uint32_t nbox = sn.bulk_bytes / P.g.box_bytes;
+                    for (uint32_t b = 0; b < nbox; ++b)
+                        ptx::tensor_g2s_2d(slot + sn.bulk_dst + b * P.g.box_bytes, &P.tmap, 0,
+                                           row0 + static_cast<int32_t>(b) * box_rows, full(s));
+                    continue;
+                }
                 if (P.hints & 1u) {
                     ptx::bulk_g2s_hint(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes,
                                        full(s), l2_policy);
@@ -369,15 +393,72 @@ RingShape auto_ring_shape(OpKind kind, int stages) {
     }
 }
 
+namespace {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+template <class Op>
+void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeom& g, int stages, uint32_t tx_extra,
+                 uint64_t timeout, uint32_t* status, int64_t coef_off, uint32_t hints, const CUtensorMap& tmap) {
+    P.tmap = tmap;
+    P.in = in;
+    P.out = out;
+    P.g = g;
+    P.stages = stages;
+    P.tx_extra = tx_extra;
+    P.timeout_ns = timeout;
+    P.status = status;
+    P.coef_off = static_cast<uint32_t>(coef_off);
+    P.hints = hints;
+}
+
+}  // namespace
+
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
-                      int64_t unit, int stages, const OpArgs& op, cudaStream_t stream) {
+                      int64_t unit, int stages, const OpArgs& op, int64_t tensor_cols, cudaStream_t stream) {
     const RingShape shape = auto_ring_shape(op.kind, stages);
     const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : shape.payload;
     const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : shape.ctas_per_sm;
     const int64_t warps = o.consumer_warps > 0 ? o.consumer_warps : shape.consumer_warps;
-    const int64_t se = stage_elems_for(payload, unit);
+    int64_t se = stage_elems_for(payload, unit);
     StreamGeom g;
-    make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    if (tensor_cols > 0) {
+        // Row shift through 2-D tensor-map boxes of box_rows x cols floats
+        // (box_rows a multiple of 8 so every box is a multiple of 128 bytes).
+        const int64_t cols = tensor_cols;
+        const int64_t rows = n / cols;
+        const int64_t box_rows = std::min<int64_t>(256, (rows + 7) / 8 * 8);
+        const int64_t box_elems = box_rows * cols;
+        se = std::max<int64_t>(box_elems, se / box_elems * box_elems);
+        make_geom_tensor(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se, cols,
+                         box_rows);
+        auto encode = tensor_map_encoder();
+        if (encode == nullptr) return AP_ERR_CUDA;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(4 * cols)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), static_cast<cuuint32_t>(box_rows)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(in), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return AP_ERR_CUDA;
+    } else {
+        make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
+    }
     const int64_t coef_off =
         static_cast<int64_t>(stages) * (g.slot_bytes + static_cast<int64_t>(sizeof(SlotDesc))) + 2 * 8 * stages + 16;
     const int64_t coef_bytes = op.kind == OP_POLY ? (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
@@ -391,33 +472,27 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     int64_t flags = 0;
     if (g.h_in > 0 || g.t_in < n) flags |= 1;
     if (((ia + 4 * static_cast<uint64_t>(off) - oa) & 15) != 0 || off != 0) flags |= 2;
+    if (tensor_cols > 0) flags |= 4;
     record_launch(PATH_RING, grid, se, smem, stages, flags);
 
     const uint64_t timeout = static_cast<uint64_t>(o.timeout_ns);
-    const uint32_t hints = static_cast<uint32_t>(o.cache_hints);
     const uint32_t tx_extra = static_cast<uint32_t>(o.tx_extra);
+    const uint32_t hints = static_cast<uint32_t>(o.cache_hints);
     switch (op.kind) {
         case OP_COPY: {
-            RingParams<OpCopyDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
-                                    static_cast<uint32_t>(coef_off), hints, OpCopyDev{}};
+            RingParams<OpCopyDev> P;
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
             return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
         case OP_SCALE: {
-            RingParams<OpScaleDev> P{in,      out,       g, stages, tx_extra, timeout, di.status,
-                                     static_cast<uint32_t>(coef_off), hints, OpScaleDev{op.alpha}};
+            RingParams<OpScaleDev> P;
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            P.op.alpha = op.alpha;
             return launch_ring_warps(di, warps, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
-            P.in = in;
-            P.out = out;
-            P.g = g;
-            P.stages = stages;
-            P.tx_extra = tx_extra;
-            P.timeout_ns = timeout;
-            P.status = di.status;
-            P.coef_off = static_cast<uint32_t>(coef_off);
-            P.hints = hints;
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, P, grid, smem, stream);

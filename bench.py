@@ -622,6 +622,15 @@ def sweep(which: str, args):
                 yield line("roll 2^26x4 f32", f"ring {name} S={S or 'default'}", 8 * n, ms,
                            flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
+        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)  # the 2-D tensor-map producer (aligned variant)
+        for S in (2, 3, 4):
+            ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
+            A, B = abuf[:n], bbuf[:n]
+            ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
+            yield line("roll 2^26x4 f32", f"ring tensor-map producer S={S}", 8 * n, ms,
+                       flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
+        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 0)
+        ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
         del abuf, bbuf
     if "exchange" in groups:
         n = 1 << 28

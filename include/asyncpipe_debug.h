@@ -21,7 +21,10 @@ extern "C" {
 typedef enum ap_debug_key {
     /* settable */
     AP_DBG_FORCE_PATH = 1,      /* 0 auto; 1 always the ring (also for small row shifts);
-                                   2 small one-CTA row shift when it fits */
+                                   2 small one-CTA row shift when it fits; 3 row shift through the
+                                   ring with a 2-D tensor-map producer (cp.async.bulk.tensor boxes of
+                                   whole rows) where A and B are 16-byte aligned and cols is a
+                                   multiple of 4 no larger than 256, the 1-D producer otherwise */
     AP_DBG_EXPECT_TX_EXTRA = 2, /* bytes added to every stage's expected transaction count:
                                    the barrier then never completes and the consumers' bounded
                                    waits give up (fault injection; 0 = off) */
@@ -44,7 +47,8 @@ typedef enum ap_debug_key {
     AP_DBG_LAST_STAGES = 104,   /* ring depth */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar
-                                   shared-memory path (input/output alignments differ or wrap) */
+                                   shared-memory path (input/output alignments differ or wrap);
+                                   bit 2: the tensor-map producer ran */
 } ap_debug_key;
 
 /* Set a settable key. AP_ERR_ARG for an unknown key or a negative value. */
@@ -80,6 +84,18 @@ ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaS
  */
 ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n, int64_t off,
                                 int in_mis, int out_mis, int64_t stage_elems);
+
+/*
+ * As ap_debug_emulate_ring, for the tensor-map producer of the row shift:
+ * B[i, :] = A[(i + shift) mod rows, :] for a rows x cols matrix at 16-byte
+ * aligned addresses, spans loaded as whole boxes of box_rows x cols floats
+ * (rows past the matrix arrive as zeros, as the copy engine writes them).
+ * Checks every box destination (128-byte aligned, inside the slot) and every
+ * consumer access. cols a multiple of 4 in 4..256, box_rows a multiple of 8
+ * in 8..256, stage_elems a multiple of box_rows * cols.
+ */
+ap_status ap_debug_emulate_ring_tensor(const float* in_host, float* out_host, int64_t rows, int64_t cols,
+                                       int64_t shift, int64_t box_rows, int64_t stage_elems);
 
 #ifdef __cplusplus
 }

@@ -165,3 +165,23 @@ def test_emulator_rejects_bad_arguments(ap):
     assert ap.ap_debug_emulate_ring(x, y, 16, 16, 0, 0, 4) == ap.AP_ERR_SHAPE
     assert ap.ap_debug_emulate_ring(x, y, 16, 0, 2, 0, 4) == ap.AP_ERR_ALIGN
     assert ap.ap_debug_emulate_ring(x, y, 16, 0, 0, 0, 6) == ap.AP_ERR_SHAPE
+
+
+def test_emulated_tensor_ring_matches_oracle(ap, orc):
+    """The tensor-map producer's plan: whole-row boxes (zero rows past the
+    end), 128-byte aligned box destinations, every element moved once."""
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        cols = int(rng.choice([4, 8, 12, 16, 64, 256]))
+        rows = int(rng.integers(1, 3000 // cols + 2))
+        box_rows = int(rng.choice([8, 16, 64, 256]))
+        stage_elems = box_rows * cols * int(rng.integers(1, 4))
+        shift = int(rng.integers(-2 * rows, 2 * rows + 1))
+        A = synth.uniform_pm1_np(rows + cols, rows * cols).reshape(rows, cols)
+        y = np.full(rows * cols, np.nan, dtype=np.float32)
+        st = ap.ap_debug_emulate_ring_tensor(A.ravel(), y, rows, cols, shift, box_rows, stage_elems)
+        assert st == ap.AP_OK, (rows, cols, shift, box_rows, stage_elems)
+        assert np.array_equal(y.reshape(rows, cols).view(np.uint32), orc.row_roll(A, shift).view(np.uint32))
+    x = np.zeros(64, dtype=np.float32)
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 16, 4, 1, 12, 48) == ap.AP_ERR_SHAPE  # box rows not x8
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 16, 6, 1, 8, 48) == ap.AP_ERR_SHAPE  # cols not x4

@@ -114,3 +114,52 @@ def test_roll_full_size(ap, orc, variant):
     assert ap.ap_check() == ap.AP_OK
     want = orc.row_roll(to_np(A).reshape(rows, cols), 1)
     assert_bits(to_np(B), want, f"full-size roll {variant}")
+
+
+@pytest.mark.parametrize("stages", [2, 3, 6])
+@pytest.mark.parametrize("rows,cols", [(1, 4), (7, 4), (64, 4), (1000, 4), (50000, 4), (333, 8), (129, 256), (40, 12)])
+def test_roll_tensor_map_producer(ap, orc, stages, rows, cols):
+    """The 2-D tensor-map producer (boxes of whole rows, zero rows past the end
+    of the matrix) gives the oracle's result bit for bit."""
+    dev = device()
+    n = rows * cols
+    A = synth.uniform_pm1_torch(rows * 7 + cols, n, dev)
+    A_h = to_np(A).reshape(rows, cols)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, stages)
+    for stage_bytes, grid in ((0, 0), (4096, 2), (65536, 3)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        for shift in (1, 0, -1, rows // 2 + 1, 3 * rows - 2):
+            out = Guarded(n, 0, dev)
+            ap.ap_row_roll(A, out.view, rows, cols, shift)
+            assert ap.ap_check() == ap.AP_OK
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4, "tensor-map producer did not run"
+            assert_bits(to_np(out.view), orc.row_roll(A_h, shift), f"tensor roll {rows}x{cols} shift={shift} S={stages}")
+            assert out.intact()
+
+
+def test_roll_tensor_map_falls_back_when_misaligned(ap, orc):
+    dev = device()
+    rows, cols = 1000, 4
+    src = Guarded(rows * cols, 1, dev, fill=synth.uniform_pm1_torch(5, rows * cols, dev))
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    out = Guarded(rows * cols, 0, dev)
+    ap.ap_row_roll(src.view, out.view, rows, cols, 1)
+    assert ap.ap_check() == ap.AP_OK
+    assert not ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4
+    assert_bits(to_np(out.view), orc.row_roll(to_np(src.view).reshape(rows, cols), 1), "fallback")
+
+
+def test_roll_tensor_map_full_size(ap, orc):
+    import torch
+
+    dev = device()
+    rows, cols = 1 << 26, 4
+    A = synth.uniform_pm1_torch(synth.SEED_ROLL, rows * cols, dev)
+    B = torch.empty_like(A)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    ap.ap_row_roll(A, B, rows, cols, 1)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4
+    assert_bits(to_np(B), orc.row_roll(to_np(A).reshape(rows, cols), 1), "full-size tensor roll")
