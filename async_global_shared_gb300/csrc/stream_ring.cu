@@ -437,11 +437,14 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     CUtensorMap tmap;
     std::memset(&tmap, 0, sizeof(tmap));
     if (tensor_cols > 0) {
-        // Row shift through 2-D tensor-map boxes of box_rows x cols floats
-        // (box_rows a multiple of 8 so every box is a multiple of 128 bytes).
+        // Row shift through 2-D tensor-map boxes of box_rows x cols floats:
+        // box_rows a multiple of 8 (every box a multiple of 128 bytes), boxes
+        // of at most 8 KiB (a slot holds two boxes beyond its stage), and no
+        // more rows than the matrix has, rounded up to 8.
         const int64_t cols = tensor_cols;
         const int64_t rows = n / cols;
-        const int64_t box_rows = std::min<int64_t>(256, (rows + 7) / 8 * 8);
+        int64_t box_rows = std::max<int64_t>(8, std::min<int64_t>(256, 8192 / (4 * cols)) / 8 * 8);
+        box_rows = std::min<int64_t>(box_rows, (rows + 7) / 8 * 8);
         const int64_t box_elems = box_rows * cols;
         se = std::max<int64_t>(box_elems, se / box_elems * box_elems);
         make_geom_tensor(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se, cols,

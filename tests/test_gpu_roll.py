@@ -127,7 +127,7 @@ def test_roll_tensor_map_producer(ap, orc, stages, rows, cols):
     A_h = to_np(A).reshape(rows, cols)
     ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, stages)
-    for stage_bytes, grid in ((0, 0), (4096, 2), (65536, 3)):
+    for stage_bytes, grid in ((0, 0), (4096, 2), (16384, 3)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         for shift in (1, 0, -1, rows // 2 + 1, 3 * rows - 2):
