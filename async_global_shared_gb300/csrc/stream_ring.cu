@@ -447,6 +447,14 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
         box_rows = std::min<int64_t>(box_rows, (rows + 7) / 8 * 8);
         const int64_t box_elems = box_rows * cols;
         se = std::max<int64_t>(box_elems, se / box_elems * box_elems);
+        if (o.stage_bytes == 0) {
+            // automatic stages: give up whole boxes until the ring (each slot
+            // two boxes larger than its stage) fits in shared memory
+            auto ring_bytes = [&](int64_t e) {
+                return static_cast<int64_t>(stages) * (4 * e + 8 * box_elems + 256 + 64) + 16 * stages + 16;
+            };
+            while (se > box_elems && ring_bytes(se) > di.smem_optin) se -= box_elems;
+        }
         make_geom_tensor(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se, cols,
                          box_rows);
         auto encode = tensor_map_encoder();
