@@ -51,6 +51,8 @@ class Oracle:
         lib.orc_cluster_exchange_ex.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                                 ctypes.c_int64]
         lib.orc_cluster_exchange_ex.restype = ctypes.c_int
+        lib.orc_masked_copy.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_void_p]
+        lib.orc_masked_copy.restype = ctypes.c_int
         self._lib = lib
 
     def scale(self, x, alpha: float) -> np.ndarray:
@@ -97,6 +99,19 @@ class Oracle:
                                                int(shift))
         if rc != 0:
             raise ValueError("orc_cluster_exchange_ex rejected the sizes")
+        return y
+
+
+    def masked_copy(self, x, out_before, codes) -> np.ndarray:
+        """out = out_before with chunk k replaced per codes[k] (int8, one per 16 bytes)."""
+        x = _f32(x).ravel()
+        y = _f32(out_before).ravel().copy()
+        c = np.ascontiguousarray(codes, dtype=np.int8).ravel()
+        if x.size % 4 or y.size != x.size or c.size != x.size // 4:
+            raise ValueError("masked_copy needs whole 16-byte chunks and one code per chunk")
+        rc = self._lib.orc_masked_copy(_ptr(x), _ptr(y), c.size, c.ctypes.data)
+        if rc != 0:
+            raise ValueError("orc_masked_copy rejected a code")
         return y
 
 

@@ -132,4 +132,29 @@ int orc_cluster_exchange_ex(const float* in, float* out, int64_t n, int cluster_
     return 0;
 }
 
+// Masked / zero-filling chunk copy over 16-byte chunks. For chunk k with
+// code c = codes[k]:
+//   c in 0..16  copy the first c bytes of in chunk k, write zeros to the rest
+//               of out chunk k (c = 16 is a plain copy, c = 0 all zeros);
+//   c == -2     write zeros to the whole out chunk (the source is ignored);
+//   c == -1     leave out chunk k unchanged (the copy is predicated off).
+// "Asynchronous Copies" (TVM TIRx guide), section A Global-to-Shared Copy: a
+// false predicate skips the copy and leaves the destination unchanged, a source
+// size copies a byte prefix and zero-fills the rest, and ignoring the source
+// zero-fills the whole chunk. Returns 0, or -1 for a code outside -2..16.
+int orc_masked_copy(const float* in, float* out, int64_t n_chunks, const signed char* codes) {
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
+    unsigned char* dst = reinterpret_cast<unsigned char*>(out);
+    for (int64_t k = 0; k < n_chunks; ++k) {
+        const int c = codes[k];
+        if (c < -2 || c > 16) return -1;
+        if (c == -1) continue;
+        const int keep = c < 0 ? 0 : c;
+        for (int b = 0; b < 16; ++b) {
+            dst[16 * k + b] = b < keep ? src[16 * k + b] : 0;
+        }
+    }
+    return 0;
+}
+
 }  // extern "C"

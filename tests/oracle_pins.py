@@ -331,6 +331,50 @@ def pin_exchange_ex_invariants(orc):
         raise AssertionError("a partial chunk was accepted")
 
 
+def pin_masked_copy_worked_example(orc):
+    with open(os.path.join(GOLDEN, "masked_copy_small.txt")) as f:
+        lines = [l.strip() for l in f if l.strip() and not l.startswith("#")]
+    codes = [int(t) for t in lines[0].split(":")[1].split()]
+    want = [float(t) for t in lines[1].split(":")[1].split()]
+    x = np.arange(1, 25, dtype=np.float32)
+    got = orc.masked_copy(x, np.full(24, -1.0, dtype=np.float32), codes)
+    assert got.tolist() == want, f"{got.tolist()} != {want}"
+
+
+def pin_masked_copy_bytes(orc):
+    """Against a byte-level numpy restatement: prefix bytes from the input,
+    zeros after, untouched chunks where the predicate is off."""
+    rng = np.random.default_rng(17)
+    for n_chunks in (1, 7, 300):
+        x = synth.uniform_pm1_np(n_chunks, 4 * n_chunks)
+        before = synth.uniform_pm1_np(n_chunks + 1, 4 * n_chunks)
+        codes = rng.integers(-2, 17, n_chunks).astype(np.int8)
+        xb = x.view(np.uint8).reshape(n_chunks, 16)
+        want = before.copy().view(np.uint8).reshape(n_chunks, 16)
+        cols = np.arange(16)[None, :]
+        keep = np.where(codes < 0, 0, codes)[:, None]
+        filled = np.where(cols < keep, xb, 0).astype(np.uint8)
+        on = (codes != -1)[:, None]
+        want = np.where(on, filled, want).astype(np.uint8).reshape(-1).view(np.float32)
+        assert_bits_equal(orc.masked_copy(x, before, codes), want, f"masked copy n={n_chunks}")
+
+
+def pin_masked_copy_special_codes(orc):
+    x = synth.uniform_pm1_np(3, 64)
+    before = synth.uniform_pm1_np(4, 64)
+    assert_bits_equal(orc.masked_copy(x, before, np.full(16, 16, np.int8)), x, "all 16: plain copy")
+    assert_bits_equal(orc.masked_copy(x, before, np.full(16, -1, np.int8)), before, "all -1: unchanged")
+    zeros = np.zeros(64, dtype=np.float32)
+    assert_bits_equal(orc.masked_copy(x, before, np.full(16, 0, np.int8)), zeros, "all 0: zeros")
+    assert_bits_equal(orc.masked_copy(x, before, np.full(16, -2, np.int8)), zeros, "all -2: zeros")
+    try:
+        orc.masked_copy(x, before, np.full(16, 17, np.int8))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("code 17 accepted")
+
+
 ALL_PINS = [
     pin_roll_worked_example,
     pin_roll_brute_force,
@@ -346,6 +390,9 @@ ALL_PINS = [
     pin_exchange_ex_worked_examples,
     pin_exchange_ex_library,
     pin_exchange_ex_invariants,
+    pin_masked_copy_worked_example,
+    pin_masked_copy_bytes,
+    pin_masked_copy_special_codes,
 ]
 
 

@@ -32,6 +32,9 @@ MUTANTS = {
     "exchange_accepts_partial": ("if (n % (E * cs) != 0) return -1;", ""),
     "exchange_ex_last_group_uses_cs": ("const int64_t m = left < cs ? left : cs;", "const int64_t m = cs;"),
     "exchange_ex_shift_sign": ("const int64_t s = ((shift % m) + m) % m;", "const int64_t s = ((-shift % m) + m) % m;"),
+    "masked_skip_writes": ("if (c == -1) continue;", "if (c == -1) { }"),
+    "masked_no_zero_fill": ("dst[16 * k + b] = b < keep ? src[16 * k + b] : 0;", "if (b < keep) dst[16 * k + b] = src[16 * k + b];"),
+    "masked_ignore_copies": ("const int keep = c < 0 ? 0 : c;", "const int keep = c < 0 ? 16 : c;"),
     "exchange_ex_ignores_shift": ("const int64_t src = first + (r + s) % m;", "const int64_t src = first + (r + 1) % m;"),
 }
 
