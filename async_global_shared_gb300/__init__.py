@@ -18,6 +18,7 @@ __all__ = [
     "ap_poly",
     "ap_cluster_exchange",
     "ap_cluster_exchange_ex",
+    "ap_masked_copy",
     "ap_check",
     "ap_status_string",
     "ap_debug_set",

@@ -64,6 +64,7 @@ EXPORTED = (
     "ap_poly",
     "ap_cluster_exchange",
     "ap_cluster_exchange_ex",
+    "ap_masked_copy",
     "ap_check",
     "ap_status_string",
     "ap_debug_set",
@@ -103,6 +104,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_poly.argtypes = [vp, vp, _i64, vp, ctypes.c_int, ctypes.c_int, vp]
     lib.ap_cluster_exchange.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, vp]
     lib.ap_cluster_exchange_ex.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, _i64, vp]
+    lib.ap_masked_copy.argtypes = [vp, vp, _i64, vp, ctypes.c_int, vp]
     lib.ap_check.argtypes = [vp]
     lib.ap_status_string.argtypes = [ctypes.c_int]
     lib.ap_status_string.restype = ctypes.c_char_p
@@ -113,7 +115,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_fma_probe.argtypes = [vp, _i64, _i64, vp]
     lib.ap_debug_emulate_ring_tensor.argtypes = [vp, vp, _i64, _i64, _i64, _i64, _i64]
     for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange",
-                 "ap_cluster_exchange_ex", "ap_check",
+                 "ap_cluster_exchange_ex", "ap_masked_copy", "ap_check",
                  "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_emulate_ring_tensor", "ap_debug_fma_probe"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
@@ -190,6 +192,18 @@ def ap_cluster_exchange(inp, out, n: int, cluster_size: int, chunk_bytes: int, s
 def ap_cluster_exchange_ex(inp, out, n: int, cluster_size: int, chunk_bytes: int, shift: int, stream=None):
     _check(load().ap_cluster_exchange_ex(_addr(inp), _addr(out), n, cluster_size, chunk_bytes, shift,
                                          _stream(stream)), "ap_cluster_exchange_ex")
+
+
+def ap_masked_copy(inp, out, n_chunks: int, codes, stages: int, stream=None):
+    """``codes``: a CUDA int8 tensor (or device address) of n_chunks codes."""
+    if hasattr(codes, "data_ptr"):
+        import torch
+
+        if codes.dtype != torch.int8 or not codes.is_cuda or not codes.is_contiguous():
+            raise TypeError("codes must be a contiguous CUDA int8 tensor")
+        codes = codes.data_ptr()
+    _check(load().ap_masked_copy(_addr(inp), _addr(out), n_chunks, codes, stages, _stream(stream)),
+           "ap_masked_copy")
 
 
 def ap_check(stream=None) -> int:

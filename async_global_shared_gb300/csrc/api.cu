@@ -279,6 +279,20 @@ ap_status ap_cluster_exchange_ex(const float* in, float* out, int64_t n, int clu
     return AP_OK;
 }
 
+ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const int8_t* codes, int stages,
+                         cudaStream_t stream) {
+    if (!valid_stages(stages)) return AP_ERR_STAGES;
+    if (n_chunks < 0 || n_chunks > kMaxElems / 4) return AP_ERR_SHAPE;
+    if (n_chunks == 0) return AP_OK;
+    if (in == nullptr || out == nullptr || codes == nullptr) return AP_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return AP_ERR_ALIGN;
+    if (in != out && overlap(in, 16 * n_chunks, out, 16 * n_chunks)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    return launch_masked_copy(di, in, out, n_chunks, reinterpret_cast<const signed char*>(codes), stages, stream);
+}
+
 ap_status ap_check(cudaStream_t stream) {
     DeviceInfo di;
     const ap_status st = current_device(&di);

@@ -23,6 +23,7 @@ enum WaitSite : uint32_t {
     SITE_EX_RECEIVER_FULL = 6,
     SITE_EX_DRAIN = 7,
     SITE_RING_TENSOR_ALIGN = 8,
+    SITE_MASKED_CODE = 9,
 };
 
 constexpr uint32_t kStatusTimeout = 9;  // AP_ERR_DEVICE_TIMEOUT

@@ -39,7 +39,7 @@ Options options();
 // What a launcher reports about the launch it made (AP_DBG_LAST_*).
 void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem, int64_t stages, int64_t flags);
 
-enum Path : int64_t { PATH_RING = 1, PATH_ROLL_SMALL = 2, PATH_SYNC = 3, PATH_EXCHANGE = 4 };
+enum Path : int64_t { PATH_RING = 1, PATH_ROLL_SMALL = 2, PATH_SYNC = 3, PATH_EXCHANGE = 4, PATH_MASKED = 5 };
 
 // Arguments of the per-element compute of a ring call.
 enum OpKind { OP_COPY, OP_SCALE, OP_POLY };
@@ -73,6 +73,9 @@ ap_status launch_roll_small(const DeviceInfo& di, const float* A, float* B, int6
 
 ap_status launch_scale_sync(const DeviceInfo& di, const float* in, float* out, int64_t n_tiles, int64_t tile,
                             float alpha, cudaStream_t stream);
+
+ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, int64_t n_chunks,
+                             const signed char* codes, int stages, cudaStream_t stream);
 
 ap_status launch_fma_probe(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
 

@@ -1,0 +1,133 @@
+// Masked / zero-filling copy of 16-byte chunks through a per-thread cp.async
+// pipeline: the three forms of "Asynchronous Copies" (TVM TIRx guide),
+// section A Global-to-Shared Copy, chunk by chunk: a false predicate skips
+// the copy and leaves the destination unchanged, a source size copies a byte
+// prefix and zero-fills the rest, and an ignored source zero-fills the whole
+// chunk.
+//
+// Each thread owns U chunks per stage and keeps S stages in flight with
+// commit groups ("Asynchronous Data Movement", section Barriers and
+// pipelines: acquire a stage, commit its copies, wait for the oldest, release
+// it): issue stage t + S - 1, commit, wait until at most S - 1 groups are
+// pending (so stage t has landed), store stage t. A thread reads back only
+// the chunks it copied itself, so no CTA barrier is needed (the page's CTA
+// barrier is for reading a neighbour's row).
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace ap {
+namespace {
+
+constexpr int kMcThreads = 256;
+constexpr int kMcChunks = 4;  // chunks per thread per stage: 16 KiB per CTA stage
+constexpr int kMcStageChunks = kMcThreads * kMcChunks;
+constexpr int kMcMaxStages = 6;
+
+struct McParams {
+    const unsigned char* in;
+    unsigned char* out;
+    const signed char* codes;
+    int64_t n_chunks;
+    uint32_t* status;
+};
+
+// Codes of a stage are kept in shared memory beside its data (each thread
+// reads back only the codes it wrote).
+__device__ __forceinline__ void issue_stage(const McParams& P, uint32_t slot, signed char* code, int64_t base,
+                                            int tid) {
+#pragma unroll
+    for (int u = 0; u < kMcChunks; ++u) {
+        const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
+        int c = -1;
+        if (k < P.n_chunks) c = P.codes[k];
+        code[tid + u * kMcThreads] = static_cast<signed char>(c);
+        const uint32_t dst = slot + 16u * static_cast<uint32_t>(tid + u * kMcThreads);
+        const unsigned char* src = P.in + 16 * k;
+        if (c >= 0 && c <= 16) {
+            ptx::cp_async_cg16(dst, src, static_cast<uint32_t>(c));  // prefix, zero fill
+        } else if (c == -2) {
+            ptx::cp_async_cg16_ignore_src(dst, src, true);  // whole chunk zero
+        }
+        // c == -1 (or past the end): predicated off, nothing copied
+    }
+}
+
+template <int S>
+__global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_constant__ McParams P) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const uint32_t base_addr = ptx::smem_addr(smem);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kMcStageChunks;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kMcStageChunks;
+    signed char* codes = reinterpret_cast<signed char*>(smem + static_cast<size_t>(S) * kMcStageChunks * 16);
+
+    // prologue: stages 0 .. S-2 in flight (empty groups keep the count right)
+#pragma unroll
+    for (int t = 0; t < S - 1; ++t) {
+        issue_stage(P, base_addr + t * kMcStageChunks * 16u, codes + t * kMcStageChunks, first + t * stride, tid);
+        ptx::cp_async_commit();
+    }
+    int64_t base = first;
+    for (int64_t t = 0; base < P.n_chunks; ++t, base += stride) {
+        const int slot = static_cast<int>(t % S);
+        const int next = static_cast<int>((t + S - 1) % S);
+        // acquire + commit the stage S - 1 ahead (its slot was released last iteration)
+        issue_stage(P, base_addr + next * kMcStageChunks * 16u, codes + next * kMcStageChunks, base + (S - 1) * stride,
+                    tid);
+        ptx::cp_async_commit();
+        // wait: at most S - 1 groups pending, so this thread's copies of stage t have landed
+        ptx::cp_async_wait_group<S - 1>();
+        const unsigned char* sl = smem + static_cast<size_t>(slot) * kMcStageChunks * 16;
+#pragma unroll
+        for (int u = 0; u < kMcChunks; ++u) {
+            const int c = codes[slot * kMcStageChunks + tid + u * kMcThreads];
+            const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
+            if (k >= P.n_chunks || c == -1) continue;
+            if (c < -2 || c > 16) {
+                atomicCAS(P.status, 0u, 11u /* AP_ERR_ARG */ | (SITE_MASKED_CODE << 8));
+                continue;
+            }
+            const uint4 v = *reinterpret_cast<const uint4*>(sl + 16 * (tid + u * kMcThreads));
+            *reinterpret_cast<uint4*>(P.out + 16 * k) = v;
+        }
+        // release: the slot is refilled by this same thread next iteration
+    }
+    ptx::cp_async_wait_all();
+}
+
+template <int S>
+ap_status launch_masked_s(const DeviceInfo& di, const McParams& P, cudaStream_t stream) {
+    const int64_t stages_total = (P.n_chunks + kMcStageChunks - 1) / kMcStageChunks;
+    int64_t grid = static_cast<int64_t>(di.sms) * 2;
+    if (grid > stages_total) grid = stages_total;
+    if (grid < 1) grid = 1;
+    const size_t smem = static_cast<size_t>(S) * kMcStageChunks * 17;  // data + one code byte per chunk
+    static int configured[64] = {0};
+    if (di.device < 0 || di.device >= 64) return AP_ERR_CUDA;
+    if (!configured[di.device]) {
+        if (cudaFuncSetAttribute(masked_copy_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kMcMaxStages * kMcStageChunks * 17)) != cudaSuccess)
+            return AP_ERR_CUDA;
+        configured[di.device] = 1;
+    }
+    record_launch(PATH_MASKED, grid, kMcStageChunks * 4, static_cast<int64_t>(smem), S, 0);
+    masked_copy_kernel<S><<<static_cast<unsigned>(grid), kMcThreads, smem, stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
+}
+
+}  // namespace
+
+ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, int64_t n_chunks,
+                             const signed char* codes, int stages, cudaStream_t stream) {
+    McParams P{reinterpret_cast<const unsigned char*>(in), reinterpret_cast<unsigned char*>(out), codes, n_chunks,
+               di.status};
+    switch (stages) {
+        case 2: return launch_masked_s<2>(di, P, stream);
+        case 3: return launch_masked_s<3>(di, P, stream);
+        case 4: return launch_masked_s<4>(di, P, stream);
+        case 5: return launch_masked_s<5>(di, P, stream);
+        default: return launch_masked_s<6>(di, P, stream);
+    }
+}
+
+}  // namespace ap

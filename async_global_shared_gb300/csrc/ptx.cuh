@@ -166,6 +166,23 @@ __device__ __forceinline__ void cp_async_cg16(uint32_t dst, const void* src, uin
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_size) : "memory");
 }
 
+// 16-byte copy whose source is ignored when `ignore` is true: the 16 bytes
+// are written as zeros instead.
+__device__ __forceinline__ void cp_async_cg16_ignore_src(uint32_t dst, const void* src, bool ignore) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %2, 0;\n\t"
+        "cp.async.cg.shared.global [%0], [%1], 16, p;\n\t}" ::"r"(dst),
+        "l"(src), "r"(static_cast<uint32_t>(ignore))
+        : "memory");
+}
+
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }

@@ -494,7 +494,7 @@ def sweep(which: str, args):
     peak, _ = hbm_peak()
     steps, warm = max(5, min(args.steps, 50)), args.warmup
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    groups = ["scale", "poly", "roll", "exchange", "small"] if which == "all" else which.split(",")
+    groups = ["scale", "poly", "roll", "exchange", "masked", "small"] if which == "all" else which.split(",")
 
     window = {}
 
@@ -658,6 +658,22 @@ def sweep(which: str, args):
                        grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+        del x, y
+    if "masked" in groups:
+        n_chunks = 1 << 26
+        x = synth.uniform_pm1_torch(synth.SEED_SCALE, 4 * n_chunks, dev)
+        y = torch.empty_like(x)
+        for name, pattern in (("all 16 (plain copy)", [16]),
+                              ("1/8 off, 1/8 half, 1/8 zeroed, 5/8 copies", [-1, 8, -2, 16, 16, 16, 16, 16])):
+            pat = torch.tensor(pattern, dtype=torch.int8)
+            codes = pat.repeat(n_chunks // len(pattern)).to(dev)
+            rd = sum(max(c, 0) for c in pattern) / len(pattern)
+            wr = sum(16 for c in pattern if c != -1) / len(pattern)
+            nbytes = n_chunks * (rd + wr + 1)
+            for S in (2, 3, 4, 6):
+                ms = run(lambda: ap.ap_masked_copy(x, y, n_chunks, codes, S))
+                yield line("masked copy 2^26 chunks", f"{name} S={S}", nbytes, ms,
+                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
         del x, y
     if "e2e" in groups:
         n_t, t = SCALE_TILES, SCALE_TILE

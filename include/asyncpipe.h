@@ -180,10 +180,32 @@ ap_status ap_cluster_exchange_ex(const float* in, float* out, int64_t n, int clu
                                  int64_t chunk_bytes, int64_t shift, cudaStream_t stream);
 
 /*
+ * ap_masked_copy: predicated / zero-filling copy of 16-byte chunks. For chunk
+ * k (floats 4k .. 4k+3) with code c = codes[k]:
+ *     0..16  the first c bytes of in chunk k are copied, the remaining
+ *            16 - c bytes of out chunk k are set to zero (16: plain copy);
+ *     -2     out chunk k is set to zero, the source is not read;
+ *     -1     out chunk k is left unchanged (the copy is predicated off).
+ * Source: "Asynchronous Copies" (TVM TIRx guide), section A Global-to-Shared
+ * Copy, which names exactly these three forms of the 16-byte copy (a false
+ * predicate, a source size, an ignored source). The chunks stream through a
+ * per-thread cp.async pipeline of `stages` commit groups into shared memory
+ * and out with 16-byte stores.
+ *  in, out     device arrays of 4 * n_chunks floats, 16-byte aligned
+ *              (AP_ERR_ALIGN); in == out is allowed, other overlap is not.
+ *  n_chunks    >= 0.
+ *  codes       DEVICE array of n_chunks int8 codes. A code outside -2..16
+ *              leaves its chunk unchanged and makes ap_check report AP_ERR_ARG.
+ *  stages      commit groups in flight per thread, AP_MIN_STAGES..AP_MAX_STAGES.
+ */
+ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const int8_t* codes, int stages,
+                         cudaStream_t stream);
+
+/*
  * ap_check: waits for `stream`, then returns and clears the device status
  * word of the current device: AP_ERR_DEVICE_TIMEOUT if a kernel's bounded
- * wait gave up since the last check, AP_ERR_CUDA if the stream reported an
- * error, AP_OK otherwise. The status word is shared by all streams of the
+ * wait gave up since the last check, AP_ERR_ARG if ap_masked_copy met a bad
+ * code, AP_ERR_CUDA if the stream reported an error, AP_OK otherwise. The status word is shared by all streams of the
  * device (the first error since the last check wins).
  */
 ap_status ap_check(cudaStream_t stream);

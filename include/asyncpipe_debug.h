@@ -40,7 +40,8 @@ typedef enum ap_debug_key {
     AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: bit 0 bulk loads carry an L2 evict-first policy,
                                    bit 1 consumer stores are streaming (st.global.cs); 0 = none */
     /* read-only: what the last call on this process launched */
-    AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange */
+    AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange,
+                                   5 masked copy */
     AP_DBG_LAST_GRID = 101,     /* CTAs launched */
     AP_DBG_LAST_STAGE_ELEMS = 102, /* elements per ring stage (chunk elements for exchange) */
     AP_DBG_LAST_SMEM = 103,     /* dynamic shared memory per CTA, bytes */

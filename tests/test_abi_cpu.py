@@ -90,6 +90,12 @@ def test_validation_before_cuda(ap):
     assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_OUT, 1000, 4, 32768, None) == ap.AP_ERR_SHAPE
     assert raw(ap, "ap_cluster_exchange", FAKE_IN + 4, FAKE_OUT, 1 << 20, 2, 32768, None) == ap.AP_ERR_ALIGN
     assert raw(ap, "ap_cluster_exchange", FAKE_IN, FAKE_IN, 1 << 20, 2, 32768, None) == ap.AP_ERR_ALIAS
+    mc = "ap_masked_copy"
+    assert raw(ap, mc, FAKE_IN, FAKE_OUT, 100, FAKE_IN, 1, None) == ap.AP_ERR_STAGES
+    assert raw(ap, mc, FAKE_IN, FAKE_OUT, 100, None, 2, None) == ap.AP_ERR_NULL
+    assert raw(ap, mc, FAKE_IN + 4, FAKE_OUT, 100, FAKE_IN, 2, None) == ap.AP_ERR_ALIGN
+    assert raw(ap, mc, FAKE_IN, FAKE_IN + 16, 100, FAKE_IN, 2, None) == ap.AP_ERR_ALIAS
+    assert raw(ap, mc, FAKE_IN, FAKE_OUT, 0, None, 2, None) == ap.AP_OK
     ex = "ap_cluster_exchange_ex"
     assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1 << 20, 0, 32768, 1, None) == ap.AP_ERR_CLUSTER
     assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1 << 20, 17, 32768, 1, None) == ap.AP_ERR_CLUSTER

@@ -36,6 +36,9 @@ def test_c_program_argument_checks(tmp_path):
 
 @pytest.mark.gpu
 def test_c_program_on_gpu(tmp_path):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
     exe = _build(tmp_path)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
