@@ -31,21 +31,30 @@ struct McParams {
     uint32_t* status;
 };
 
-// Codes of a stage are kept in shared memory beside its data (each thread
-// reads back only the codes it wrote).
-__device__ __forceinline__ void issue_stage(const McParams& P, uint32_t slot, signed char* code, int64_t base,
-                                            int tid) {
+// This thread's codes of the stage at `base` (chunk base + tid + u * kMcThreads
+// for u < kMcChunks), -1 past the end; loaded one iteration before they are
+// needed so the load latency hides behind the current stage.
+__device__ __forceinline__ void load_codes(const McParams& P, int64_t base, int tid, int (&c)[kMcChunks]) {
 #pragma unroll
     for (int u = 0; u < kMcChunks; ++u) {
         const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
-        int c = -1;
-        if (k < P.n_chunks) c = P.codes[k];
-        code[tid + u * kMcThreads] = static_cast<signed char>(c);
+        c[u] = k < P.n_chunks ? static_cast<int>(P.codes[k]) : -1;
+    }
+}
+
+// Issue this thread's copies of a stage; its codes are kept in shared memory
+// beside the data (each thread reads back only the codes it wrote).
+__device__ __forceinline__ void issue_stage(const McParams& P, uint32_t slot, signed char* code, int64_t base,
+                                            int tid, const int (&c)[kMcChunks]) {
+#pragma unroll
+    for (int u = 0; u < kMcChunks; ++u) {
+        const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
+        code[tid + u * kMcThreads] = static_cast<signed char>(c[u]);
         const uint32_t dst = slot + 16u * static_cast<uint32_t>(tid + u * kMcThreads);
         const unsigned char* src = P.in + 16 * k;
-        if (c >= 0 && c <= 16) {
-            ptx::cp_async_cg16(dst, src, static_cast<uint32_t>(c));  // prefix, zero fill
-        } else if (c == -2) {
+        if (c[u] >= 0 && c[u] <= 16) {
+            ptx::cp_async_cg16(dst, src, static_cast<uint32_t>(c[u]));  // prefix, zero fill
+        } else if (c[u] == -2) {
             ptx::cp_async_cg16_ignore_src(dst, src, true);  // whole chunk zero
         }
         // c == -1 (or past the end): predicated off, nothing copied
@@ -62,28 +71,32 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
     signed char* codes = reinterpret_cast<signed char*>(smem + static_cast<size_t>(S) * kMcStageChunks * 16);
 
     // prologue: stages 0 .. S-2 in flight (empty groups keep the count right)
+    int c[kMcChunks];
 #pragma unroll
     for (int t = 0; t < S - 1; ++t) {
-        issue_stage(P, base_addr + t * kMcStageChunks * 16u, codes + t * kMcStageChunks, first + t * stride, tid);
+        load_codes(P, first + t * stride, tid, c);
+        issue_stage(P, base_addr + t * kMcStageChunks * 16u, codes + t * kMcStageChunks, first + t * stride, tid, c);
         ptx::cp_async_commit();
     }
+    load_codes(P, first + (S - 1) * stride, tid, c);
     int64_t base = first;
     for (int64_t t = 0; base < P.n_chunks; ++t, base += stride) {
         const int slot = static_cast<int>(t % S);
         const int next = static_cast<int>((t + S - 1) % S);
         // acquire + commit the stage S - 1 ahead (its slot was released last iteration)
         issue_stage(P, base_addr + next * kMcStageChunks * 16u, codes + next * kMcStageChunks, base + (S - 1) * stride,
-                    tid);
+                    tid, c);
         ptx::cp_async_commit();
+        load_codes(P, base + S * stride, tid, c);  // for the next iteration
         // wait: at most S - 1 groups pending, so this thread's copies of stage t have landed
         ptx::cp_async_wait_group<S - 1>();
         const unsigned char* sl = smem + static_cast<size_t>(slot) * kMcStageChunks * 16;
 #pragma unroll
         for (int u = 0; u < kMcChunks; ++u) {
-            const int c = codes[slot * kMcStageChunks + tid + u * kMcThreads];
+            const int code = codes[slot * kMcStageChunks + tid + u * kMcThreads];
             const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
-            if (k >= P.n_chunks || c == -1) continue;
-            if (c < -2 || c > 16) {
+            if (k >= P.n_chunks || code == -1) continue;
+            if (code < -2 || code > 16) {
                 atomicCAS(P.status, 0u, 11u /* AP_ERR_ARG */ | (SITE_MASKED_CODE << 8));
                 continue;
             }
@@ -98,7 +111,7 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
 template <int S>
 ap_status launch_masked_s(const DeviceInfo& di, const McParams& P, cudaStream_t stream) {
     const int64_t stages_total = (P.n_chunks + kMcStageChunks - 1) / kMcStageChunks;
-    int64_t grid = static_cast<int64_t>(di.sms) * 2;
+    int64_t grid = static_cast<int64_t>(di.sms) * (S <= 3 ? 4 : 2);
     if (grid > stages_total) grid = stages_total;
     if (grid < 1) grid = 1;
     const size_t smem = static_cast<size_t>(S) * kMcStageChunks * 17;  // data + one code byte per chunk
