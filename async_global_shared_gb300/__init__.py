@@ -19,6 +19,8 @@ __all__ = [
     "ap_cluster_exchange",
     "ap_cluster_exchange_ex",
     "ap_masked_copy",
+    "ap_autotune",
+    "ap_autotune_reset",
     "ap_check",
     "ap_status_string",
     "ap_debug_set",

@@ -65,6 +65,8 @@ EXPORTED = (
     "ap_cluster_exchange",
     "ap_cluster_exchange_ex",
     "ap_masked_copy",
+    "ap_autotune",
+    "ap_autotune_reset",
     "ap_check",
     "ap_status_string",
     "ap_debug_set",
@@ -73,6 +75,16 @@ EXPORTED = (
     "ap_debug_emulate_ring_tensor",
     "ap_debug_fma_probe",
 )
+
+
+AP_TUNE_SCALE = 1
+AP_TUNE_ROW_ROLL = 2
+AP_TUNE_POLY = 3
+
+
+class RingShape(ctypes.Structure):
+    _fields_ = [("stage_bytes", ctypes.c_int64), ("ctas_per_sm", ctypes.c_int), ("consumer_warps", ctypes.c_int),
+                ("gbs", ctypes.c_double)]
 
 
 class APError(RuntimeError):
@@ -105,6 +117,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_cluster_exchange.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, vp]
     lib.ap_cluster_exchange_ex.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, _i64, vp]
     lib.ap_masked_copy.argtypes = [vp, vp, _i64, vp, ctypes.c_int, vp]
+    lib.ap_autotune.argtypes = [ctypes.c_int, vp, vp, _i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(RingShape), vp]
+    lib.ap_autotune_reset.argtypes = []
     lib.ap_check.argtypes = [vp]
     lib.ap_status_string.argtypes = [ctypes.c_int]
     lib.ap_status_string.restype = ctypes.c_char_p
@@ -115,7 +129,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_fma_probe.argtypes = [vp, _i64, _i64, vp]
     lib.ap_debug_emulate_ring_tensor.argtypes = [vp, vp, _i64, _i64, _i64, _i64, _i64]
     for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange",
-                 "ap_cluster_exchange_ex", "ap_masked_copy", "ap_check",
+                 "ap_cluster_exchange_ex", "ap_masked_copy", "ap_autotune", "ap_autotune_reset", "ap_check",
                  "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_emulate_ring_tensor", "ap_debug_fma_probe"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
@@ -204,6 +218,19 @@ def ap_masked_copy(inp, out, n_chunks: int, codes, stages: int, stream=None):
         codes = codes.data_ptr()
     _check(load().ap_masked_copy(_addr(inp), _addr(out), n_chunks, codes, stages, _stream(stream)),
            "ap_masked_copy")
+
+
+def ap_autotune(op: int, inp, out, n: int, stages: int, degree: int = 0, stream=None) -> dict:
+    """Time the ring's shapes over inp/out, install the fastest; returns it."""
+    shape = RingShape()
+    _check(load().ap_autotune(op, _addr(inp), _addr(out), n, stages, degree, ctypes.byref(shape), _stream(stream)),
+           "ap_autotune")
+    return {"stage_bytes": shape.stage_bytes, "ctas_per_sm": shape.ctas_per_sm,
+            "consumer_warps": shape.consumer_warps, "gbs": shape.gbs}
+
+
+def ap_autotune_reset():
+    _check(load().ap_autotune_reset(), "ap_autotune_reset")
 
 
 def ap_check(stream=None) -> int:

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libasyncpipe.so")
 
-SOURCES = ["api.cu", "stream_ring.cu", "roll_small.cu", "scale_sync.cu", "exchange.cu", "fma_probe.cu", "masked_copy.cu"]
+SOURCES = ["api.cu", "stream_ring.cu", "roll_small.cu", "scale_sync.cu", "exchange.cu", "fma_probe.cu", "masked_copy.cu", "autotune.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -291,6 +292,49 @@ ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const in
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     return launch_masked_copy(di, in, out, n_chunks, reinterpret_cast<const signed char*>(codes), stages, stream);
+}
+
+ap_status ap_autotune(ap_tune_op op, const float* in, float* out, int64_t n, int stages, int degree,
+                      ap_ring_shape* chosen, cudaStream_t stream) {
+    if (op != AP_TUNE_SCALE && op != AP_TUNE_ROW_ROLL && op != AP_TUNE_POLY) return AP_ERR_ARG;
+    if (!valid_stages(stages)) return AP_ERR_STAGES;
+    if (op == AP_TUNE_POLY && (degree < 0 || degree > AP_POLY_MAX_DEGREE)) return AP_ERR_ARG;
+    if (n < (int64_t(1) << 16) || n > kMaxElems || n % 4 != 0) return AP_ERR_SHAPE;
+    if (in == nullptr || out == nullptr || chosen == nullptr) return AP_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return AP_ERR_ALIGN;
+    if (overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    // probe operations: scale by 2 over 256-float tiles; the row shift of an
+    // (n / 4) x 4 matrix by one row; Horner with coefficients 1 / (k + 2)
+    std::vector<float> coeffs(static_cast<size_t>(degree) + 1);
+    for (int k = 0; k <= degree; ++k) coeffs[k] = 1.0f / static_cast<float>(k + 2);
+    OpArgs args{OP_SCALE, 2.0f, 0, nullptr};
+    int64_t off = 0, unit = 256;
+    if (op == AP_TUNE_ROW_ROLL) {
+        args = OpArgs{OP_COPY, 1.0f, 0, nullptr};
+        off = 4;
+        unit = 4;
+    } else if (op == AP_TUNE_POLY) {
+        args = OpArgs{OP_POLY, 0.0f, degree, coeffs.data()};
+        unit = 1;
+    }
+    RingShape best{};
+    double gbs = 0.0;
+    const ap_status r = autotune_ring(di, options(), args.kind, in, out, n, off, unit, stages, args, &best, &gbs, stream);
+    if (r != AP_OK) return r;
+    set_tuned_shape(di.device, args.kind, stages, best);
+    chosen->stage_bytes = best.payload;
+    chosen->ctas_per_sm = static_cast<int>(best.ctas_per_sm);
+    chosen->consumer_warps = static_cast<int>(best.consumer_warps);
+    chosen->gbs = gbs;
+    return AP_OK;
+}
+
+ap_status ap_autotune_reset(void) {
+    clear_tuned_shapes();
+    return AP_OK;
 }
 
 ap_status ap_check(cudaStream_t stream) {

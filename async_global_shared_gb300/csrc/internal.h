@@ -63,6 +63,18 @@ struct RingShape {
 };
 RingShape auto_ring_shape(OpKind kind, int stages);
 
+// Shapes installed by ap_autotune, per device, operation and ring depth;
+// they take the place of auto_ring_shape's defaults.
+bool tuned_shape(int device, OpKind kind, int stages, RingShape* out);
+void set_tuned_shape(int device, OpKind kind, int stages, const RingShape& shape);
+void clear_tuned_shapes();
+
+// Time every fitting (stage size, CTAs per SM, consumer warps) on the given
+// buffers; the fastest goes to *best with its GB/s (8 bytes per element).
+ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, const float* in, float* out,
+                        int64_t n, int64_t off, int64_t unit, int stages, const OpArgs& op, RingShape* best,
+                        double* best_gbs, cudaStream_t stream);
+
 // tensor_cols > 0 selects the tensor-map producer for a rows x cols row shift
 // (in and out 16-byte aligned, cols a multiple of 4 and at most 256).
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,

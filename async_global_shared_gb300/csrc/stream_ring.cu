@@ -428,7 +428,8 @@ void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeo
 
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
                       int64_t unit, int stages, const OpArgs& op, int64_t tensor_cols, cudaStream_t stream) {
-    const RingShape shape = auto_ring_shape(op.kind, stages);
+    RingShape shape;
+    if (tensor_cols > 0 || !tuned_shape(di.device, op.kind, stages, &shape)) shape = auto_ring_shape(op.kind, stages);
     const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : shape.payload;
     const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : shape.ctas_per_sm;
     const int64_t warps = o.consumer_warps > 0 ? o.consumer_warps : shape.consumer_warps;

@@ -659,6 +659,18 @@ def sweep(which: str, args):
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         del x, y
+    if "autotune" in groups:
+        n = 1 << 28
+        x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
+        y = torch.empty_like(x)
+        for name, op, S, deg in (("scale", ap.AP_TUNE_SCALE, 2, 0), ("scale", ap.AP_TUNE_SCALE, 4, 0),
+                                 ("roll", ap.AP_TUNE_ROW_ROLL, 3, 0), ("poly K=32", ap.AP_TUNE_POLY, 3, 32)):
+            t0 = time.perf_counter()
+            shape = ap.ap_autotune(op, x, y, n, S, deg)
+            yield {"workload": "autotune 2^28 f32", "kernel": f"{name} S={S}", "chosen": shape,
+                   "tuning_seconds": round(time.perf_counter() - t0, 2)}
+        ap.ap_autotune_reset()
+        del x, y
     if "masked" in groups:
         n_chunks = 1 << 26
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, 4 * n_chunks, dev)

@@ -202,6 +202,40 @@ ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const in
                          cudaStream_t stream);
 
 /*
+ * ap_autotune: choose the ring's stage size, CTAs per SM and consumer warps by
+ * timing them on this device. Source: "CUDA Async Copy and Pipeline Guide",
+ * FAQ: more stages hide more latency but use more shared memory, and the
+ * sweet spot is found by profiling. For the given ring depth the call runs
+ * the operation over in/out for every stage size from 8 to 96 KiB and every
+ * CTAs-per-SM count (1-4) whose shared memory fits, three timed launches
+ * each (CUDA events on `stream`, median), keeps the fastest and installs it:
+ * later calls of that operation with that depth on this device use it
+ * instead of the built-in defaults (explicit ap_debug_set settings still
+ * win). Blocks until the timing is done.
+ *  op      AP_TUNE_SCALE (ap_scale, alpha 2, 256-float tiles), AP_TUNE_ROW_ROLL
+ *          (ap_row_roll of an (n / 4) x 4 matrix by one row), AP_TUNE_POLY
+ *          (ap_poly of the given degree; the choice is kept for every degree).
+ *  in, out device buffers of n floats, 16-byte aligned, not overlapping. out
+ *          is overwritten; in is only read.
+ *  n       elements, a multiple of 4, at least 65536 (larger than the L2,
+ *          256 MiB or more, gives the choice that holds for streaming work).
+ *  chosen  receives the chosen shape and its rate (8 bytes per element / time).
+ * ap_autotune_reset forgets every installed choice.
+ */
+typedef enum ap_tune_op { AP_TUNE_SCALE = 1, AP_TUNE_ROW_ROLL = 2, AP_TUNE_POLY = 3 } ap_tune_op;
+
+typedef struct ap_ring_shape {
+    int64_t stage_bytes; /* payload of one ring stage */
+    int ctas_per_sm;     /* resident CTAs per SM the grid is sized for */
+    int consumer_warps;  /* consumer warps per CTA */
+    double gbs;          /* measured rate of the chosen shape, GB/s */
+} ap_ring_shape;
+
+ap_status ap_autotune(ap_tune_op op, const float* in, float* out, int64_t n, int stages, int degree,
+                      ap_ring_shape* chosen, cudaStream_t stream);
+ap_status ap_autotune_reset(void);
+
+/*
  * ap_check: waits for `stream`, then returns and clears the device status
  * word of the current device: AP_ERR_DEVICE_TIMEOUT if a kernel's bounded
  * wait gave up since the last check, AP_ERR_ARG if ap_masked_copy met a bad

@@ -96,6 +96,18 @@ def test_validation_before_cuda(ap):
     assert raw(ap, mc, FAKE_IN + 4, FAKE_OUT, 100, FAKE_IN, 2, None) == ap.AP_ERR_ALIGN
     assert raw(ap, mc, FAKE_IN, FAKE_IN + 16, 100, FAKE_IN, 2, None) == ap.AP_ERR_ALIAS
     assert raw(ap, mc, FAKE_IN, FAKE_OUT, 0, None, 2, None) == ap.AP_OK
+    import ctypes
+
+    shape = ap._lib.RingShape()
+    at = "ap_autotune"
+    big = 1 << 20
+    assert raw(ap, at, 9, FAKE_IN, FAKE_OUT, big, 2, 0, ctypes.byref(shape), None) == ap.AP_ERR_ARG
+    assert raw(ap, at, ap.AP_TUNE_SCALE, FAKE_IN, FAKE_OUT, big, 7, 0, ctypes.byref(shape), None) == ap.AP_ERR_STAGES
+    assert raw(ap, at, ap.AP_TUNE_SCALE, FAKE_IN, FAKE_OUT, 1000, 2, 0, ctypes.byref(shape), None) == ap.AP_ERR_SHAPE
+    assert raw(ap, at, ap.AP_TUNE_POLY, FAKE_IN, FAKE_OUT, big, 2, 2000, ctypes.byref(shape), None) == ap.AP_ERR_ARG
+    assert raw(ap, at, ap.AP_TUNE_SCALE, FAKE_IN, FAKE_OUT, big, 2, 0, None, None) == ap.AP_ERR_NULL
+    assert raw(ap, at, ap.AP_TUNE_SCALE, FAKE_IN, FAKE_IN + 64, big, 2, 0, ctypes.byref(shape), None) == ap.AP_ERR_ALIAS
+    assert raw(ap, "ap_autotune_reset") == ap.AP_OK
     ex = "ap_cluster_exchange_ex"
     assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1 << 20, 0, 32768, 1, None) == ap.AP_ERR_CLUSTER
     assert raw(ap, ex, FAKE_IN, FAKE_OUT, 1 << 20, 17, 32768, 1, None) == ap.AP_ERR_CLUSTER
