@@ -83,6 +83,7 @@ struct OpPolyDev {
 #pragma unroll
             for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], ck);
         }
+#pragma unroll 2
         for (; k >= 3; k -= 4) {  // steps k, k-1, k-2, k-3 from one aligned 16-byte word
             const float4 q = *reinterpret_cast<const float4*>(cs + k - 3);
 #pragma unroll

@@ -648,6 +648,16 @@ def sweep(which: str, args):
                            slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+        for cps in (3, 4):
+            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+            for piece_kib in (4, 8):
+                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
+                ms = run(lambda: ap.ap_cluster_exchange_ex(x, y, n, 16, 32768, 1))
+                yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster_ex cs=16 ctas/SM={cps} piece={piece_kib}KiB",
+                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
+                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         for cs, shift in ((3, 1), (6, 2), (16, 1), (16, 5)):
             ms = run(lambda: ap.ap_cluster_exchange_ex(x, y, n, cs, 32768, shift))
             yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster_ex cs={cs} shift={shift}", 8 * n, ms,
