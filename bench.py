@@ -784,7 +784,8 @@ def sweep(which: str, args):
 
 # ----------------------------------------------------------------------------- profiling cases
 
-PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "exchange4")
+PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
+                 "masked")
 
 
 def profile_case(name: str, args):
@@ -799,6 +800,7 @@ def profile_case(name: str, args):
     n = 1 << 26  # 256 MiB in + 256 MiB out
     x = synth.uniform_pm1_torch(synth.SEED_SCALE, n + 4, dev)
     y = torch.empty_like(x)
+    codes = torch.tensor([-1, 8, -2, 16, 16, 16, 16, 16], dtype=torch.int8).repeat(n // 32).to(dev)
     calls = {
         "scale": lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, 2),
         "sync": lambda: ap.ap_scale_sync(x[:n], y[:n], n // 256, 256, 2.0),
@@ -807,7 +809,12 @@ def profile_case(name: str, args):
         "roll": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "roll_mis": lambda: ap.ap_row_roll(x[1:n + 1], y[:n], n // 4, 4, 1),
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
+        "exchange16": lambda: ap.ap_cluster_exchange_ex(x[:n], y[:n], n, 16, 32768, 1),
+        "roll_tensor": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
+        "masked": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
     }
+    if name == "roll_tensor":
+        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     fn = calls[name]
     for _ in range(args.warmup + args.steps):
         fn()
