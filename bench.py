@@ -602,7 +602,7 @@ def sweep(which: str, args):
         probe = torch.empty(sms * 1024, dtype=torch.float32, device=dev)
         iters = 1 << 16
         ms = run(lambda: ap.ap_debug_fma_probe(probe, probe.numel(), iters))
-        tfma = sms * 1024 * 16 * iters / (ms * 1e-3) / 1e12
+        tfma = sms * 1024 * 32 * iters / (ms * 1e-3) / 1e12
         d = line("fp32 fma probe (registers only)", "fma_probe_kernel", 0, ms, fp32_tflops=round(2 * tfma, 2))
         d.pop("GB/s")
         d.pop("frac_of_measured_hbm")

@@ -60,7 +60,7 @@ int64_t ap_debug_get(int key);
 
 /*
  * FP32 FMA throughput probe: each thread of a grid sized to the device runs
- * 16 independent fmaf chains of `iters` steps on registers only and writes
+ * 32 independent fmaf chains of `iters` steps on registers only and writes
  * one float (the chains' sum) to out[thread]; the number of threads launched
  * is min(out_elems, SMs * 1024) rounded down to whole CTAs of 512. Timing a
  * call gives the achievable fma rate that bounds ap_poly at high degree.
