@@ -377,7 +377,7 @@ ap_status ap_debug_set(int key, int64_t value) {
             g_roll_stages = value;
             return AP_OK;
         case AP_DBG_CONSUMER_WARPS:
-            if (value != 0 && value != 8 && value != 16) return AP_ERR_ARG;
+            if (value != 0 && value != 8 && value != 15 && value != 16) return AP_ERR_ARG;
             g_consumer_warps = value;
             return AP_OK;
         case AP_DBG_EXCHANGE_STORE:

@@ -41,7 +41,8 @@ namespace {
 // the polynomial's coefficients) before the ring starts; apply() transforms
 // N values held in registers.
 // kGroups: 16-byte groups a consumer thread keeps in flight per iteration
-// (4 groups = 16 values; for the polynomial, 16 independent Horner chains).
+// (4 groups = 16 values; the polynomial wants 8, i.e. 32 independent Horner
+// chains, where registers allow).
 struct OpCopyDev {
     static constexpr int kGroups = 4;
     __device__ __forceinline__ void stage(float*, int, int) const {}
@@ -65,7 +66,7 @@ struct OpScaleDev {
 // read from shared memory four at a time (one 16-byte broadcast load per four
 // fma steps per chain), highest power first.
 struct OpPolyDev {
-    static constexpr int kGroups = 4;
+    static constexpr int kGroups = 8;
     int degree;
     float c[AP_POLY_MAX_DEGREE + 1];
     __device__ __forceinline__ void stage(float* cs, int tid, int nthreads) const {
@@ -160,7 +161,11 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         const float4* src = reinterpret_cast<const float4*>(slot + o0);
         float4* dst = reinterpret_cast<float4*>(out + d.e_al);
         int64_t q = ct;
-        vec_groups<Op::kGroups, kConsumers>(P, src, dst, q, ngroups, cs);
+        // 17 warps (16 consumers + producer) leave at most 96 registers a
+        // thread, too few for 32 chains: 16 chains there.
+        constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
+        vec_groups<kG, kConsumers>(P, src, dst, q, ngroups, cs);
+        if (kG > 4) vec_groups<4, kConsumers>(P, src, dst, q, ngroups, cs);
         vec_groups<1, kConsumers>(P, src, dst, q, ngroups, cs);
     } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
@@ -352,6 +357,7 @@ template <class Op>
 ap_status launch_ring_warps(const DeviceInfo& di, int64_t warps, const RingParams<Op>& P, int64_t grid, int64_t smem,
                             cudaStream_t stream) {
     if (warps == 16) return launch_ring_op<Op, 16>(di, P, grid, smem, stream);
+    if (warps == 15) return launch_ring_op<Op, 15>(di, P, grid, smem, stream);
     return launch_ring_op<Op, 8>(di, P, grid, smem, stream);
 }
 

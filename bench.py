@@ -574,9 +574,9 @@ def sweep(which: str, args):
         if "polywarps" in groups:
             for K in (8, 32, 128):
                 c = synth.coeffs_np(K).tolist()
-                for warps in (8, 16):
+                for warps in (15, 16):
                     ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
-                    for S, kib in ((2, 64), (3, 64), (4, 48), (4, 32), (6, 32), (2, 96), (3, 48)):
+                    for S, kib in ((2, 96), (3, 64), (4, 48), (6, 32)):
                         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
                         ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
                         tflops = 2.0 * K * n / (ms * 1e-3) / 1e12

@@ -26,7 +26,7 @@ def test_poly_small(ap, orc, degree, stages):
     x = synth.uniform_pm1_torch(n + degree, n, dev)
     c = synth.coeffs_np(degree)
     want = orc.poly(to_np(x), c)
-    for stage_bytes, grid, warps in ((256, 2, 8), (0, 0, 0), (1024, 3, 16), (0, 0, 16)):
+    for stage_bytes, grid, warps in ((256, 2, 8), (0, 0, 0), (1024, 3, 16), (0, 0, 16), (2048, 2, 15), (0, 0, 15)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
