@@ -49,12 +49,14 @@ AP_DBG_ROLL_STAGES = 7
 AP_DBG_CONSUMER_WARPS = 8
 AP_DBG_EXCHANGE_STORE = 9
 AP_DBG_CACHE_HINTS = 10
+AP_DBG_DEVICE_CHECKS = 11
 AP_DBG_LAST_PATH = 100
 AP_DBG_LAST_GRID = 101
 AP_DBG_LAST_STAGE_ELEMS = 102
 AP_DBG_LAST_SMEM = 103
 AP_DBG_LAST_STAGES = 104
 AP_DBG_LAST_FLAGS = 105
+AP_DBG_LAST_SITE = 106
 
 # Every symbol the headers under include/ declare.
 EXPORTED = (

@@ -31,9 +31,10 @@ std::atomic<int64_t> g_roll_stages{0};
 std::atomic<int64_t> g_consumer_warps{0};
 std::atomic<int64_t> g_ex_tma_store{0};
 std::atomic<int64_t> g_cache_hints{0};
+std::atomic<int64_t> g_device_checks{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
-    g_last_flags{0};
+    g_last_flags{0}, g_last_site{0};
 
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;  // 2 s
 
@@ -117,6 +118,7 @@ Options options() {
     o.consumer_warps = g_consumer_warps.load();
     o.ex_tma_store = g_ex_tma_store.load();
     o.cache_hints = g_cache_hints.load();
+    o.device_checks = g_device_checks.load();
     return o;
 }
 
@@ -347,6 +349,7 @@ ap_status ap_check(cudaStream_t stream) {
         return AP_ERR_CUDA;
     if (cudaMemsetAsync(di.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return AP_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return AP_ERR_CUDA;
+    g_last_site = static_cast<int64_t>((word >> 8) & 0xff);
     if (word == 0) return AP_OK;
     return static_cast<ap_status>(word & 0xff);
 }
@@ -388,6 +391,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 3) return AP_ERR_ARG;
             g_cache_hints = value;
             return AP_OK;
+        case AP_DBG_DEVICE_CHECKS:
+            if (value > 1) return AP_ERR_ARG;
+            g_device_checks = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -405,12 +412,14 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_CONSUMER_WARPS: return o.consumer_warps;
         case AP_DBG_EXCHANGE_STORE: return o.ex_tma_store;
         case AP_DBG_CACHE_HINTS: return o.cache_hints;
+        case AP_DBG_DEVICE_CHECKS: return o.device_checks;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();
         case AP_DBG_LAST_SMEM: return g_last_smem.load();
         case AP_DBG_LAST_STAGES: return g_last_stages.load();
         case AP_DBG_LAST_FLAGS: return g_last_flags.load();
+        case AP_DBG_LAST_SITE: return g_last_site.load();
         default: return -1;
     }
 }

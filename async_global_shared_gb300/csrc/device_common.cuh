@@ -24,10 +24,13 @@ enum WaitSite : uint32_t {
     SITE_EX_DRAIN = 7,
     SITE_RING_TENSOR_ALIGN = 8,
     SITE_MASKED_CODE = 9,
+    SITE_CHECK_PRODUCER = 10,
+    SITE_CHECK_CONSUMER = 11,
 };
 
 constexpr uint32_t kStatusTimeout = 9;  // AP_ERR_DEVICE_TIMEOUT
 constexpr uint32_t kStatusAlign = 3;    // AP_ERR_ALIGN
+constexpr uint32_t kStatusShape = 2;    // AP_ERR_SHAPE
 
 __device__ __forceinline__ void raise_timeout(uint32_t* status, uint32_t site, volatile int* abort_flag) {
     atomicCAS(status, 0u, kStatusTimeout | (site << 8));

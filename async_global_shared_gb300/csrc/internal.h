@@ -32,6 +32,7 @@ struct Options {
     int64_t consumer_warps;
     int64_t ex_tma_store;
     int64_t cache_hints;
+    int64_t device_checks;
 };
 
 Options options();

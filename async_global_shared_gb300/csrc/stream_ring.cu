@@ -151,6 +151,61 @@ __device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4
     }
 }
 
+// ---------------------------------------------------------------- checked build
+// With kChecks the kernel verifies, for every stage, that each copy it is about
+// to issue and each shared/global range its consumers will touch lies inside
+// the caller's buffers and the stage slot; a violation is recorded in the
+// status word (AP_ERR_SHAPE and the site), the CTA aborts, and nothing is
+// accessed. Used by the tests as a stand-in for a memory checker.
+
+__device__ __forceinline__ void check_fail(uint32_t* status, uint32_t site, volatile int* abort_flag) {
+    atomicCAS(status, 0u, kStatusShape | (site << 8));
+    *abort_flag = 1;
+}
+
+// The copies the producer issues for one stage.
+__device__ __forceinline__ bool producer_plan_ok(const StreamGeom& g, const StagePlan& sp) {
+    const uint64_t lo = g.in_addr, hi = g.in_addr + 4 * static_cast<uint64_t>(g.n);
+    for (int k = 0; k < sp.nspans; ++k) {
+        const Span& sn = sp.span[k];
+        if (sn.x0 < 0 || sn.x1 > g.n || sn.x0 >= sn.x1) return false;
+        if (g.box_bytes != 0) {
+            if (sn.bulk_dst % 128 || sn.bulk_dst + static_cast<uint64_t>(sn.bulk_bytes) > g.slot_bytes) return false;
+            if (sn.x0 % g.cols) return false;
+            continue;
+        }
+        if (sn.bulk_bytes) {
+            if (sn.bulk_src % 16 || sn.bulk_dst % 16 || sn.bulk_bytes % 16) return false;
+            if (sn.bulk_src < lo || sn.bulk_src + sn.bulk_bytes > hi) return false;
+            if (sn.bulk_dst + static_cast<uint64_t>(sn.bulk_bytes) > g.slot_bytes) return false;
+        }
+        if (sn.head_end > sn.x0 && sn.region + sn.lead + 4 * static_cast<uint64_t>(sn.head_end - sn.x0) > g.slot_bytes)
+            return false;
+        if (sn.tail_begin < sn.x1 && (sn.tail_dst % 16 || sn.tail_dst + 16ull > g.slot_bytes)) return false;
+    }
+    return true;
+}
+
+// The shared-memory and output ranges the consumers touch for one stage.
+__device__ __forceinline__ bool consumer_desc_ok(const StreamGeom& g, const SlotDesc& d, uint64_t out_addr) {
+    if (d.lo < 0 || d.lo > d.e_al || d.e_al > d.e_end || d.e_end > d.hi || d.hi > g.n) return false;
+    if ((d.e_end - d.e_al) % 4 || d.e_al - d.lo > 3 || d.hi - d.e_end > 3) return false;
+    if (d.e_end > d.e_al && (out_addr + 4 * static_cast<uint64_t>(d.e_al)) % 16) return false;
+    const uint64_t ngroups = static_cast<uint64_t>(d.e_end - d.e_al) / 4;
+    const uint64_t o0 = d.off0 + 4 * static_cast<uint64_t>(d.e_al - d.lo);
+    if (d.mode == MODE_VEC) {
+        if (o0 % 16 || o0 + 16 * ngroups > g.slot_bytes) return false;
+    } else if (d.mode == MODE_SHIFTED) {
+        if (o0 % 4 == 0 && o0 % 16 == 0) return false;
+        if ((o0 & ~15ull) + 16 * ngroups + 16 > g.slot_bytes) return false;
+    }
+    const uint64_t L = static_cast<uint64_t>(d.hi - d.lo);
+    const uint64_t l1 = d.len1 < static_cast<int64_t>(L) ? static_cast<uint64_t>(d.len1) : L;
+    if (d.off0 + 4 * l1 > g.slot_bytes) return false;
+    if (L > l1 && d.off1 + 4 * (L - l1) > g.slot_bytes) return false;
+    return true;
+}
+
 template <int kConsumers, class Op>
 __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const SlotDesc& d, const unsigned char* slot,
                                               const float* cs, int ct) {
@@ -209,7 +264,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
 }
 
 // kConsumerWarps consumer warps plus one producer warp per CTA.
-template <class Op, int kConsumerWarps>
+template <class Op, int kConsumerWarps, bool kChecks>
 __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(const __grid_constant__ RingParams<Op> P) {
     constexpr int kConsumers = 32 * kConsumerWarps;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -264,6 +319,10 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             }
             StagePlan sp;
             plan_stage(P.g, j, &sp);
+            if (kChecks && !producer_plan_ok(P.g, sp)) {
+                check_fail(P.status, SITE_CHECK_PRODUCER, abort_flag);
+                break;
+            }
             make_slot_desc(sp, &descs[s]);  // published to the consumers by the arrive below
             const uint32_t slot = smem_base + static_cast<uint32_t>(s) * slot_bytes;
             bool edges = false;
@@ -330,20 +389,24 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
         if (w != WAIT_OK) break;
         __syncwarp();  // orders lane 0's observation of the phase before the other lanes' reads
         const SlotDesc d = descs[s];
+        if (kChecks && !consumer_desc_ok(P.g, d, reinterpret_cast<uint64_t>(P.out))) {
+            if (lane == 0) check_fail(P.status, SITE_CHECK_CONSUMER, abort_flag);
+            break;
+        }
         consume_stage<kConsumers>(P, d, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty(s));
     }
 }
 
-template <class Op, int kConsumerWarps>
+template <class Op, int kConsumerWarps, bool kChecks>
 ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t grid, int64_t smem,
                          cudaStream_t stream) {
     // Raise the kernel's dynamic shared-memory limit once per device.
     static int64_t configured[64] = {0};
     const int d = di.device;
     if (d < 0 || d >= 64) return AP_ERR_CUDA;
-    auto kernel = ring_kernel<Op, kConsumerWarps>;
+    auto kernel = ring_kernel<Op, kConsumerWarps, kChecks>;
     if (configured[d] < smem) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
             return AP_ERR_CUDA;
@@ -353,12 +416,19 @@ ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t 
     return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
 }
 
+template <class Op, bool kChecks>
+ap_status launch_ring_checks(const DeviceInfo& di, int64_t warps, const RingParams<Op>& P, int64_t grid, int64_t smem,
+                             cudaStream_t stream) {
+    if (warps == 16) return launch_ring_op<Op, 16, kChecks>(di, P, grid, smem, stream);
+    if (warps == 15) return launch_ring_op<Op, 15, kChecks>(di, P, grid, smem, stream);
+    return launch_ring_op<Op, 8, kChecks>(di, P, grid, smem, stream);
+}
+
 template <class Op>
-ap_status launch_ring_warps(const DeviceInfo& di, int64_t warps, const RingParams<Op>& P, int64_t grid, int64_t smem,
-                            cudaStream_t stream) {
-    if (warps == 16) return launch_ring_op<Op, 16>(di, P, grid, smem, stream);
-    if (warps == 15) return launch_ring_op<Op, 15>(di, P, grid, smem, stream);
-    return launch_ring_op<Op, 8>(di, P, grid, smem, stream);
+ap_status launch_ring_warps(const DeviceInfo& di, int64_t warps, bool checks, const RingParams<Op>& P, int64_t grid,
+                            int64_t smem, cudaStream_t stream) {
+    if (checks) return launch_ring_checks<Op, true>(di, warps, P, grid, smem, stream);
+    return launch_ring_checks<Op, false>(di, warps, P, grid, smem, stream);
 }
 
 }  // namespace
@@ -501,20 +571,20 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
         case OP_COPY: {
             RingParams<OpCopyDev> P;
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
-            return launch_ring_warps(di, warps, P, grid, smem, stream);
+            return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_SCALE: {
             RingParams<OpScaleDev> P;
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
             P.op.alpha = op.alpha;
-            return launch_ring_warps(di, warps, P, grid, smem, stream);
+            return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
-            return launch_ring_warps(di, warps, P, grid, smem, stream);
+            return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
     }
     return AP_ERR_ARG;

@@ -39,6 +39,10 @@ typedef enum ap_debug_key {
                                    piece to a shared->global bulk copy, 2 eight warps of 16-byte stores */
     AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: bit 0 bulk loads carry an L2 evict-first policy,
                                    bit 1 consumer stores are streaming (st.global.cs); 0 = none */
+    AP_DBG_DEVICE_CHECKS = 11,  /* 1: ring kernels verify, before every stage, that each copy and each
+                                   shared/global range they touch lies inside the caller's buffers and
+                                   the stage slot; a violation makes ap_check report AP_ERR_SHAPE (site
+                                   in AP_DBG_LAST_SITE) and nothing out of range is accessed */
     /* read-only: what the last call on this process launched */
     AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange,
                                    5 masked copy */
@@ -46,6 +50,7 @@ typedef enum ap_debug_key {
     AP_DBG_LAST_STAGE_ELEMS = 102, /* elements per ring stage (chunk elements for exchange) */
     AP_DBG_LAST_SMEM = 103,     /* dynamic shared memory per CTA, bytes */
     AP_DBG_LAST_STAGES = 104,   /* ring depth */
+    AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar
                                    shared-memory path (input/output alignments differ or wrap);

@@ -40,6 +40,7 @@ def reset_debug(ap):
         ap.AP_DBG_CONSUMER_WARPS,
         ap.AP_DBG_EXCHANGE_STORE,
         ap.AP_DBG_CACHE_HINTS,
+        ap.AP_DBG_DEVICE_CHECKS,
     ):
         ap.ap_debug_set(key, 0)
 
