@@ -28,6 +28,7 @@
 // (the data reached the receiver) and that the receiver's recv[s] is free,
 // so the loader may refill send[s] and the pusher may overwrite recv[s].
 #include <algorithm>
+#include <atomic>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -268,9 +269,9 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     const int64_t smem = 2 * S * piece + 3 * 8 * S + 16;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
 
-    static bool configured[64] = {false};
+    static std::atomic<bool> configured[64];  // attributes set on this device (setting twice is harmless)
     if (di.device < 0 || di.device >= 64) return AP_ERR_CUDA;
-    if (!configured[di.device]) {
+    if (!configured[di.device].load()) {
         if (cudaFuncSetAttribute(exchange_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(exchange_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)

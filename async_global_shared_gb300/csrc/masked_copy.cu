@@ -12,6 +12,8 @@
 // pending (so stage t has landed), store stage t. A thread reads back only
 // the chunks it copied itself, so no CTA barrier is needed (the page's CTA
 // barrier is for reading a neighbour's row).
+#include <atomic>
+
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -115,9 +117,9 @@ ap_status launch_masked_s(const DeviceInfo& di, const McParams& P, cudaStream_t 
     if (grid > stages_total) grid = stages_total;
     if (grid < 1) grid = 1;
     const size_t smem = static_cast<size_t>(S) * kMcStageChunks * 17;  // data + one code byte per chunk
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];  // attribute set on this device (setting twice is harmless)
     if (di.device < 0 || di.device >= 64) return AP_ERR_CUDA;
-    if (!configured[di.device]) {
+    if (!configured[di.device].load()) {
         if (cudaFuncSetAttribute(masked_copy_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kMcMaxStages * kMcStageChunks * 17)) != cudaSuccess)
             return AP_ERR_CUDA;

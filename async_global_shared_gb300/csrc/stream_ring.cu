@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "device_common.cuh"
@@ -403,11 +404,11 @@ template <class Op, int kConsumerWarps, bool kChecks>
 ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t grid, int64_t smem,
                          cudaStream_t stream) {
     // Raise the kernel's dynamic shared-memory limit once per device.
-    static int64_t configured[64] = {0};
+    static std::atomic<int64_t> configured[64];  // limit already set on this device (setting twice is harmless)
     const int d = di.device;
     if (d < 0 || d >= 64) return AP_ERR_CUDA;
     auto kernel = ring_kernel<Op, kConsumerWarps, kChecks>;
-    if (configured[d] < smem) {
+    if (configured[d].load() < smem) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
             return AP_ERR_CUDA;
         configured[d] = di.smem_optin;

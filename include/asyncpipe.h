@@ -239,7 +239,9 @@ ap_status ap_autotune_reset(void);
  * ap_check: waits for `stream`, then returns and clears the device status
  * word of the current device: AP_ERR_DEVICE_TIMEOUT if a kernel's bounded
  * wait gave up since the last check, AP_ERR_ARG if ap_masked_copy met a bad
- * code, AP_ERR_CUDA if the stream reported an error, AP_OK otherwise. The status word is shared by all streams of the
+ * code, AP_ERR_SHAPE if the device-checked ring (asyncpipe_debug.h) found an
+ * access out of range, AP_ERR_CUDA if the stream reported an error, AP_OK
+ * otherwise. The status word is shared by all streams of the
  * device (the first error since the last check wins).
  */
 ap_status ap_check(cudaStream_t stream);
