@@ -32,6 +32,7 @@ std::atomic<int64_t> g_consumer_warps{0};
 std::atomic<int64_t> g_ex_tma_store{0};
 std::atomic<int64_t> g_cache_hints{0};
 std::atomic<int64_t> g_device_checks{0};
+std::atomic<int64_t> g_schedule{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0}, g_last_site{0};
@@ -119,6 +120,7 @@ Options options() {
     o.ex_tma_store = g_ex_tma_store.load();
     o.cache_hints = g_cache_hints.load();
     o.device_checks = g_device_checks.load();
+    o.schedule = g_schedule.load();
     return o;
 }
 
@@ -395,6 +397,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 1) return AP_ERR_ARG;
             g_device_checks = value;
             return AP_OK;
+        case AP_DBG_SCHEDULE:
+            if (value > 1) return AP_ERR_ARG;
+            g_schedule = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -413,6 +419,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_EXCHANGE_STORE: return o.ex_tma_store;
         case AP_DBG_CACHE_HINTS: return o.cache_hints;
         case AP_DBG_DEVICE_CHECKS: return o.device_checks;
+        case AP_DBG_SCHEDULE: return o.schedule;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

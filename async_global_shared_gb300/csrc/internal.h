@@ -33,6 +33,7 @@ struct Options {
     int64_t ex_tma_store;
     int64_t cache_hints;
     int64_t device_checks;
+    int64_t schedule;
 };
 
 Options options();

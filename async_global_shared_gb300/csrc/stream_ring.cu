@@ -114,6 +114,7 @@ struct RingParams {
     uint32_t* status;
     uint32_t coef_off;  // byte offset of the op's staged data in dynamic shared memory
     uint32_t hints;     // bit 0: loads marked L2 evict-first; bit 1: streaming (.cs) stores
+    uint32_t schedule;  // 0: CTA b takes stages b, b + grid, ...; 1: a contiguous run of stages
     Op op;
 };
 
@@ -293,6 +294,18 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
 
     const int64_t T = P.g.n_stages;
     const int64_t G = gridDim.x;
+    // This CTA's stages: j0, j0 + step, ... (count of them).
+    int64_t j0, step, count;
+    if (P.schedule == 0) {
+        j0 = blockIdx.x;
+        step = G;
+        count = j0 < T ? (T - j0 + G - 1) / G : 0;
+    } else {
+        const int64_t per = (T + G - 1) / G;
+        j0 = static_cast<int64_t>(blockIdx.x) * per;
+        step = 1;
+        count = j0 < T ? (T - j0 < per ? T - j0 : per) : 0;
+    }
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             ptx::prefetch_tensormap(&P.tmap);
         }
         int64_t issued = 0;
-        for (int64_t j = blockIdx.x; j < T; j += G, ++issued) {
+        for (int64_t j = j0; issued < count; j += step, ++issued) {
             const int s = static_cast<int>(issued % S);
             const uint32_t ph = static_cast<uint32_t>((issued / S) & 1);
             const int w = wait_phase<false>(empty(s), ph ^ 1u, P.timeout_ns, abort_flag);
@@ -378,7 +391,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     // ---------------------------------------------------- consumers
     const int ct = threadIdx.x - 32;
     int64_t i = 0;
-    for (int64_t j = blockIdx.x; j < T; j += G, ++i) {
+    for (int64_t j = j0; i < count; j += step, ++i) {
         const int s = static_cast<int>(i % S);
         const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
         int w = WAIT_OK;
@@ -500,6 +513,7 @@ void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeo
     P.status = status;
     P.coef_off = static_cast<uint32_t>(coef_off);
     P.hints = hints;
+    P.schedule = 0;
 }
 
 }  // namespace
@@ -572,17 +586,20 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
         case OP_COPY: {
             RingParams<OpCopyDev> P;
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            P.schedule = static_cast<uint32_t>(o.schedule);
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_SCALE: {
             RingParams<OpScaleDev> P;
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            P.schedule = static_cast<uint32_t>(o.schedule);
             P.op.alpha = op.alpha;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            P.schedule = static_cast<uint32_t>(o.schedule);
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);

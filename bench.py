@@ -517,7 +517,7 @@ def sweep(which: str, args):
         window["t1"] = datetime.datetime.now()
         return ms
 
-    if "scale" in groups or "tune" in groups or "hints" in groups:
+    if "scale" in groups or "tune" in groups or "hints" in groups or "schedule" in groups:
         n_t, t = SCALE_TILES, SCALE_TILE
         n = n_t * t
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
@@ -530,6 +530,22 @@ def sweep(which: str, args):
                 yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
                            grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+        if "schedule" in groups:
+            cands = [(2, 0, 0, 0), (2, 1, 0, 0), (3, 0, 0, 0), (3, 1, 0, 0), (4, 0, 0, 0), (4, 1, 0, 0),
+                     (2, 1, 32, 1), (2, 1, 64, 1), (3, 1, 48, 1), (2, 1, 16, 1)]
+            reps = {c: [] for c in cands}
+            for _ in range(5):
+                for S, sched, kib, cps in cands:
+                    ap.ap_debug_set(ap.AP_DBG_SCHEDULE, sched)
+                    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                    ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                    reps[(S, sched, kib, cps)].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S)))
+            for key in (ap.AP_DBG_SCHEDULE, ap.AP_DBG_STAGE_BYTES, ap.AP_DBG_CTAS_PER_SM):
+                ap.ap_debug_set(key, 0)
+            for (S, sched, kib, cps), v in reps.items():
+                v = sorted(v)
+                yield line("scale 2^28 f32", f"ring S={S} schedule={sched} stage={kib or 'auto'}KiB ctas/SM={cps or 'auto'}",
+                           8 * n, v[2], min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
         if "hints" in groups:
             reps = {h: [] for h in (0, 1, 2, 3)}
             for _ in range(5):

@@ -50,6 +50,8 @@ typedef enum ap_debug_key {
     AP_DBG_LAST_STAGE_ELEMS = 102, /* elements per ring stage (chunk elements for exchange) */
     AP_DBG_LAST_SMEM = 103,     /* dynamic shared memory per CTA, bytes */
     AP_DBG_LAST_STAGES = 104,   /* ring depth */
+    AP_DBG_SCHEDULE = 12,       /* ring stage order: 0 CTA b takes stages b, b + grid, ... (all CTAs
+                                   stream one window of memory); 1 each CTA takes a contiguous run */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar

@@ -41,6 +41,7 @@ def reset_debug(ap):
         ap.AP_DBG_EXCHANGE_STORE,
         ap.AP_DBG_CACHE_HINTS,
         ap.AP_DBG_DEVICE_CHECKS,
+        ap.AP_DBG_SCHEDULE,
     ):
         ap.ap_debug_set(key, 0)
 

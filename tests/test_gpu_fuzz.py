@@ -25,6 +25,7 @@ def _knobs(ap, rng):
     ap.ap_debug_set(ap.AP_DBG_GRID, int(rng.choice([0, 0, 1, 2, 5, 37])))
     ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2, 3])))
     ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, int(rng.choice([0, 8, 15, 16])))
+    ap.ap_debug_set(ap.AP_DBG_SCHEDULE, int(rng.choice([0, 1])))
 
 
 @pytest.mark.parametrize("seed", range(6))
