@@ -407,6 +407,9 @@ def bench_scale(args, d: Dist) -> dict:
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if not args.no_per_kernel:
+        del xh, yh, xd
+        res["per_kernel"] = per_kernel_lines(ap, synth, dev, stream, peak, x, y)
     if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
         import numpy as np  # noqa: F811
 
@@ -420,6 +423,48 @@ def bench_scale(args, d: Dist) -> dict:
             "sample": f"{passes} full passes of the oracle's scale over the 2^28-float input ({el:.1f} s, 1 thread)",
         }
     return res
+
+
+def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
+    """Every kernel of the path at its workload's full size, 20 timed launches
+    after 3 warm-up (CUDA events), as GB/s (read + write bytes) and the
+    fraction of the measured copy. Timed separately from the headline."""
+    import torch
+
+    out = {}
+
+    def put(name, nbytes, fn, **extra):
+        ms = time_steps(fn, 20, 3, stream) / 20
+        gb = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"GB/s": round(gb, 1), "frac": round(gb / peak, 4), "ms": round(ms, 4), **extra}
+
+    n = x.numel()  # 2^28 floats
+    put("scale_sync (baseline), 2^20 x 256", 8 * n, lambda: ap.ap_scale_sync(x, y, n // 256, 256, 2.0, stream))
+    for S in (3, 4):
+        put(f"scale ring S={S}, 2^20 x 256", 8 * n, lambda: ap.ap_scale(x, y, n // 256, 256, 2.0, S, stream))
+    put("row roll 2^26 x 4, shift 1", 8 * n, lambda: ap.ap_row_roll(x, y, n // 4, 4, 1, stream))
+    put("row roll 2^26 x 4, A + 4 bytes", 8 * (n - 4), lambda: ap.ap_row_roll(x[1:n - 3], y[:n - 4], (n - 4) // 4, 4, 1,
+                                                                                   stream))
+    for cs in (2, 4, 8):
+        put(f"cluster exchange cs={cs}, 32 KiB chunks", 8 * n,
+            lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768, stream))
+    codes = torch.full((n // 4,), 16, dtype=torch.int8, device=dev)
+    # per 16-byte chunk: 16 read + 16 written + 1 code byte
+    put("masked copy, all chunks copied", 33 * (n // 4), lambda: ap.ap_masked_copy(x, y, n // 4, codes, 4, stream))
+    del codes
+    xp = synth.uniform_pm1_torch(synth.SEED_POLY, 1 << 30, dev)
+    yp = torch.empty_like(xp)
+    for K in (8, 32, 128):
+        c = synth.coeffs_np(K).tolist()
+        put(f"poly K={K}, 2^30, S=2", 8 * (1 << 30), lambda: ap.ap_poly(xp, yp, 1 << 30, c, K, 2, stream),
+            fp32_tflops=None)
+        ms = out[f"poly K={K}, 2^30, S=2"]["ms"]
+        out[f"poly K={K}, 2^30, S=2"]["fp32_tflops"] = round(2.0 * K * (1 << 30) / (ms * 1e-3) / 1e12, 2)
+    del xp, yp
+    st = ap.ap_check()
+    if st != 0:
+        raise RuntimeError(f"device status {ap.ap_status_string(st)}")
+    return out
 
 
 def run_reference(args, d: Dist):
@@ -849,6 +894,7 @@ def main(argv=None):
     ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap_.add_argument("--workload", default="scale")
     ap_.add_argument("--no-cpu-baseline", action="store_true")
+    ap_.add_argument("--no-per-kernel", action="store_true")
     ap_.add_argument("--profile-case", choices=PROFILE_CASES, default=None)
     args = ap_.parse_args(argv)
     if args.warmup < 3:
