@@ -236,6 +236,35 @@ class Dist:
 # ----------------------------------------------------------------------------- oracle (CPU baseline)
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_parallel_rate(fn, arrays, n: int, bytes_per_elem: float, threads: int, min_seconds: float,
+                         max_passes: int) -> tuple[float, int, float]:
+    """The oracle's own loops over [0, n) split into `threads` contiguous ranges
+    run from Python threads (ctypes releases the GIL in foreign calls): bytes/s."""
+    import threading
+
+    bounds = [(t * n // threads, (t + 1) * n // threads) for t in range(threads)]
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        ths = [threading.Thread(target=fn, args=(*[a[lo:hi] for a in arrays], hi - lo)) for lo, hi in bounds]
+        for th in ths:
+            th.start()
+        for th in ths:
+            th.join()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= max_passes:
+            break
+    return bytes_per_elem * n * passes / el, passes, el
+
+
 def oracle_scale_rate(x_host, alpha: float, min_seconds: float, max_passes: int) -> tuple[float, int, float]:
     """Bytes/s of the oracle's scale over x_host, passes until min_seconds."""
     import numpy as np
@@ -421,6 +450,26 @@ def bench_scale(args, d: Dist) -> dict:
             "cores": 1,
             "kind": "oracle",
             "sample": f"{passes} full passes of the oracle's scale over the 2^28-float input ({el:.1f} s, 1 thread)",
+        }
+        import ctypes
+
+        import numpy as np
+
+        import oracle
+
+        lib = oracle.load()._lib
+        y_host = np.empty_like(x_host)
+        cores = host_cores()
+        fn = lambda a, b, m: lib.orc_scale(a.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),  # noqa: E731
+                                           b.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), m, ctypes.c_float(2.0))
+        prate, ppasses, pel = oracle_parallel_rate(fn, [x_host, y_host], x_host.size, 8.0, cores, 5.0, 40)
+        res["cpu_baseline_all_cores"] = {
+            "value": round(prate / 1e9, 3),
+            "unit": "GB/s",
+            "cores": cores,
+            "kind": "oracle",
+            "sample": f"{ppasses} passes over the 2^28-float input, the oracle's loop on {cores} contiguous ranges "
+                      f"in {cores} threads ({pel:.1f} s)",
         }
     return res
 
@@ -833,6 +882,60 @@ def sweep(which: str, args):
                 yield line("e2e scale 2^28 f32 pinned host", f"chunks={chunks} copy_streams={n_in}", 8 * n, ms / 10,
                            output_ok=ok)
         del x, xd, yd
+    if "oracle" in groups:
+        # the CPU oracle on each workload: one thread, and (where its loop splits
+        # into independent ranges) the same loop on every host core
+        import ctypes
+
+        import numpy as np
+
+        import oracle
+
+        orc = oracle.load()
+        lib = orc._lib
+        fp = ctypes.POINTER(ctypes.c_float)
+        cores = host_cores()
+
+        def rate1(fn, nbytes, min_s=2.0):
+            t0 = time.perf_counter()
+            k = 0
+            while True:
+                fn()
+                k += 1
+                el = time.perf_counter() - t0
+                if el >= min_s or k >= 20:
+                    return nbytes * k / el / 1e9
+
+        n = 1 << 28
+        x = synth.uniform_pm1_np(synth.SEED_SCALE, n)
+        y = np.empty_like(x)
+        r1 = rate1(lambda: orc.scale(x, 2.0), 8.0 * n)
+        sc = lambda a, b, m: lib.orc_scale(a.ctypes.data_as(fp), b.ctypes.data_as(fp), m, ctypes.c_float(2.0))  # noqa
+        rN = oracle_parallel_rate(sc, [x, y], n, 8.0, cores, 2.0, 20)[0] / 1e9
+        yield {"workload": "oracle: scale 2^28 f32", "GB/s 1 core": round(r1, 2), f"GB/s {cores} cores": round(rN, 2)}
+        A = x[: 1 << 28].reshape(-1, 4)
+        r1 = rate1(lambda: orc.row_roll(A, 1), 8.0 * n)
+        yield {"workload": "oracle: row roll 2^26x4 f32", "GB/s 1 core": round(r1, 2),
+               "note": "one call over the whole matrix (the wrap couples its ends)"}
+        r1 = rate1(lambda: orc.cluster_exchange(x, 4, 32768), 8.0 * n)
+        ex = lambda a, b, m: lib.orc_cluster_exchange(a.ctypes.data_as(fp), b.ctypes.data_as(fp), m, 4, 32768)  # noqa
+        groups = n // (4 * 8192)
+        # the threads' ranges must hold whole groups of 4 chunks
+        rN = oracle_parallel_rate(ex, [x, y], n, 8.0, cores, 2.0, 20)[0] / 1e9 if groups % cores == 0 else None
+        yield {"workload": "oracle: cluster exchange cs=4 2^28 f32", "GB/s 1 core": round(r1, 2),
+               f"GB/s {cores} cores": None if rN is None else round(rN, 2)}
+        m = 1 << 22
+        xs = x[:m]
+        ys = np.empty_like(xs)
+        for K in (8, 32, 128):
+            c = synth.coeffs_np(K)
+            r1 = rate1(lambda: orc.poly(xs, c), 8.0 * m)
+            pf = lambda a, b, mm: lib.orc_poly(a.ctypes.data_as(fp), b.ctypes.data_as(fp), mm,  # noqa: E731
+                                               c.ctypes.data_as(fp), K)
+            rN = oracle_parallel_rate(pf, [xs, ys], m, 8.0, cores, 2.0, 20)[0] / 1e9
+            yield {"workload": f"oracle: poly K={K} (2^22-float sample)", "GB/s 1 core": round(r1, 3),
+                   f"GB/s {cores} cores": round(rN, 3), "GFLOP/s 1 core": round(r1 / 8 * 2 * K, 2)}
+        del x, y
     if "small" in groups:
         A = torch.arange(256, dtype=torch.float32, device=dev).reshape(64, 4)
         B = torch.empty_like(A)
