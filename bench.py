@@ -919,9 +919,9 @@ def sweep(which: str, args):
                "note": "one call over the whole matrix (the wrap couples its ends)"}
         r1 = rate1(lambda: orc.cluster_exchange(x, 4, 32768), 8.0 * n)
         ex = lambda a, b, m: lib.orc_cluster_exchange(a.ctypes.data_as(fp), b.ctypes.data_as(fp), m, 4, 32768)  # noqa
-        groups = n // (4 * 8192)
+        n_groups = n // (4 * 8192)
         # the threads' ranges must hold whole groups of 4 chunks
-        rN = oracle_parallel_rate(ex, [x, y], n, 8.0, cores, 2.0, 20)[0] / 1e9 if groups % cores == 0 else None
+        rN = oracle_parallel_rate(ex, [x, y], n, 8.0, cores, 2.0, 20)[0] / 1e9 if n_groups % cores == 0 else None
         yield {"workload": "oracle: cluster exchange cs=4 2^28 f32", "GB/s 1 core": round(r1, 2),
                f"GB/s {cores} cores": None if rN is None else round(rN, 2)}
         m = 1 << 22
