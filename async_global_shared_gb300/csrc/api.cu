@@ -431,6 +431,20 @@ int64_t ap_debug_get(int key) {
     }
 }
 
+ap_status ap_debug_scale_pages_async(const float* in, float* out, int64_t n_tiles, int64_t tile_elems, float alpha,
+                                     cudaStream_t stream) {
+    if (n_tiles < 0 || tile_elems < 1 || tile_elems > 1024) return AP_ERR_SHAPE;
+    const int64_t n = n_tiles * tile_elems;
+    if (n == 0) return AP_OK;
+    if (in == nullptr || out == nullptr) return AP_ERR_NULL;
+    if (!aligned4(in) || !aligned4(out)) return AP_ERR_ALIGN;
+    if (in != out && overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    return launch_scale_pages_async(di, in, out, n_tiles, tile_elems, alpha, stream);
+}
+
 ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaStream_t stream) {
     if (out == nullptr) return AP_ERR_NULL;
     if (out_elems < 1 || iters < 1 || iters > (int64_t(1) << 24)) return AP_ERR_SHAPE;

@@ -41,7 +41,14 @@ Options options();
 // What a launcher reports about the launch it made (AP_DBG_LAST_*).
 void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem, int64_t stages, int64_t flags);
 
-enum Path : int64_t { PATH_RING = 1, PATH_ROLL_SMALL = 2, PATH_SYNC = 3, PATH_EXCHANGE = 4, PATH_MASKED = 5 };
+enum Path : int64_t {
+    PATH_RING = 1,
+    PATH_ROLL_SMALL = 2,
+    PATH_SYNC = 3,
+    PATH_EXCHANGE = 4,
+    PATH_MASKED = 5,
+    PATH_PAGES_ASYNC = 6
+};
 
 // Arguments of the per-element compute of a ring call.
 enum OpKind { OP_COPY, OP_SCALE, OP_POLY };
@@ -87,6 +94,9 @@ ap_status launch_roll_small(const DeviceInfo& di, const float* A, float* B, int6
 
 ap_status launch_scale_sync(const DeviceInfo& di, const float* in, float* out, int64_t n_tiles, int64_t tile,
                             float alpha, cudaStream_t stream);
+
+ap_status launch_scale_pages_async(const DeviceInfo& di, const float* in, float* out, int64_t n_tiles, int64_t tile,
+                                   float alpha, cudaStream_t stream);
 
 ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, int64_t n_chunks,
                              const signed char* codes, int stages, cudaStream_t stream);

@@ -489,6 +489,8 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
 
     n = x.numel()  # 2^28 floats
     put("scale_sync (baseline), 2^20 x 256", 8 * n, lambda: ap.ap_scale_sync(x, y, n // 256, 256, 2.0, stream))
+    put("scale, the pages' 2 x 1 KiB per-thread cp.async pipeline, 2^20 x 256", 8 * n,
+        lambda: ap.ap_debug_scale_pages_async(x, y, n // 256, 256, 2.0, stream))
     for S in (3, 4):
         put(f"scale ring S={S}, 2^20 x 256", 8 * n, lambda: ap.ap_scale(x, y, n // 256, 256, 2.0, S, stream))
     put("row roll 2^26 x 4, shift 1", 8 * n, lambda: ap.ap_row_roll(x, y, n // 4, 4, 1, stream))
@@ -619,6 +621,8 @@ def sweep(which: str, args):
         if "scale" in groups:
             ms = run(lambda: ap.ap_scale_sync(x, y, n_t, t, 2.0))
             yield line("scale 2^28 f32", "scale_sync", 8 * n, ms)
+            ms = run(lambda: ap.ap_debug_scale_pages_async(x, y, n_t, t, 2.0))
+            yield line("scale 2^28 f32", "the pages' async pipeline (2 x 1 KiB, per-thread cp.async)", 8 * n, ms)
             for S in (2, 3, 4, 5, 6):
                 ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
                 yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,

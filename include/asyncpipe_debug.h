@@ -45,7 +45,7 @@ typedef enum ap_debug_key {
                                    in AP_DBG_LAST_SITE) and nothing out of range is accessed */
     /* read-only: what the last call on this process launched */
     AP_DBG_LAST_PATH = 100,     /* 1 ring, 2 small row shift, 3 synchronous, 4 cluster exchange,
-                                   5 masked copy */
+                                   5 masked copy, 6 the pages' asynchronous tiled scale */
     AP_DBG_LAST_GRID = 101,     /* CTAs launched */
     AP_DBG_LAST_STAGE_ELEMS = 102, /* elements per ring stage (chunk elements for exchange) */
     AP_DBG_LAST_SMEM = 103,     /* dynamic shared memory per CTA, bytes */
@@ -64,6 +64,17 @@ ap_status ap_debug_set(int key, int64_t value);
 
 /* Read any key; -1 for an unknown key. */
 int64_t ap_debug_get(int key);
+
+/*
+ * The pages' own asynchronous tiled scale, kept as a measured baseline: a
+ * two-stage double buffer of one tile per CTA, every thread copying its own
+ * 4-byte element with cp.async, commit, wait for the older group, CTA
+ * barrier, compute, store ("CUDA Async Copy and Pipeline Guide",
+ * Implementation Comparison, "After" kernel; CTA b takes tiles b, b + grid,
+ * ...). Same arguments and result as ap_scale; tile_elems at most 1024.
+ */
+ap_status ap_debug_scale_pages_async(const float* in, float* out, int64_t n_tiles, int64_t tile_elems, float alpha,
+                                     cudaStream_t stream);
 
 /*
  * FP32 FMA throughput probe: each thread of a grid sized to the device runs

@@ -150,3 +150,17 @@ def test_scale_cache_hints(ap, orc, hints):
         assert ap.ap_check() == ap.AP_OK
         assert_bits(to_np(out.view), orc.scale(to_np(x), 2.0), f"hints={hints} S={stages}")
         assert out.intact()
+
+
+@pytest.mark.parametrize("n_tiles,tile", [(1, 1), (5, 3), (37, 256), (1000, 1024), (1 << 20, 256)])
+def test_scale_pages_async_baseline(ap, orc, n_tiles, tile):
+    """The pages' two-stage, per-thread cp.async version gives the same bits."""
+    dev = device()
+    n = n_tiles * tile
+    x = synth.uniform_pm1_torch(n + 3, n, dev)
+    out = Guarded(n, 0, dev)
+    ap.ap_debug_scale_pages_async(x, out.view, n_tiles, tile, 2.0)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 6
+    assert_bits(to_np(out.view), orc.scale(to_np(x), 2.0), f"pages async {n_tiles}x{tile}")
+    assert out.intact()
