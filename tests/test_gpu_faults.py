@@ -76,3 +76,23 @@ def test_bad_arguments_raise(ap):
         ap.ap_scale(x.double(), x, 1, 1024, 2.0, 2)
     with pytest.raises(TypeError):
         ap.ap_scale(x.cpu(), x, 1, 1024, 2.0, 2)
+
+
+def test_tensor_map_ring_wait_times_out_and_recovers(ap, orc):
+    """The same bounded wait behind the tensor-map producer."""
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    rows, cols = 20000, 4
+    A = synth.uniform_pm1_torch(6, rows * cols, dev)
+    B = torch.empty_like(A)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    _inject(ap)
+    ap.ap_row_roll(A, B, rows, cols, 1)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    reset_debug(ap)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    ap.ap_row_roll(A, B, rows, cols, 1)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(B), orc.row_roll(to_np(A).reshape(rows, cols), 1), "tensor roll after recovery")
