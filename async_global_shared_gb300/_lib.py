@@ -265,14 +265,14 @@ def ap_debug_emulate_ring(in_host, out_host, n: int, off: int, in_mis: int, out_
                                         stage_elems)
 
 
-def ap_debug_emulate_ring_tensor(in_host, out_host, rows: int, cols: int, shift: int, box_rows: int,
+def ap_debug_emulate_ring_tensor(in_host, out_host, rows: int, cols: int, shift: int, line_boxes: int,
                                  stage_elems: int) -> int:
-    """Host emulation of the tensor-map row shift (numpy float32 arrays); returns the status code."""
+    """Host emulation of the tensor-map producer's row shift (numpy float32 arrays); returns the status code."""
     import numpy as np
 
     assert in_host.dtype == np.float32 and out_host.dtype == np.float32
     return load().ap_debug_emulate_ring_tensor(in_host.ctypes.data, out_host.ctypes.data, rows, cols, shift,
-                                               box_rows, stage_elems)
+                                               line_boxes, stage_elems)
 
 
 def ap_debug_fma_probe(out, out_elems: int, iters: int, stream=None):

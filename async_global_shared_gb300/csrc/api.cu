@@ -171,7 +171,8 @@ ap_status ap_scale(const float* in, float* out, int64_t n_tiles, int64_t tile_el
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     OpArgs op{OP_SCALE, alpha, 0, nullptr};
-    return launch_ring(di, options(), in, out, n, 0, tile_elems, stages, op, 0, stream);
+    const Options o = options();
+    return launch_ring(di, o, in, out, n, 0, tile_elems, stages, op, o.force_path == 3, stream);
 }
 
 ap_status ap_scale_sync(const float* in, float* out, int64_t n_tiles, int64_t tile_elems, float alpha,
@@ -212,12 +213,9 @@ ap_status ap_row_roll(const float* A, float* B, int64_t rows, int64_t cols, int6
         return launch_roll_small(di, A, B, rows, cols, s, stream);
     }
     OpArgs op{OP_COPY, 1.0f, 0, nullptr};
-    // The tensor-map producer (2-D boxes of whole rows) on request, where the
-    // matrix meets its alignment rules; the 1-D bulk producer otherwise.
-    const bool tensor_ok = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0 &&
-                           cols % 4 == 0 && cols <= 256 && rows < (int64_t(1) << 30);
-    const int64_t tensor_cols = (o.force_path == 3 && tensor_ok) ? cols : 0;
-    return launch_ring(di, o, A, B, n, s * cols, cols, stages, op, tensor_cols, stream);
+    // The tensor-map producer on request (it falls back to the 1-D bulk
+    // producer where the matrix misses its alignment rules).
+    return launch_ring(di, o, A, B, n, s * cols, cols, stages, op, o.force_path == 3, stream);
 }
 
 ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, int degree, int stages,
@@ -233,7 +231,8 @@ ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, i
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     OpArgs op{OP_POLY, 0.0f, degree, coeffs};
-    return launch_ring(di, options(), in, out, n, 0, 1, stages, op, 0, stream);
+    const Options o = options();
+    return launch_ring(di, o, in, out, n, 0, 1, stages, op, o.force_path == 3, stream);
 }
 
 ap_status ap_cluster_exchange(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes,
@@ -496,25 +495,32 @@ ap_status emulate_ring(const StreamGeom& g, const float* in_host, float* out_hos
         for (int k = 0; k < sp.nspans && result == AP_OK; ++k) {
             const Span& sn = sp.span[k];
             if (g.box_bytes != 0) {
-                // tensor-map boxes: whole rows, rows past the matrix arrive as zeros
-                if (sn.bulk_dst % 128 || sn.x0 % g.cols || sn.bulk_bytes % g.box_bytes) {
+                // tensor-map boxes: one 2-D box of whole lines of the line
+                // view, or 1-D boxes from the span's first element (on a
+                // 16-byte boundary; what lies past n arrives as zeros)
+                if (sn.bulk_dst % 128) {
                     fail();
                     break;
                 }
-                const int64_t box_rows = g.box_elems / g.cols;
-                const int64_t rows = n / g.cols;
-                const uint32_t nbox = sn.bulk_bytes / g.box_bytes;
-                const uint32_t row_bytes = static_cast<uint32_t>(4 * g.cols);
-                for (uint32_t b = 0; b < nbox && result == AP_OK; ++b) {
-                    for (int64_t r = 0; r < box_rows; ++r) {
-                        const int64_t row = sn.x0 / g.cols + b * box_rows + r;
-                        const uint32_t dst = sn.bulk_dst + b * g.box_bytes + static_cast<uint32_t>(r) * row_bytes;
-                        if (row < rows) {
-                            gcopy(dst, in_addr + static_cast<uint64_t>(row) * row_bytes, row_bytes, row_bytes);
-                        } else {
-                            gcopy(dst, in_addr, row_bytes, 0);
-                        }
+                if (sn.line_y >= 0) {
+                    const int64_t e0 = g.line_r + sn.line_y * kFlatBoxElems;
+                    if (g.line_h <= 0 || sp.nspans != 1 || e0 != sn.x0 || sn.line_y + g.line_h > g.line_rows ||
+                        sn.bulk_bytes != 4 * kFlatBoxElems * g.line_h) {
+                        fail();
+                        break;
                     }
+                    gcopy(sn.bulk_dst, in_addr + 4 * static_cast<uint64_t>(e0), sn.bulk_bytes, sn.bulk_bytes);
+                    continue;
+                }
+                if (sn.x0 % 4 || sn.bulk_bytes % g.box_bytes ||
+                    sn.bulk_bytes != boxes_for(g, sn.x1 - sn.x0) * g.box_bytes) {
+                    fail();
+                    break;
+                }
+                const int64_t e_end = sn.x0 + static_cast<int64_t>(sn.bulk_bytes / 4);
+                for (int64_t e = sn.x0; e < e_end && result == AP_OK; ++e) {
+                    const uint32_t dst = sn.bulk_dst + static_cast<uint32_t>(4 * (e - sn.x0));
+                    gcopy(dst, in_addr + 4 * static_cast<uint64_t>(e < n ? e : 0), 4, e < n ? 4u : 0u);
                 }
                 continue;
             }
@@ -607,14 +613,16 @@ ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n
 }
 
 ap_status ap_debug_emulate_ring_tensor(const float* in_host, float* out_host, int64_t rows, int64_t cols,
-                                       int64_t shift, int64_t box_rows, int64_t stage_elems) {
-    if (rows < 1 || cols < 4 || cols % 4 || cols > 256) return AP_ERR_SHAPE;
-    if (box_rows < 8 || box_rows % 8 || box_rows > 256) return AP_ERR_SHAPE;
-    if (stage_elems < box_rows * cols || stage_elems % (box_rows * cols)) return AP_ERR_SHAPE;
-    if (in_host == nullptr || out_host == nullptr) return AP_ERR_NULL;
+                                       int64_t shift, int64_t line_boxes, int64_t stage_elems) {
+    if (rows < 1 || cols < 1 || cols > kMaxElems / rows) return AP_ERR_SHAPE;
+    if (line_boxes != 0 && line_boxes != 1) return AP_ERR_ARG;
+    if (stage_elems < kFlatBoxElems || stage_elems % kFlatBoxElems) return AP_ERR_SHAPE;
+    const int64_t n = rows * cols;
     const int64_t s = ((shift % rows) + rows) % rows;
+    if (!tensor_ok(uint64_t(1) << 40, uint64_t(3) << 40, n, s * cols)) return AP_ERR_ALIGN;
+    if (in_host == nullptr || out_host == nullptr) return AP_ERR_NULL;
     StreamGeom g;
-    make_geom_tensor(&g, uint64_t(1) << 40, uint64_t(3) << 40, rows * cols, s * cols, stage_elems, cols, box_rows);
+    make_geom_tensor(&g, uint64_t(1) << 40, uint64_t(3) << 40, n, s * cols, stage_elems, line_boxes != 0);
     return emulate_ring(g, in_host, out_host);
 }
 

@@ -77,7 +77,7 @@ ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, 
                 o.stage_bytes = kib * 1024;
                 o.ctas_per_sm = cps;
                 o.consumer_warps = warps;
-                ap_status st = launch_ring(di, o, in, out, n, off, unit, stages, op, 0, stream);  // warm-up
+                ap_status st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);  // warm-up
                 if (st == AP_ERR_SMEM) continue;
                 if (st != AP_OK) {
                     result = st;
@@ -86,7 +86,7 @@ ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, 
                 float ms_rep[3];
                 for (int r = 0; r < 3 && result == AP_OK; ++r) {
                     if (cudaEventRecord(e0, stream) != cudaSuccess) result = AP_ERR_CUDA;
-                    st = launch_ring(di, o, in, out, n, off, unit, stages, op, 0, stream);
+                    st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);
                     if (st != AP_OK) result = st;
                     if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
                         cudaEventElapsedTime(&ms_rep[r], e0, e1) != cudaSuccess)

@@ -84,10 +84,10 @@ ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, 
                         int64_t n, int64_t off, int64_t unit, int stages, const OpArgs& op, RingShape* best,
                         double* best_gbs, cudaStream_t stream);
 
-// tensor_cols > 0 selects the tensor-map producer for a rows x cols row shift
-// (in and out 16-byte aligned, cols a multiple of 4 and at most 256).
+// tensor asks for the tensor-map producer; where tensor_ok() refuses the
+// buffers, the 1-D bulk producer runs instead.
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
-                      int64_t unit, int stages, const OpArgs& op, int64_t tensor_cols, cudaStream_t stream);
+                      int64_t unit, int stages, const OpArgs& op, bool tensor, cudaStream_t stream);
 
 ap_status launch_roll_small(const DeviceInfo& di, const float* A, float* B, int64_t rows, int64_t cols, int64_t s,
                             cudaStream_t stream);

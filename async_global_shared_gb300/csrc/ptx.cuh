@@ -116,6 +116,18 @@ __device__ __forceinline__ void tensor_g2s_2d(uint32_t dst, const void* tmap, in
         : "memory");
 }
 
+// Global -> shared copy of one 1-D box described by a tensor map: box_elems
+// consecutive elements from element c0 (c0 * element size a multiple of 16);
+// elements past the tensor's end arrive as zeros. Completes `box bytes` of
+// transactions on bar; dst 128-byte aligned.
+__device__ __forceinline__ void tensor_g2s_1d(uint32_t dst, const void* tmap, int32_t c0, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(
+            dst),
+        "l"(tmap), "r"(c0), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

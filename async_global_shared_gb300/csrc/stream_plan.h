@@ -31,6 +31,18 @@
 // source size is the tail's byte count (the rest of the 16 is zero-filled).
 // If the buffer holds no aligned 16-byte block at all, every element is a
 // 4-byte copy.
+//
+// Tensor-map mode (input and output 16-byte aligned, every span starting on
+// a 16-byte boundary). The input is described twice to the copy engine: as a
+// flat 1-D tensor of n floats, loaded in boxes of 256 floats (1 KiB), and as a
+// 2-D "line view" of 1 KiB lines starting at element line_r = off mod 256,
+// loaded in boxes of one whole stage (se / 256 lines). A stage with a single
+// span that starts on a line of the view and whose box stays inside the
+// view's whole lines takes ONE 2-D box; the others (the stage that wraps past
+// n, the one that reaches the ragged end) take 1-D boxes. One copy-engine
+// instruction per stage matters: boxes issued back to back by one thread are
+// accepted about one per 25 ns on GB300, so 1 KiB boxes cannot keep a stage
+// ring fed from one producer thread.
 #pragma once
 
 #include <cstdint>
@@ -57,11 +69,12 @@ struct StreamGeom {
     int64_t h_in;         // inputs [0, h_in) lie before I0 (4-byte copies)
     int64_t t_in;         // inputs [t_in, n) lie at or after I1 (one zero-filling 16-byte copy)
     uint32_t slot_bytes;  // shared-memory bytes of one stage slot (multiple of 16)
-    // Tensor-map mode (row shift only; 0 = 1-D bulk copies): spans are whole
-    // rows and load as 2-D boxes of box_rows x cols floats.
-    uint32_t box_bytes;   // bytes of one box (multiple of 128), 0 in 1-D mode
-    int64_t box_elems;    // box_rows * cols
-    int64_t cols;         // row length of the tensor
+    // Tensor-map mode (box_bytes != 0; 0 = 1-D bulk copies).
+    uint32_t box_bytes;   // bytes of one flat 1-D box (1024), 0 in bulk mode
+    int64_t box_elems;    // floats of one flat 1-D box (256)
+    int64_t line_r;       // first element of the line view (off mod 256)
+    int64_t line_rows;    // whole 1 KiB lines in the line view
+    int64_t line_h;       // lines of one 2-D box (se / 256); 0: no line view
 };
 
 // Bytes of a stage slot for stages of `se` elements: two regions, each the
@@ -96,28 +109,49 @@ AP_HD void make_geom(StreamGeom* g, uint64_t in_addr, uint64_t out_addr, int64_t
     g->slot_bytes = slot_bytes_for(se);
     g->box_bytes = 0;
     g->box_elems = 0;
-    g->cols = 0;
+    g->line_r = 0;
+    g->line_rows = 0;
+    g->line_h = 0;
 }
 
-// Tensor-map geometry for the row shift of a rows x cols matrix whose input and
-// output are 16-byte aligned and cols a multiple of 4: off = shift * cols and
-// the stage a whole number of boxes, so every span starts on a row. A span
-// loads ceil(len / box_elems) whole boxes (the last may run past the span, or
-// past the last row, where the engine writes zeros), so each region is sized
-// for whole boxes: slot = 4 se + 2 box_bytes + 256, regions 128-byte aligned.
+// Floats in one box of the flat 1-D tensor map, and in one line of the line
+// view: the largest box extent a dimension may have (256), 1 KiB.
+constexpr int64_t kFlatBoxElems = 256;
+
+// Whether the tensor-map producer can stream n floats read at offset off:
+// input and output 16-byte aligned, and every span starting on a 16-byte
+// boundary (off a multiple of 4; n too when off != 0, for the span that
+// starts after the wrap), with box coordinates inside int32.
+AP_HD bool tensor_ok(uint64_t in_addr, uint64_t out_addr, int64_t n, int64_t off) {
+    if (((in_addr | out_addr) & 15) != 0 || n <= 0 || off < 0 || off >= n) return false;
+    return off % 4 == 0 && (off == 0 || n % 4 == 0) && n <= 0x7fffffffll - 2 * kFlatBoxElems;
+}
+
+// Tensor-map geometry (tensor_ok holds; se a multiple of 256). Spans load as
+// whole 1-D boxes from their first element (the last may run past the span,
+// or past n, where the engine writes zeros), so each region is sized for
+// whole boxes: slot = 4 se + 2 box_bytes + 256, regions 128-byte aligned. With
+// `lines`, the line view covers the whole lines from element off mod 256 and a
+// 2-D box is one stage (it fills region 0, 4 se bytes).
 AP_HD void make_geom_tensor(StreamGeom* g, uint64_t in_addr, uint64_t out_addr, int64_t n, int64_t off, int64_t se,
-                            int64_t cols, int64_t box_rows) {
+                            bool lines) {
     make_geom(g, in_addr, out_addr, n, off, se);
-    g->cols = cols;
-    g->box_elems = box_rows * cols;
-    g->box_bytes = static_cast<uint32_t>(4 * g->box_elems);
+    g->box_elems = kFlatBoxElems;
+    g->box_bytes = static_cast<uint32_t>(4 * kFlatBoxElems);
     g->slot_bytes = static_cast<uint32_t>(4 * se + 2 * static_cast<int64_t>(g->box_bytes) + 256);
+    if (lines) {
+        g->line_r = off % kFlatBoxElems;
+        g->line_rows = (n - g->line_r) / kFlatBoxElems;
+        g->line_h = se / kFlatBoxElems;
+        if (g->line_rows < g->line_h || g->line_h > 256) g->line_h = 0;
+    }
 }
 
 AP_HD int64_t boxes_for(const StreamGeom& g, int64_t len) { return (len + g.box_elems - 1) / g.box_elems; }
 
 struct Span {
     int64_t x0, x1;        // input elements [x0, x1)
+    int64_t line_y;        // tensor-map mode: first line of its one 2-D box, -1 for 1-D boxes
     uint32_t region;       // slot-relative byte offset of the span's region (multiple of 16)
     uint32_t lead;         // (in_addr + 4*x0) mod 16: byte offset of x0 inside the region
     int64_t head_end;      // [x0, head_end): 4-byte cp.async.ca copies
@@ -141,7 +175,8 @@ AP_HD void plan_span(const StreamGeom& g, int64_t x0, int64_t x1, uint32_t regio
     s->x0 = x0;
     s->x1 = x1;
     s->region = region;
-    if (g.box_bytes != 0) {  // whole rows, aligned: boxes only, no edges
+    s->line_y = -1;
+    if (g.box_bytes != 0) {  // whole boxes from an aligned first element: no edges
         s->lead = 0;
         s->head_end = x0;
         s->tail_begin = x1;
@@ -196,6 +231,12 @@ AP_HD void plan_stage(const StreamGeom& g, int64_t j, StagePlan* p) {
         plan_span(g, 0, L - len1, r2, &p->span[1]);
     } else {
         p->nspans = 1;
+        // one 2-D box of the line view for the whole stage where it fits
+        const int64_t rel = a - g.line_r;
+        if (g.line_h > 0 && rel >= 0 && rel % kFlatBoxElems == 0 && rel / kFlatBoxElems + g.line_h <= g.line_rows) {
+            p->span[0].line_y = rel / kFlatBoxElems;
+            p->span[0].bulk_bytes = static_cast<uint32_t>(4 * kFlatBoxElems * g.line_h);
+        }
     }
     int64_t e_al = lo > g.out_head ? lo : g.out_head;
     if (e_al > hi) e_al = hi;

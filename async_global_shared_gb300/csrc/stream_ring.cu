@@ -72,6 +72,7 @@ struct OpPolyDev {
     float c[AP_POLY_MAX_DEGREE + 1];
     __device__ __forceinline__ void stage(float* cs, int tid, int nthreads) const {
         for (int k = tid; k <= degree; k += nthreads) cs[k] = c[k];
+        if (tid < 4) cs[tid - 4] = 0.0f;
     }
     template <int N>
     __device__ __forceinline__ void apply(float (&v)[N], const float* cs) const {
@@ -85,17 +86,24 @@ struct OpPolyDev {
 #pragma unroll
             for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], ck);
         }
+        // Steps k, k-1, k-2, k-3 from one aligned 16-byte word, the next word
+        // loaded one iteration ahead (the last iteration reads the four zero
+        // floats staged before c[0]).
+        if (k >= 3) {
+            float4 q = *reinterpret_cast<const float4*>(cs + k - 3);
 #pragma unroll 2
-        for (; k >= 3; k -= 4) {  // steps k, k-1, k-2, k-3 from one aligned 16-byte word
-            const float4 q = *reinterpret_cast<const float4*>(cs + k - 3);
+            for (; k >= 3; k -= 4) {
+                const float4 next = *reinterpret_cast<const float4*>(cs + k - 7);
 #pragma unroll
-            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.w);
+                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.w);
 #pragma unroll
-            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.z);
+                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.z);
 #pragma unroll
-            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.y);
+                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.y);
 #pragma unroll
-            for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.x);
+                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.x);
+                q = next;
+            }
         }
 #pragma unroll
         for (int t = 0; t < N; ++t) v[t] = p[t];
@@ -104,7 +112,8 @@ struct OpPolyDev {
 
 template <class Op>
 struct RingParams {
-    CUtensorMap tmap;   // the row shift's input as a rows x cols tensor (tensor-map mode only)
+    CUtensorMap tmap;        // tensor-map mode: the input as a flat 1-D tensor (boxes of 256 floats)
+    CUtensorMap tmap_lines;  // tensor-map mode: the line view (2-D boxes of one stage), if g.line_h > 0
     const float* in;
     float* out;
     StreamGeom g;
@@ -173,7 +182,14 @@ __device__ __forceinline__ bool producer_plan_ok(const StreamGeom& g, const Stag
         if (sn.x0 < 0 || sn.x1 > g.n || sn.x0 >= sn.x1) return false;
         if (g.box_bytes != 0) {
             if (sn.bulk_dst % 128 || sn.bulk_dst + static_cast<uint64_t>(sn.bulk_bytes) > g.slot_bytes) return false;
-            if (sn.x0 % g.cols) return false;
+            if (sn.line_y >= 0) {  // one 2-D box of whole lines inside the line view
+                if (g.line_h <= 0 || sp.nspans != 1 || sn.x0 != g.line_r + sn.line_y * kFlatBoxElems) return false;
+                if (sn.line_y + g.line_h > g.line_rows || sn.bulk_bytes != 4 * kFlatBoxElems * g.line_h) return false;
+                continue;
+            }
+            if (sn.x0 % 4 != 0) return false;
+            if (sn.bulk_bytes % g.box_bytes || boxes_for(g, sn.x1 - sn.x0) * g.box_bytes != sn.bulk_bytes) return false;
+            if (sn.x0 + (boxes_for(g, sn.x1 - sn.x0) - 1) * g.box_elems > 0x7fffffffll) return false;  // int32
             continue;
         }
         if (sn.bulk_bytes) {
@@ -223,6 +239,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
         vec_groups<kG, kConsumers>(P, src, dst, q, ngroups, cs);
         if (kG > 4) vec_groups<4, kConsumers>(P, src, dst, q, ngroups, cs);
+        vec_groups<2, kConsumers>(P, src, dst, q, ngroups, cs);
         vec_groups<1, kConsumers>(P, src, dst, q, ngroups, cs);
     } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
@@ -280,7 +297,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     auto full = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(s); };
     auto empty = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(S + s); };
 
-    float* cs = reinterpret_cast<float*>(smem + P.coef_off);
+    float* cs = reinterpret_cast<float*>(smem + P.coef_off) + 4;  // the op's data, after 16 bytes of zeros
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full(s), 1);
@@ -321,6 +338,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
                 return;
             }
             ptx::prefetch_tensormap(&P.tmap);
+            if (P.g.line_h > 0) ptx::prefetch_tensormap(&P.tmap_lines);
         }
         int64_t issued = 0;
         for (int64_t j = j0; issued < count; j += step, ++issued) {
@@ -360,13 +378,19 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
                 const Span& sn = sp.span[k];
                 if (sn.bulk_bytes == 0) continue;
                 if (P.g.box_bytes != 0) {
-                    // tensor-map mode: whole boxes of box_rows rows from the span's first row
-                    const int32_t box_rows = static_cast<int32_t>(P.g.box_elems / P.g.cols);
-                    const int32_t row0 = static_cast<int32_t>(sn.x0 / P.g.cols);
-                    const uint32_t nbox = sn.bulk_bytes / P.g.box_bytes;
-                    for (uint32_t b = 0; b < nbox; ++b)
-                        ptx::tensor_g2s_2d(slot + sn.bulk_dst + b * P.g.box_bytes, &P.tmap, 0,
-                                           row0 + static_cast<int32_t>(b) * box_rows, full(s));
+                    // tensor-map mode: the stage as one 2-D box of the line
+                    // view, else whole 1-D boxes from the span's first element
+                    if (sn.line_y >= 0) {
+                        ptx::tensor_g2s_2d(slot + sn.bulk_dst, &P.tmap_lines, 0, static_cast<int32_t>(sn.line_y),
+                                           full(s));
+                    } else {
+                        const uint32_t nbox = sn.bulk_bytes / P.g.box_bytes;
+                        const int32_t be = static_cast<int32_t>(P.g.box_elems);
+                        const int32_t x0 = static_cast<int32_t>(sn.x0);
+                        for (uint32_t b = 0; b < nbox; ++b)
+                            ptx::tensor_g2s_1d(slot + sn.bulk_dst + b * P.g.box_bytes, &P.tmap,
+                                               x0 + static_cast<int32_t>(b) * be, full(s));
+                    }
                     continue;
                 }
                 if (P.hints & 1u) {
@@ -470,9 +494,11 @@ RingShape auto_ring_shape(OpKind kind, int stages) {
     // ring per SM in 16-24 KiB stages for depths 2-4; larger rings lose
     // bandwidth. The fma-heavy polynomial wants 16 consumer warps and the
     // largest stages that fit, since every stage costs each consumer warp a
-    // barrier wait, a descriptor read and a release.
+    // barrier wait, a descriptor read and a release; in multiples of 32 KiB
+    // (512 consumers x 16 chains x 4 bytes), so that every chain of every
+    // thread is busy for the whole stage.
     if (kind == OP_POLY) {
-        const int64_t per = (196 * 1024) / stages / 4096 * 4096;
+        const int64_t per = (196 * 1024) / stages / (32 * 1024) * (32 * 1024);
         return RingShape{std::min<int64_t>(96 * 1024, per), 1, 16};
     }
     switch (stages) {
@@ -502,8 +528,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 template <class Op>
 void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeom& g, int stages, uint32_t tx_extra,
-                 uint64_t timeout, uint32_t* status, int64_t coef_off, uint32_t hints, const CUtensorMap& tmap) {
+                 uint64_t timeout, uint32_t* status, int64_t coef_off, uint32_t hints, const CUtensorMap& tmap,
+                 const CUtensorMap& tmap_lines) {
     P.tmap = tmap;
+    P.tmap_lines = tmap_lines;
     P.in = in;
     P.out = out;
     P.g = g;
@@ -519,53 +547,55 @@ void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeo
 }  // namespace
 
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
-                      int64_t unit, int stages, const OpArgs& op, int64_t tensor_cols, cudaStream_t stream) {
+                      int64_t unit, int stages, const OpArgs& op, bool tensor, cudaStream_t stream) {
     RingShape shape;
-    if (tensor_cols > 0 || !tuned_shape(di.device, op.kind, stages, &shape)) shape = auto_ring_shape(op.kind, stages);
+    if (tensor || !tuned_shape(di.device, op.kind, stages, &shape)) shape = auto_ring_shape(op.kind, stages);
     const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : shape.payload;
     const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : shape.ctas_per_sm;
     const int64_t warps = o.consumer_warps > 0 ? o.consumer_warps : shape.consumer_warps;
     int64_t se = stage_elems_for(payload, unit);
     StreamGeom g;
-    CUtensorMap tmap;
+    CUtensorMap tmap, tmap_lines;
     std::memset(&tmap, 0, sizeof(tmap));
-    if (tensor_cols > 0) {
-        // Row shift through 2-D tensor-map boxes of box_rows x cols floats:
-        // box_rows a multiple of 8 (every box a multiple of 128 bytes), boxes
-        // of at most 8 KiB (a slot holds two boxes beyond its stage), and no
-        // more rows than the matrix has, rounded up to 8.
-        const int64_t cols = tensor_cols;
-        const int64_t rows = n / cols;
-        int64_t box_rows = std::max<int64_t>(8, std::min<int64_t>(256, 8192 / (4 * cols)) / 8 * 8);
-        box_rows = std::min<int64_t>(box_rows, (rows + 7) / 8 * 8);
-        const int64_t box_elems = box_rows * cols;
-        se = std::max<int64_t>(box_elems, se / box_elems * box_elems);
+    std::memset(&tmap_lines, 0, sizeof(tmap_lines));
+    const bool use_tensor = tensor && tensor_ok(reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off);
+    if (use_tensor) {
+        // Whole 1 KiB boxes per stage; automatic stages give up boxes until
+        // the ring (each slot two boxes larger than its stage) fits in shared
+        // memory.
+        se = std::max<int64_t>(kFlatBoxElems, se / kFlatBoxElems * kFlatBoxElems);
         if (o.stage_bytes == 0) {
-            // automatic stages: give up whole boxes until the ring (each slot
-            // two boxes larger than its stage) fits in shared memory
             auto ring_bytes = [&](int64_t e) {
-                return static_cast<int64_t>(stages) * (4 * e + 8 * box_elems + 256 + 64) + 16 * stages + 16;
+                return static_cast<int64_t>(stages) * (4 * e + 8 * kFlatBoxElems + 256 + 64) + 16 * stages + 16;
             };
-            while (se > box_elems && ring_bytes(se) > di.smem_optin) se -= box_elems;
+            while (se > kFlatBoxElems && ring_bytes(se) > di.smem_optin) se -= kFlatBoxElems;
         }
-        make_geom_tensor(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se, cols,
-                         box_rows);
+        make_geom_tensor(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se, true);
         auto encode = tensor_map_encoder();
         if (encode == nullptr) return AP_ERR_CUDA;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(4 * cols)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), static_cast<cuuint32_t>(box_rows)};
         const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(in), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return AP_ERR_CUDA;
+        const cuuint64_t dims[1] = {static_cast<cuuint64_t>(n)};
+        const cuuint64_t strides[1] = {0};  // a rank-1 tensor has no strides; never read
+        const cuuint32_t box[1] = {static_cast<cuuint32_t>(kFlatBoxElems)};
+        CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(in), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS && g.line_h > 0) {
+            // line_rows lines of 256 floats from element line_r (16-byte aligned: off % 4 == 0)
+            const cuuint64_t ldims[2] = {static_cast<cuuint64_t>(kFlatBoxElems), static_cast<cuuint64_t>(g.line_rows)};
+            const cuuint64_t lstrides[1] = {static_cast<cuuint64_t>(4 * kFlatBoxElems)};
+            const cuuint32_t lbox[2] = {static_cast<cuuint32_t>(kFlatBoxElems), static_cast<cuuint32_t>(g.line_h)};
+            r = encode(&tmap_lines, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(in) + g.line_r, ldims,
+                       lstrides, lbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (r != CUDA_SUCCESS) return AP_ERR_CUDA;
     } else {
         make_geom(&g, reinterpret_cast<uint64_t>(in), reinterpret_cast<uint64_t>(out), n, off, se);
     }
     const int64_t coef_off =
         static_cast<int64_t>(stages) * (g.slot_bytes + static_cast<int64_t>(sizeof(SlotDesc))) + 2 * 8 * stages + 16;
-    const int64_t coef_bytes = op.kind == OP_POLY ? (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
+    const int64_t coef_bytes = op.kind == OP_POLY ? 16 + (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
     const int64_t smem = coef_off + coef_bytes;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
     int64_t grid = std::min<int64_t>(g.n_stages, static_cast<int64_t>(di.sms) * cps);
@@ -576,7 +606,7 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     int64_t flags = 0;
     if (g.h_in > 0 || g.t_in < n) flags |= 1;
     if (((ia + 4 * static_cast<uint64_t>(off) - oa) & 15) != 0 || off != 0) flags |= 2;
-    if (tensor_cols > 0) flags |= 4;
+    if (use_tensor) flags |= g.line_h > 0 ? 4 | 8 : 4;
     record_launch(PATH_RING, grid, se, smem, stages, flags);
 
     const uint64_t timeout = static_cast<uint64_t>(o.timeout_ns);
@@ -585,20 +615,20 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     switch (op.kind) {
         case OP_COPY: {
             RingParams<OpCopyDev> P;
-            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
             P.schedule = static_cast<uint32_t>(o.schedule);
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_SCALE: {
             RingParams<OpScaleDev> P;
-            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
             P.schedule = static_cast<uint32_t>(o.schedule);
             P.op.alpha = op.alpha;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
-            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap);
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
             P.schedule = static_cast<uint32_t>(o.schedule);
             P.op.degree = op.degree;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;

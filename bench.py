@@ -613,7 +613,7 @@ def sweep(which: str, args):
         window["t1"] = datetime.datetime.now()
         return ms
 
-    if "scale" in groups or "tune" in groups or "hints" in groups or "schedule" in groups:
+    if "scale" in groups or "tune" in groups or "hints" in groups or "schedule" in groups or "tensortune" in groups:
         n_t, t = SCALE_TILES, SCALE_TILE
         n = n_t * t
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
@@ -628,6 +628,13 @@ def sweep(which: str, args):
                 yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
                            grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+            ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)  # the tensor-map producer
+            for S in (2, 3, 4, 5, 6):
+                ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
+                yield line("scale 2^28 f32", f"ring tensor-map producer S={S}", 8 * n, ms,
+                           stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
+                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
+            ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 0)
         if "schedule" in groups:
             cands = [(2, 0, 0, 0), (2, 1, 0, 0), (3, 0, 0, 0), (3, 1, 0, 0), (4, 0, 0, 0), (4, 1, 0, 0),
                      (2, 1, 32, 1), (2, 1, 64, 1), (3, 1, 48, 1), (2, 1, 16, 1)]
@@ -655,6 +662,23 @@ def sweep(which: str, args):
                 v = sorted(v)
                 yield line("scale 2^28 f32", f"ring S=2 cache_hints={h} (median of 5)", 8 * n, v[2],
                            min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
+        if "tensortune" in groups:
+            # the tensor-map producer: ring depth x stage size x CTAs per SM
+            cands = [(S, kib, cps) for S in (2, 3, 4, 6) for kib in (8, 16, 32) for cps in (1, 2, 3, 4)
+                     if S * (kib + 3) * cps <= 220]
+            reps = {c: [] for c in cands}
+            ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+            for _ in range(3):
+                for S, kib, cps in cands:
+                    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                    ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                    reps[(S, kib, cps)].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S)))
+            for key in (ap.AP_DBG_FORCE_PATH, ap.AP_DBG_STAGE_BYTES, ap.AP_DBG_CTAS_PER_SM):
+                ap.ap_debug_set(key, 0)
+            for (S, kib, cps), v in reps.items():
+                v = sorted(v)
+                yield line("scale 2^28 f32", f"ring tensor-map producer S={S} stage={kib}KiB ctas/SM={cps} (median of 3)",
+                           8 * n, v[1], min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
         if "tune" in groups:
             cands = [(2, 16, 2), (2, 12, 3), (3, 24, 1), (3, 8, 3), (4, 16, 1), (4, 8, 2),
                      (5, 12, 1), (5, 16, 1), (5, 8, 2), (5, 36, 1), (5, 24, 1), (5, 6, 3), (5, 4, 4),
@@ -688,7 +712,7 @@ def sweep(which: str, args):
         if "polywarps" in groups:
             for K in (8, 32, 128):
                 c = synth.coeffs_np(K).tolist()
-                for warps in (15, 16):
+                for warps in (8, 15, 16):
                     ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
                     for S, kib in ((2, 96), (3, 64), (4, 48), (6, 32)):
                         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
@@ -736,13 +760,17 @@ def sweep(which: str, args):
                 yield line("roll 2^26x4 f32", f"ring {name} S={S or 'default'}", 8 * n, ms,
                            flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
-        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)  # the 2-D tensor-map producer (aligned variant)
-        for S in (2, 3, 4):
-            ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
-            A, B = abuf[:n], bbuf[:n]
-            ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
-            yield line("roll 2^26x4 f32", f"ring tensor-map producer S={S}", 8 * n, ms,
-                       flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
+        # the tensor-map producer (aligned variant): each stage one 2-D box of
+        # 1 KiB lines of the input, the stage that wraps as 1-D boxes
+        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+        for r, c in ((rows, cols), (n // 64, 64)):
+            for S in (2, 3, 4):
+                ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
+                A, B = abuf[:n], bbuf[:n]
+                ms = run(lambda: ap.ap_row_roll(A, B, r, c, 1))
+                fl = ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS)
+                yield line(f"roll {r}x{c} f32", f"ring tensor-map producer S={S}",
+                           8 * n, ms, flags=fl, stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
         ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 0)
         ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
         del abuf, bbuf

@@ -21,10 +21,13 @@ extern "C" {
 typedef enum ap_debug_key {
     /* settable */
     AP_DBG_FORCE_PATH = 1,      /* 0 auto; 1 always the ring (also for small row shifts);
-                                   2 small one-CTA row shift when it fits; 3 row shift through the
-                                   ring with a 2-D tensor-map producer (cp.async.bulk.tensor boxes of
-                                   whole rows) where A and B are 16-byte aligned and cols is a
-                                   multiple of 4 no larger than 256, the 1-D producer otherwise */
+                                   2 small one-CTA row shift when it fits; 3 ring with a tensor-map
+                                   producer (cp.async.bulk.tensor) for ap_row_roll, ap_scale and
+                                   ap_poly where input and output are 16-byte aligned and every span
+                                   starts on a 16-byte boundary (shift * cols a multiple of 4, and
+                                   rows * cols too for a nonzero shift): each stage one 2-D box of
+                                   1 KiB lines of the input where it fits, else 1-D boxes of 256
+                                   floats; the 1-D bulk producer otherwise */
     AP_DBG_EXPECT_TX_EXTRA = 2, /* bytes added to every stage's expected transaction count:
                                    the barrier then never completes and the consumers' bounded
                                    waits give up (fault injection; 0 = off) */
@@ -33,7 +36,7 @@ typedef enum ap_debug_key {
     AP_DBG_STAGE_BYTES = 4,     /* ring stage payload in bytes (0 = automatic) */
     AP_DBG_GRID = 5,            /* cap on the number of CTAs of ring kernels (0 = automatic) */
     AP_DBG_CTAS_PER_SM = 6,     /* resident ring CTAs per SM the grid is sized for (0 = 1) */
-    AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 4) */
+    AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 3) */
     AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8, 15 or 16 (0 = automatic) */
     AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
                                    piece to a shared->global bulk copy, 2 eight warps of 16-byte stores */
@@ -56,7 +59,8 @@ typedef enum ap_debug_key {
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar
                                    shared-memory path (input/output alignments differ or wrap);
-                                   bit 2: the tensor-map producer ran */
+                                   bit 2: the tensor-map producer ran; bit 3: with the line
+                                   view (2-D boxes of whole stages) set up beside the flat map */
 } ap_debug_key;
 
 /* Set a settable key. AP_ERR_ARG for an unknown key or a negative value. */
@@ -105,16 +109,22 @@ ap_status ap_debug_emulate_ring(const float* in_host, float* out_host, int64_t n
                                 int in_mis, int out_mis, int64_t stage_elems);
 
 /*
- * As ap_debug_emulate_ring, for the tensor-map producer of the row shift:
+ * As ap_debug_emulate_ring, for the tensor-map producer:
  * B[i, :] = A[(i + shift) mod rows, :] for a rows x cols matrix at 16-byte
- * aligned addresses, spans loaded as whole boxes of box_rows x cols floats
- * (rows past the matrix arrive as zeros, as the copy engine writes them).
- * Checks every box destination (128-byte aligned, inside the slot) and every
- * consumer access. cols a multiple of 4 in 4..256, box_rows a multiple of 8
- * in 8..256, stage_elems a multiple of box_rows * cols.
+ * aligned addresses (shift 0 is the plain stream of scale and poly). Spans
+ * load as whole 1-D boxes of 256 floats of the flat input (floats past its
+ * end arrive as zeros, as the copy engine writes them); with line_boxes = 1 a
+ * stage whose single span starts on a line of the line view (1 KiB lines from
+ * element (shift mod rows) * cols mod 256) and stays inside its whole lines
+ * loads as one 2-D box instead. (shift mod rows) * cols must be a multiple
+ * of 4, and rows * cols too when that shift is not 0 (else AP_ERR_ALIGN);
+ * stage_elems a multiple of 256; line_boxes 0 or 1 (else AP_ERR_ARG).
+ * Checks every box (first coordinate on a 16-byte boundary, a 2-D box inside
+ * the line view, destination 128-byte aligned and inside the slot) and every
+ * consumer access.
  */
 ap_status ap_debug_emulate_ring_tensor(const float* in_host, float* out_host, int64_t rows, int64_t cols,
-                                       int64_t shift, int64_t box_rows, int64_t stage_elems);
+                                       int64_t shift, int64_t line_boxes, int64_t stage_elems);
 
 #ifdef __cplusplus
 }

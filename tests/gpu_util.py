@@ -88,3 +88,14 @@ def assert_bits(got, want, what: str, nan_equal: bool = False):
         f"{what}: {bad.size} of {g.size} differ; first {bad[:5].tolist()} got {g[bad[:5]].tolist()} "
         f"want {w[bad[:5]].tolist()}"
     )
+
+
+def tensor_flags(ap, n: int, off: int) -> int:
+    """LAST_FLAGS bits 2-3 the tensor-map producer should report for a stream
+    of n floats read at offset off, from the stage size the call used: bit 2
+    always; bit 3 when the line view (1 KiB lines from element off mod 256)
+    holds at least one whole stage."""
+    se = ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS)
+    line_h = se // 256
+    line_rows = (n - off % 256) // 256
+    return 12 if 0 < line_h <= 256 and line_rows >= line_h else 4

@@ -185,21 +185,45 @@ def test_emulator_rejects_bad_arguments(ap):
     assert ap.ap_debug_emulate_ring(x, y, 16, 0, 0, 0, 6) == ap.AP_ERR_SHAPE
 
 
-def test_emulated_tensor_ring_matches_oracle(ap, orc):
-    """The tensor-map producer's plan: whole-row boxes (zero rows past the
-    end), 128-byte aligned box destinations, every element moved once."""
-    rng = np.random.default_rng(9)
+@pytest.mark.parametrize("line_boxes", [0, 1])
+def test_emulated_tensor_ring_matches_oracle(ap, orc, line_boxes):
+    """The tensor-map producer's plan: each stage one 2-D box of the line view
+    (1 KiB lines from element off mod 256) where it fits, else 1-D boxes of
+    256 floats from the span's first element (on a 16-byte boundary, zeros
+    past the end); every element moved once. Shift 0 is the plain stream of
+    scale and poly, any length."""
+    rng = np.random.default_rng(9 + line_boxes)
     for _ in range(200):
-        cols = int(rng.choice([4, 8, 12, 16, 64, 256]))
-        rows = int(rng.integers(1, 3000 // cols + 2))
-        box_rows = int(rng.choice([8, 16, 64, 256]))
-        stage_elems = box_rows * cols * int(rng.integers(1, 4))
-        shift = int(rng.integers(-2 * rows, 2 * rows + 1))
-        A = synth.uniform_pm1_np(rows + cols, rows * cols).reshape(rows, cols)
-        y = np.full(rows * cols, np.nan, dtype=np.float32)
-        st = ap.ap_debug_emulate_ring_tensor(A.ravel(), y, rows, cols, shift, box_rows, stage_elems)
-        assert st == ap.AP_OK, (rows, cols, shift, box_rows, stage_elems)
+        cols = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 64, 300]))
+        rows = int(rng.integers(1, 6000 // cols + 2))
+        stage_elems = 256 * int(rng.integers(1, 6))
+        if rng.random() < 0.4:
+            shift = 0
+        else:
+            # a shift whose element offset is a multiple of 4 (rows * cols too)
+            rows = (rows + 3) // 4 * 4 if cols % 4 else rows
+            step = 4 // np.gcd(cols, 4)
+            shift = int(rng.integers(-rows, rows + 1)) * step
+        n = rows * cols
+        A = synth.uniform_pm1_np(n + 7, n).reshape(rows, cols)
+        y = np.full(n, np.nan, dtype=np.float32)
+        st = ap.ap_debug_emulate_ring_tensor(A.ravel(), y, rows, cols, shift, line_boxes, stage_elems)
+        assert st == ap.AP_OK, (rows, cols, shift, stage_elems)
         assert np.array_equal(y.reshape(rows, cols).view(np.uint32), orc.row_roll(A, shift).view(np.uint32))
     x = np.zeros(64, dtype=np.float32)
-    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 16, 4, 1, 12, 48) == ap.AP_ERR_SHAPE  # box rows not x8
-    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 16, 6, 1, 8, 48) == ap.AP_ERR_SHAPE  # cols not x4
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 64, 1, 1, line_boxes, 256) == ap.AP_ERR_ALIGN  # 4-byte offset
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 32, 2, 1, line_boxes, 256) == ap.AP_ERR_ALIGN  # 8 bytes
+    assert ap.ap_debug_emulate_ring_tensor(x[:63], x[:63].copy(), 21, 3, 4, line_boxes, 256) == ap.AP_ERR_ALIGN
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 64, 1, 0, line_boxes, 128) == ap.AP_ERR_SHAPE  # not x256
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 16, 4, 4, line_boxes, 512) == ap.AP_OK
+    assert ap.ap_debug_emulate_ring_tensor(x, x.copy(), 16, 4, 4, 2, 512) == ap.AP_ERR_ARG
+
+
+def test_emulated_tensor_ring_large_line_view(ap, orc):
+    """Many whole-stage 2-D boxes: a 2**18 x 4 shift by 1 (line view from
+    element 4) and a plain stream with a ragged end."""
+    for rows, cols, shift, se in ((1 << 18, 4, 1, 6144), (1 << 18, 4, -77, 4096), (100003, 1, 0, 4096)):
+        A = synth.uniform_pm1_np(rows, rows * cols).reshape(rows, cols)
+        y = np.full(rows * cols, np.nan, dtype=np.float32)
+        assert ap.ap_debug_emulate_ring_tensor(A.ravel(), y, rows, cols, shift, 1, se) == ap.AP_OK
+        assert np.array_equal(y.reshape(rows, cols).view(np.uint32), orc.row_roll(A, shift).view(np.uint32))

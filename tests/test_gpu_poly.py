@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, tensor_flags, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +34,22 @@ def test_poly_small(ap, orc, degree, stages):
         ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
         assert ap.ap_check() == ap.AP_OK
         assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} stage={stage_bytes} warps={warps}")
+        assert out.intact()
+
+
+@pytest.mark.parametrize("degree", [0, 3, 8, 128])
+def test_poly_tensor_map_producer(ap, orc, degree):
+    """Horner over the tensor-map producer's boxes, ragged lengths."""
+    dev = device()
+    c = synth.coeffs_np(degree)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    for n, stages in ((1, 2), (7, 3), (256, 4), (20011, 2), (20011, 6), (1 << 18, 3)):
+        x = synth.uniform_pm1_torch(n + degree, n, dev)
+        out = Guarded(n, 0, dev)
+        ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 12 == tensor_flags(ap, n, 0)
+        assert_bits(to_np(out.view), orc.poly(to_np(x), c), f"tensor poly K={degree} n={n} S={stages}")
         assert out.intact()
 
 

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, tensor_flags, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -117,26 +117,50 @@ def test_roll_full_size(ap, orc, variant):
 
 
 @pytest.mark.parametrize("stages", [2, 3, 6])
-@pytest.mark.parametrize("rows,cols", [(1, 4), (7, 4), (64, 4), (1000, 4), (50000, 4), (333, 8), (129, 256), (40, 12)])
+@pytest.mark.parametrize(
+    "rows,cols",
+    [(1, 4), (7, 4), (64, 4), (1000, 4), (50000, 4), (333, 8), (40, 12), (129, 256), (50, 64), (77, 128), (3, 200)],
+)
 def test_roll_tensor_map_producer(ap, orc, stages, rows, cols):
-    """The 2-D tensor-map producer (boxes of whole rows, zero rows past the end
-    of the matrix) gives the oracle's result bit for bit."""
+    """The tensor-map producer gives the oracle's result bit for bit: stages
+    as one 2-D box of 1 KiB lines where the line view holds them, else 1-D
+    boxes of 256 floats (zeros past the end of the input)."""
     dev = device()
     n = rows * cols
     A = synth.uniform_pm1_torch(rows * 7 + cols, n, dev)
     A_h = to_np(A).reshape(rows, cols)
     ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, stages)
-    for stage_bytes, grid in ((0, 0), (4096, 2), (16384, 3)):
+    for stage_bytes, grid in ((0, 0), (4096, 2), (16384, 3), (1024, 4)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         for shift in (1, 0, -1, rows // 2 + 1, 3 * rows - 2):
             out = Guarded(n, 0, dev)
             ap.ap_row_roll(A, out.view, rows, cols, shift)
             assert ap.ap_check() == ap.AP_OK
-            assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4, "tensor-map producer did not run"
+            off = (shift % rows) * cols
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 12 == tensor_flags(ap, n, off), "tensor-map producer"
             assert_bits(to_np(out.view), orc.row_roll(A_h, shift), f"tensor roll {rows}x{cols} shift={shift} S={stages}")
             assert out.intact()
+
+
+@pytest.mark.parametrize("rows,cols,shift,tensor", [(1000, 3, 4, True), (1000, 3, 1, False), (999, 4, 5, True),
+                                                    (250, 2, 2, True), (250, 2, 3, False), (10, 300, 3, True)])
+def test_roll_tensor_map_rules(ap, orc, rows, cols, shift, tensor):
+    """Rows of any length take the tensor-map producer when every span starts
+    on a 16-byte boundary, else the 1-D bulk producer."""
+    dev = device()
+    n = rows * cols
+    A = synth.uniform_pm1_torch(rows + 3 * cols, n, dev)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 1024)
+    out = Guarded(n, 0, dev)
+    ap.ap_row_roll(A, out.view, rows, cols, shift)
+    assert ap.ap_check() == ap.AP_OK
+    want = tensor_flags(ap, n, (shift % rows) * cols) if tensor else 0
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 12 == want
+    assert_bits(to_np(out.view), orc.row_roll(to_np(A).reshape(rows, cols), shift), f"{rows}x{cols} shift {shift}")
+    assert out.intact()
 
 
 def test_roll_tensor_map_falls_back_when_misaligned(ap, orc):
@@ -151,15 +175,17 @@ def test_roll_tensor_map_falls_back_when_misaligned(ap, orc):
     assert_bits(to_np(out.view), orc.row_roll(to_np(src.view).reshape(rows, cols), 1), "fallback")
 
 
-def test_roll_tensor_map_full_size(ap, orc):
+@pytest.mark.parametrize("rows,cols,shift", [(1 << 26, 4, 1), (1 << 22, 64, 1), (1 << 26, 4, -12345)])
+def test_roll_tensor_map_full_size(ap, orc, rows, cols, shift):
+    """1 GiB through the tensor maps: whole stages as 2-D boxes of the line
+    view, the stage that wraps as 1-D boxes."""
     import torch
 
     dev = device()
-    rows, cols = 1 << 26, 4
     A = synth.uniform_pm1_torch(synth.SEED_ROLL, rows * cols, dev)
     B = torch.empty_like(A)
     ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
-    ap.ap_row_roll(A, B, rows, cols, 1)
+    ap.ap_row_roll(A, B, rows, cols, shift)
     assert ap.ap_check() == ap.AP_OK
-    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4
-    assert_bits(to_np(B), orc.row_roll(to_np(A).reshape(rows, cols), 1), "full-size tensor roll")
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 12 == 12
+    assert_bits(to_np(B), orc.row_roll(to_np(A).reshape(rows, cols), shift), f"full-size tensor roll {rows}x{cols}")

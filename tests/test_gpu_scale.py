@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, tensor_flags, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +56,53 @@ def test_scale_misaligned(ap, orc, in_shift, out_shift):
         assert_bits(to_np(out.view), want, f"misaligned in+{in_shift} out+{out_shift}")
         assert out.intact()
         assert src.intact()
+
+
+@pytest.mark.parametrize("stages", [2, 3, 6])
+@pytest.mark.parametrize("n", [1, 3, 4, 255, 256, 257, 1000, 4099, 65536 + 5, 300001])
+def test_scale_tensor_map_producer(ap, orc, stages, n):
+    """The tensor-map producer (whole stages as 2-D boxes of 1 KiB lines, the
+    ragged end as 1-D boxes of 256 floats with zeros past it) carries the
+    scale stream bit for bit."""
+    dev = device()
+    x = synth.uniform_pm1_torch(n + 31, n, dev)
+    want = orc.scale(to_np(x), -3.0)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    for stage_bytes, grid in ((0, 0), (1024, 2), (8192, 5)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_scale(x, out.view, n, 1, -3.0, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 12 == tensor_flags(ap, n, 0), "tensor map did not run"
+        assert_bits(to_np(out.view), want, f"tensor scale n={n} S={stages} stage={stage_bytes}")
+        assert out.intact()
+    # in place, and a misaligned output (the bulk producer takes over)
+    y = x.clone()
+    ap.ap_scale(y, y, n, 1, -3.0, stages)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), want, "tensor scale in place")
+    out = Guarded(n, 1, dev)
+    ap.ap_scale(x, out.view, n, 1, -3.0, stages)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4 == 0
+    assert_bits(to_np(out.view), want, "misaligned output falls back")
+    assert out.intact()
+
+
+def test_scale_tensor_map_full_size(ap, orc):
+    """2**20 tiles x 256 floats through the tensor maps, 2 stages."""
+    import torch
+
+    dev = device()
+    n = 1 << 28
+    x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
+    y = torch.empty_like(x)
+    ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
+    ap.ap_scale(x, y, n >> 8, 256, 2.0, 2)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 12 == 12
+    assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "full-size tensor scale")
 
 
 def test_scale_in_place(ap, orc):
