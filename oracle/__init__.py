@@ -51,6 +51,8 @@ class Oracle:
         lib.orc_cluster_exchange_ex.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                                 ctypes.c_int64]
         lib.orc_cluster_exchange_ex.restype = ctypes.c_int
+        lib.orc_cluster_all_to_all.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64]
+        lib.orc_cluster_all_to_all.restype = ctypes.c_int
         lib.orc_masked_copy.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_void_p]
         lib.orc_masked_copy.restype = ctypes.c_int
         self._lib = lib
@@ -101,6 +103,14 @@ class Oracle:
             raise ValueError("orc_cluster_exchange_ex rejected the sizes")
         return y
 
+
+    def cluster_all_to_all(self, x, cluster_size: int, chunk_bytes: int) -> np.ndarray:
+        x = _f32(x).ravel()
+        y = np.empty_like(x)
+        rc = self._lib.orc_cluster_all_to_all(_ptr(x), _ptr(y), x.size, int(cluster_size), int(chunk_bytes))
+        if rc != 0:
+            raise ValueError("orc_cluster_all_to_all rejected the sizes")
+        return y
 
     def masked_copy(self, x, out_before, codes) -> np.ndarray:
         """out = out_before with chunk k replaced per codes[k] (int8, one per 16 bytes)."""

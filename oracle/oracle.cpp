@@ -132,6 +132,38 @@ int orc_cluster_exchange_ex(const float* in, float* out, int64_t n, int cluster_
     return 0;
 }
 
+// All-to-all inside each group of cluster_size consecutive chunks. Chunk c of
+// a group (the CTA of rank c) holds cluster_size equal sub-blocks; sub-block j
+// goes to the CTA of rank j, which stores it as sub-block c of its own output
+// chunk. With E = chunk_bytes / 4 floats per chunk and B = E / cluster_size
+// per sub-block:
+//   out[(g*cs + d)*E + r*B + k] = in[(g*cs + r)*E + d*B + k]
+// for every group g, receiver d, sender r and 0 <= k < B, i.e. each group is a
+// cs x cs matrix of sub-blocks and the result is its block transpose.
+// "Asynchronous Copies" (TVM TIRx guide), section Copies between CTAs: a CTA
+// bulk-copies shared memory into another CTA of its cluster and the receiver
+// waits on its own transaction barrier for the bytes it expects; here every
+// CTA sends to every CTA and each receiver expects the bytes of all senders.
+// Returns 0, or -1 for sizes that are not whole groups of whole sub-blocks.
+int orc_cluster_all_to_all(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes) {
+    if (cluster_size < 1 || chunk_bytes < 4 || chunk_bytes % 4 != 0 || n < 0) return -1;
+    const int64_t E = chunk_bytes / 4;
+    const int64_t cs = cluster_size;
+    if (E % cs != 0 || n % (E * cs) != 0) return -1;
+    const int64_t B = E / cs;
+    const int64_t groups = n / (E * cs);
+    for (int64_t g = 0; g < groups; ++g) {
+        for (int64_t d = 0; d < cs; ++d) {
+            for (int64_t r = 0; r < cs; ++r) {
+                const float* src = in + (g * cs + r) * E + d * B;
+                float* dst = out + (g * cs + d) * E + r * B;
+                for (int64_t k = 0; k < B; ++k) dst[k] = src[k];
+            }
+        }
+    }
+    return 0;
+}
+
 // Masked / zero-filling chunk copy over 16-byte chunks. For chunk k with
 // code c = codes[k]:
 //   c in 0..16  copy the first c bytes of in chunk k, write zeros to the rest

@@ -331,6 +331,54 @@ def pin_exchange_ex_invariants(orc):
         raise AssertionError("a partial chunk was accepted")
 
 
+def pin_all_to_all_worked_examples(orc):
+    with open(os.path.join(GOLDEN, "all_to_all_small.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, tail = line.split(":")
+            n, cs, cb = (int(t) for t in head.split())
+            want = [float(t) for t in tail.split()]
+            got = orc.cluster_all_to_all(np.arange(n, dtype=np.float32), cs, cb)
+            assert got.tolist() == want, f"n={n} cs={cs} chunk={cb}: {got.tolist()} != {want}"
+
+
+def pin_all_to_all_library(orc):
+    """Against numpy: each group viewed as a (cs, cs, B) array of sub-blocks,
+    the first two axes swapped."""
+    for cs in (1, 2, 3, 4, 5, 8, 16):
+        for B in (1, 3, 4):
+            for groups in (1, 2, 5):
+                E = cs * B
+                n = groups * cs * E
+                x = synth.uniform_pm1_np(9000 + n + cs, n)
+                want = x.reshape(groups, cs, cs, B).transpose(0, 2, 1, 3).reshape(-1)
+                assert_bits_equal(orc.cluster_all_to_all(x, cs, 4 * E), want, f"cs={cs} B={B} groups={groups}")
+
+
+def pin_all_to_all_invariants(orc):
+    x = synth.uniform_pm1_np(4343, 6 * 4 * 8)  # 6 groups of cs 4 with 8-float chunks, or 3 groups of cs 8
+    for cs, E in ((1, 8), (2, 8), (4, 8), (8, 8), (4, 4)):
+        once = orc.cluster_all_to_all(x, cs, 4 * E)
+        assert_bits_equal(orc.cluster_all_to_all(once, cs, 4 * E), x, f"cs={cs}: a block transpose twice is the identity")
+        if cs == 1:
+            assert_bits_equal(once, x, "cs 1 is the identity")
+        # each output sub-block is some input sub-block of the same group
+        B = E // cs
+        blocks = lambda a: sorted(map(tuple, a.reshape(-1, B).tolist()))
+        assert blocks(once) == blocks(x), f"cs={cs}: not a permutation of sub-blocks"
+        # with B == E / cs and cs == E (one float per sub-block) it is the matrix transpose
+        if B == 1:
+            assert_bits_equal(once, x.reshape(-1, cs, cs).transpose(0, 2, 1).reshape(-1), f"cs={cs} matrix transpose")
+    for bad in ((x, 3, 32), (x[:-8], 4, 32), (x, 4, 6)):
+        try:
+            orc.cluster_all_to_all(*bad)
+        except ValueError:
+            continue
+        raise AssertionError(f"partial sub-block or group accepted: n={bad[0].size} cs={bad[1]} chunk={bad[2]}")
+
+
 def pin_masked_copy_worked_example(orc):
     with open(os.path.join(GOLDEN, "masked_copy_small.txt")) as f:
         lines = [l.strip() for l in f if l.strip() and not l.startswith("#")]
@@ -390,6 +438,9 @@ ALL_PINS = [
     pin_exchange_ex_worked_examples,
     pin_exchange_ex_library,
     pin_exchange_ex_invariants,
+    pin_all_to_all_worked_examples,
+    pin_all_to_all_library,
+    pin_all_to_all_invariants,
     pin_masked_copy_worked_example,
     pin_masked_copy_bytes,
     pin_masked_copy_special_codes,

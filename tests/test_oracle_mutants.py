@@ -36,6 +36,11 @@ MUTANTS = {
     "masked_no_zero_fill": ("dst[16 * k + b] = b < keep ? src[16 * k + b] : 0;", "if (b < keep) dst[16 * k + b] = src[16 * k + b];"),
     "masked_ignore_copies": ("const int keep = c < 0 ? 0 : c;", "const int keep = c < 0 ? 16 : c;"),
     "exchange_ex_ignores_shift": ("const int64_t src = first + (r + s) % m;", "const int64_t src = first + (r + 1) % m;"),
+    "a2a_no_transpose": ("const float* src = in + (g * cs + r) * E + d * B;",
+                         "const float* src = in + (g * cs + d) * E + r * B;"),
+    "a2a_wrong_sub_block": ("float* dst = out + (g * cs + d) * E + r * B;", "float* dst = out + (g * cs + d) * E + d * B;"),
+    "a2a_drops_group": ("const float* src = in + (g * cs + r) * E + d * B;", "const float* src = in + r * E + d * B;"),
+    "a2a_accepts_partial_block": ("if (E % cs != 0 || n % (E * cs) != 0) return -1;", "if (n % (E * cs) != 0) return -1;"),
 }
 
 
