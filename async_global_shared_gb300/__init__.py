@@ -18,6 +18,7 @@ __all__ = [
     "ap_poly",
     "ap_cluster_exchange",
     "ap_cluster_exchange_ex",
+    "ap_cluster_all_to_all",
     "ap_masked_copy",
     "ap_autotune",
     "ap_autotune_reset",

@@ -67,6 +67,7 @@ EXPORTED = (
     "ap_poly",
     "ap_cluster_exchange",
     "ap_cluster_exchange_ex",
+    "ap_cluster_all_to_all",
     "ap_masked_copy",
     "ap_autotune",
     "ap_autotune_reset",
@@ -120,6 +121,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_poly.argtypes = [vp, vp, _i64, vp, ctypes.c_int, ctypes.c_int, vp]
     lib.ap_cluster_exchange.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, vp]
     lib.ap_cluster_exchange_ex.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, _i64, vp]
+    lib.ap_cluster_all_to_all.argtypes = [vp, vp, _i64, ctypes.c_int, _i64, vp]
     lib.ap_masked_copy.argtypes = [vp, vp, _i64, vp, ctypes.c_int, vp]
     lib.ap_autotune.argtypes = [ctypes.c_int, vp, vp, _i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(RingShape), vp]
     lib.ap_autotune_reset.argtypes = []
@@ -134,7 +136,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_scale_pages_async.argtypes = [vp, vp, _i64, _i64, ctypes.c_float, vp]
     lib.ap_debug_emulate_ring_tensor.argtypes = [vp, vp, _i64, _i64, _i64, _i64, _i64]
     for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange",
-                 "ap_cluster_exchange_ex", "ap_masked_copy", "ap_autotune", "ap_autotune_reset", "ap_check",
+                 "ap_cluster_exchange_ex", "ap_cluster_all_to_all", "ap_masked_copy", "ap_autotune", "ap_autotune_reset", "ap_check",
                  "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_emulate_ring_tensor", "ap_debug_fma_probe",
                  "ap_debug_scale_pages_async"):
         getattr(lib, name).restype = ctypes.c_int
@@ -212,6 +214,11 @@ def ap_cluster_exchange(inp, out, n: int, cluster_size: int, chunk_bytes: int, s
 def ap_cluster_exchange_ex(inp, out, n: int, cluster_size: int, chunk_bytes: int, shift: int, stream=None):
     _check(load().ap_cluster_exchange_ex(_addr(inp), _addr(out), n, cluster_size, chunk_bytes, shift,
                                          _stream(stream)), "ap_cluster_exchange_ex")
+
+
+def ap_cluster_all_to_all(inp, out, n: int, cluster_size: int, chunk_bytes: int, stream=None):
+    _check(load().ap_cluster_all_to_all(_addr(inp), _addr(out), n, cluster_size, chunk_bytes, _stream(stream)),
+           "ap_cluster_all_to_all")
 
 
 def ap_masked_copy(inp, out, n_chunks: int, codes, stages: int, stream=None):

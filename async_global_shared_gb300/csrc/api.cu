@@ -250,7 +250,24 @@ ap_status ap_cluster_exchange(const float* in, float* out, int64_t n, int cluste
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     const int64_t groups = (4 * n) / (static_cast<int64_t>(cluster_size) * chunk_bytes);
-    return launch_exchange(di, options(), in, out, groups, cluster_size, chunk_bytes, 1, stream);
+    return launch_exchange(di, options(), in, out, groups, cluster_size, chunk_bytes, 1, false, stream);
+}
+
+ap_status ap_cluster_all_to_all(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes,
+                                cudaStream_t stream) {
+    if (cluster_size < 1 || cluster_size > AP_MAX_CLUSTER_NONPORTABLE) return AP_ERR_CLUSTER;
+    if (chunk_bytes < 16 * cluster_size || chunk_bytes % (16 * cluster_size) != 0) return AP_ERR_SHAPE;
+    if (n < 0 || n > kMaxElems) return AP_ERR_SHAPE;
+    if ((4 * n) % (static_cast<int64_t>(cluster_size) * chunk_bytes) != 0) return AP_ERR_SHAPE;
+    if (n == 0) return AP_OK;
+    if (in == nullptr || out == nullptr) return AP_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return AP_ERR_ALIGN;
+    if (overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    const int64_t groups = (4 * n) / (static_cast<int64_t>(cluster_size) * chunk_bytes);
+    return launch_exchange(di, options(), in, out, groups, cluster_size, chunk_bytes, 0, true, stream);
 }
 
 ap_status ap_cluster_exchange_ex(const float* in, float* out, int64_t n, int cluster_size, int64_t chunk_bytes,
@@ -272,13 +289,13 @@ ap_status ap_cluster_exchange_ex(const float* in, float* out, int64_t n, int clu
     const int64_t groups = chunks / cluster_size;
     const int64_t m = chunks % cluster_size;  // chunks of the short last group
     if (groups > 0) {
-        const ap_status s1 = launch_exchange(di, o, in, out, groups, cluster_size, chunk_bytes, shift, stream);
+        const ap_status s1 = launch_exchange(di, o, in, out, groups, cluster_size, chunk_bytes, shift, false, stream);
         if (s1 != AP_OK) return s1;
     }
     if (m > 0) {
         // The short last group runs as one cluster of m CTAs.
         const int64_t off = groups * cluster_size * (chunk_bytes / 4);
-        return launch_exchange(di, o, in + off, out + off, 1, static_cast<int>(m), chunk_bytes, shift, stream);
+        return launch_exchange(di, o, in + off, out + off, 1, static_cast<int>(m), chunk_bytes, shift, false, stream);
     }
     return AP_OK;
 }

@@ -18,15 +18,26 @@
 //            the group from global memory into send[s] (bulk copy, load_full[s]).
 //   pusher   (warp 1): waits load_full[s], pushes send[s] into recv[s] of
 //            rank (r-1) mod cs, completing on that CTA's recv_full[s].
-//   receiver (8 warps): registers the piece's bytes on its recv_full[s], waits,
-//            stores recv[s] to its output chunk with 16-byte stores, then
-//            each warp arrives (remote) on credit[s] of rank (r+1) mod cs,
-//            the CTA that sends to it. In the TMA-store form one thread
-//            instead hands recv[s] to a shared->global bulk copy and credits
-//            the slot once that copy has read it.
+//   receiver (8 warps, one item each in turn): waits on recv_full[s],
+//            stores recv[s] to its output chunk with 16-byte stores, arms
+//            recv_full[s] with the bytes of the slot's next item, then
+//            arrives (remote) on credit[s] of rank (r+1) mod cs, the CTA
+//            that sends to it. In the TMA-store form one thread instead
+//            hands recv[s] to a shared->global bulk copy and credits the
+//            slot once that copy has read it.
+// Before the final cluster barrier each pusher waits (bounded) for the
+// credits of its last S pieces, so no copy is in flight when a CTA leaves.
 // credit[s] therefore tells a sender both that its send[s] has been read
 // (the data reached the receiver) and that the receiver's recv[s] is free,
 // so the loader may refill send[s] and the pusher may overwrite recv[s].
+//
+// All-to-all form (a2a): each chunk is cs sub-blocks; sub-block j of rank r's
+// chunk goes to rank j as sub-block r of its output chunk. The senders go
+// round-robin: item i of every CTA goes to rank (r + i) mod cs, so each
+// receiver takes exactly one piece per item, from rank (d - i) mod cs. With
+// S a multiple of cs, items i and i + S of a sender go to the same receiver
+// and slot, so every (receiver, slot) pair has one fixed sender and the
+// credit protocol above holds unchanged, with the peer chosen per item.
 #include <algorithm>
 #include <atomic>
 
@@ -50,11 +61,45 @@ struct ExParams {
     int pieces;            // chunk_bytes / piece_bytes
     int cs;                // cluster size
     int shift;             // rank r receives from rank (r + shift) mod cs, 0 <= shift < cs
-    int stages;            // ring slots per direction
+    int stages;            // ring slots per direction (a multiple of cs in the all-to-all form)
     int tma_store;         // receiver stores with bulk copies (1) or with 8 warps (0)
+    int a2a;               // 1: all-to-all (shift unused, pieces = cs x sub_pieces)
+    int sub_pieces;        // all-to-all: pieces per sub-block (chunk_bytes / cs / piece_bytes)
     uint32_t tx_extra;
     uint64_t timeout_ns;
     uint32_t* status;
+};
+
+// A CTA's items in order, without divisions (a 64-bit division per item in
+// the single-thread roles would cost them more than moving a piece): item i
+// uses ring slot s = i mod S in phase ph = (i / S) mod 2, and is piece
+// il = i mod NP of group grp = cid + (i / NP) * ncl; in the all-to-all form
+// q = il mod cs picks the peer and t = il / cs the piece of the sub-block.
+struct ItemCursor {
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t round = 0;  // i / S: how many items used slot s before this one
+    int64_t grp;
+    int64_t il = 0;
+    int q = 0;
+    int64_t t = 0;
+    __device__ explicit ItemCursor(int64_t cid) : grp(cid) {}
+    __device__ void next(int S, int64_t NP, int cs, int64_t ncl) {
+        if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+            ++round;
+        }
+        if (++il == NP) {
+            il = 0;
+            q = 0;
+            t = 0;
+            grp += ncl;
+        } else if (++q == cs) {
+            q = 0;
+            ++t;
+        }
+    }
 };
 
 __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_constant__ ExParams P) {
@@ -66,6 +111,8 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
     unsigned char* recv = smem + static_cast<size_t>(S) * CB;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * static_cast<size_t>(S) * CB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * S);
+    // taken[s]: items of slot s the receivers have finished with (warp-store form)
+    volatile uint32_t* taken = reinterpret_cast<volatile uint32_t*>(bars + 3 * S) + 4;
     const uint32_t bar_base = ptx::smem_addr(bars);
     auto load_full = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(s); };
     auto credit = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(S + s); };
@@ -84,16 +131,36 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
         const int64_t grp = cid + (i / NP) * ncl;
         return (grp * P.cs + rank) * static_cast<int64_t>(P.chunk_bytes) + (i % NP) * static_cast<int64_t>(CB);
     };
+    // Byte offset of the piece of item c (a cursor) in this CTA's chunk: piece
+    // il; in the all-to-all form piece t of sub-block blk, where blk is the
+    // receiver (rank + q) mod cs for the piece this CTA sends, and the sender
+    // (rank - q) mod cs for the piece it receives (that sender wrote its
+    // sub-block `rank`, which lands as sub-block `sender` here).
+    const int64_t sub_bytes = static_cast<int64_t>(CB) * P.sub_pieces;
+    auto item_off = [&](const ItemCursor& c, uint32_t blk) -> int64_t {
+        const int64_t base = (c.grp * P.cs + rank) * static_cast<int64_t>(P.chunk_bytes);
+        if (!P.a2a) return base + c.il * static_cast<int64_t>(CB);
+        return base + blk * sub_bytes + c.t * static_cast<int64_t>(CB);
+    };
+    auto a2a_dst = [&](const ItemCursor& c) {
+        const uint32_t d = rank + static_cast<uint32_t>(c.q);
+        return d >= cs ? d - cs : d;
+    };
+    auto a2a_src = [&](const ItemCursor& c) {
+        const uint32_t q = static_cast<uint32_t>(c.q);
+        return rank >= q ? rank - q : rank + cs - q;
+    };
     const unsigned char* in_bytes = reinterpret_cast<const unsigned char*>(P.in);
     unsigned char* out_bytes = reinterpret_cast<unsigned char*>(P.out);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(load_full(s), 1);
-            ptx::mbar_init(credit(s), P.tma_store ? 1 : kExConsumerWarps);
+            ptx::mbar_init(credit(s), 1);  // one arrival per item: the warp (or thread) that stored it
             ptx::mbar_init(recv_full(s), 1);
         }
         *abort_flag = 0;
+        for (int s = 0; s < S; ++s) taken[s] = 0;
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -105,17 +172,17 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
     if (warp == 0) {
         if (lane == 0) {
             int64_t i = 0;
-            for (; i < count; ++i) {
-                const int s = static_cast<int>(i % S);
-                const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-                const int w = wait_phase<true>(credit(s), ph ^ 1u, P.timeout_ns, abort_flag);
+            ItemCursor c(cid);
+            for (; i < count; ++i, c.next(S, NP, P.cs, ncl)) {
+                const int s = c.s;
+                const int w = wait_phase<true>(credit(s), c.ph ^ 1u, P.timeout_ns, abort_flag);
                 if (w != WAIT_OK) {
                     if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_LOADER_CREDIT, abort_flag);
                     break;
                 }
                 ptx::mbar_arrive_expect_tx(load_full(s), CB + P.tx_extra);
-                ptx::bulk_g2s(ptx::smem_addr(send + static_cast<size_t>(s) * CB), in_bytes + piece_off(i), CB,
-                              load_full(s));
+                ptx::bulk_g2s(ptx::smem_addr(send + static_cast<size_t>(s) * CB), in_bytes + item_off(c, a2a_dst(c)),
+                              CB, load_full(s));
             }
             for (int64_t k = i > S ? i - S : 0; k < i; ++k) {
                 if (wait_phase<false>(load_full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1),
@@ -125,12 +192,17 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t peer_recv = ptx::mapa(ptx::smem_addr(recv), dst_rank);
-            const uint32_t peer_bars = ptx::mapa(bar_base, dst_rank);
-            for (int64_t i = 0; i < count; ++i) {
-                const int s = static_cast<int>(i % S);
-                const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-                const int w = wait_phase<false>(load_full(s), ph, P.timeout_ns, abort_flag);
+            uint32_t peer_recv = ptx::mapa(ptx::smem_addr(recv), dst_rank);
+            uint32_t peer_bars = ptx::mapa(bar_base, dst_rank);
+            ItemCursor c(cid);
+            int64_t i = 0;
+            for (; i < count; ++i, c.next(S, NP, P.cs, ncl)) {
+                if (P.a2a) {
+                    peer_recv = ptx::mapa(ptx::smem_addr(recv), a2a_dst(c));
+                    peer_bars = ptx::mapa(bar_base, a2a_dst(c));
+                }
+                const int s = c.s;
+                const int w = wait_phase<false>(load_full(s), c.ph, P.timeout_ns, abort_flag);
                 if (w != WAIT_OK) {
                     if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_PUSHER_LOADED, abort_flag);
                     break;
@@ -138,6 +210,17 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                 ptx::bulk_s2s_cluster(peer_recv + static_cast<uint32_t>(s) * CB,
                                       ptx::smem_addr(send + static_cast<size_t>(s) * CB), CB,
                                       peer_bars + 8u * static_cast<uint32_t>(2 * S + s));
+            }
+            // Before the final cluster barrier: every piece pushed has been
+            // taken by its receiver (its credit, bounded), so no push is still
+            // reading this CTA's shared memory or landing in a peer's when a
+            // CTA of the cluster leaves. Item k's credit completes phase k / S.
+            for (int64_t k = i > S ? i - S : 0; k < i; ++k) {
+                if (wait_phase<true>(credit(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1), P.timeout_ns,
+                                     nullptr) != WAIT_OK) {
+                    raise_timeout(P.status, SITE_EX_DRAIN, abort_flag);
+                    break;
+                }
             }
         }
     } else if (P.tma_store) {
@@ -182,57 +265,70 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
             ptx::bulk_wait_all();
         }
     } else {
+        // Receivers, one warp per item: warp cw takes items cw, cw + 8, ...,
+        // so eight items drain at once. The slot's expected bytes for item k
+        // are registered by the warp that consumed item k - S (the first S at
+        // the start), right after that phase completed and before the sender
+        // is credited, so every phase is armed exactly once. A warp waits on
+        // item k's phase only once taken[s] shows item k - S consumed: a
+        // barrier's phase is known by its parity alone, and a warp that ran
+        // two phases ahead would take the older completed phase for its own.
         const int cw = warp - 2;
-        const int ct = threadIdx.x - 64;
-        const bool leader = (cw == 0 && lane == 0);
-        const uint32_t peer_credit = ptx::mapa(credit(0), src_rank);
-        int64_t i = 0;
-        int64_t armed = 0;  // items [0, armed) have their expected bytes registered
-        for (; i < count; ++i) {
-            const int s = static_cast<int>(i % S);
-            const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-            if (leader) {
-                ptx::mbar_arrive_expect_tx(recv_full(s), CB);
-                armed = i + 1;
-            }
+        if (cw == 0 && lane == 0) {
+            for (int64_t k = 0; k < count && k < S; ++k) ptx::mbar_arrive_expect_tx(recv_full(static_cast<int>(k)), CB);
+        }
+        uint32_t peer_credit = ptx::mapa(credit(0), src_rank);
+        ItemCursor c(cid);
+        for (int k = 0; k < cw; ++k) c.next(S, NP, P.cs, ncl);
+        for (int64_t i = cw; i < count; i += kExConsumerWarps) {
+            const int s = c.s;
             int w = WAIT_OK;
             if (lane == 0) {
-                w = wait_phase<true>(recv_full(s), ph, P.timeout_ns, abort_flag);
+                if (taken[s] < c.round) {  // bounded wait for item k - S to be consumed
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (taken[s] < c.round) {
+                        if (*abort_flag) {
+                            w = WAIT_ABORTED;
+                            break;
+                        }
+                        if (ptx::globaltimer_ns() - t0 > P.timeout_ns) {
+                            w = WAIT_TIMEOUT;
+                            break;
+                        }
+                    }
+                }
+                if (w == WAIT_OK) w = wait_phase<true>(recv_full(s), c.ph, P.timeout_ns, abort_flag);
                 if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_RECEIVER_FULL, abort_flag);
             }
             w = __shfl_sync(0xffffffffu, w, 0);
             if (w != WAIT_OK) break;
             __syncwarp();
             const float4* src = reinterpret_cast<const float4*>(recv + static_cast<size_t>(s) * CB);
-            float4* dst = reinterpret_cast<float4*>(out_bytes + piece_off(i));
+            float4* dst = reinterpret_cast<float4*>(out_bytes + item_off(c, a2a_src(c)));
+            if (P.a2a) peer_credit = ptx::mapa(credit(0), a2a_src(c));
             const int64_t nq = CB / 16;
-            int64_t q = ct;
-            for (; q + 3 * kExConsumers < nq; q += 4 * kExConsumers) {
+            int64_t q = lane;
+            for (; q + 96 < nq; q += 128) {
                 const float4 a = src[q];
-                const float4 b = src[q + kExConsumers];
-                const float4 c = src[q + 2 * kExConsumers];
-                const float4 d = src[q + 3 * kExConsumers];
+                const float4 b = src[q + 32];
+                const float4 e = src[q + 64];
+                const float4 f = src[q + 96];
                 dst[q] = a;
-                dst[q + kExConsumers] = b;
-                dst[q + 2 * kExConsumers] = c;
-                dst[q + 3 * kExConsumers] = d;
+                dst[q + 32] = b;
+                dst[q + 64] = e;
+                dst[q + 96] = f;
             }
-            for (; q < nq; q += kExConsumers) dst[q] = src[q];
+            for (; q < nq; q += 32) dst[q] = src[q];
             __syncwarp();
             // The slot's values are in registers (the stores used them), so a
             // relaxed arrive suffices: it does not wait for the global stores.
-            if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>(s));
-        }
-        if (leader && i < count) {
-            // Gave up early: chunks a peer already sent may still be landing in
-            // recv[]. Wait for them (bounded) before the final cluster barrier.
-            for (int64_t k = i; k < count && k < i + S; ++k) {
-                const int s = static_cast<int>(k % S);
-                if (k >= armed) ptx::mbar_arrive_expect_tx(recv_full(s), CB);
-                if (wait_phase<true>(recv_full(s), static_cast<uint32_t>((k / S) & 1), P.timeout_ns, nullptr) !=
-                    WAIT_OK)
-                    raise_timeout(P.status, SITE_EX_DRAIN, abort_flag);
+            if (lane == 0) {
+                if (i + S < count) ptx::mbar_arrive_expect_tx(recv_full(s), CB);
+                __threadfence_block();
+                taken[s] = c.round + 1;
+                ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>(s));
             }
+            for (int k = 0; k < kExConsumerWarps; ++k) c.next(S, NP, P.cs, ncl);
         }
     }
     __syncwarp();
@@ -242,7 +338,7 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
 }  // namespace
 
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t groups, int cs,
-                          int64_t chunk_bytes, int64_t shift, cudaStream_t stream) {
+                          int64_t chunk_bytes, int64_t shift, bool a2a, cudaStream_t stream) {
     // Piece: the largest multiple of 16 dividing chunk_bytes that is at most
     // the target (8 KiB, or the stage-bytes setting), and two CTAs per SM.
     // Measured on GB300 with 32 KiB chunks: the loader and pusher are single
@@ -250,23 +346,54 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     // them, and a second CTA per SM doubles those threads; whole 32 KiB chunks
     // leave too few slots in flight.
     const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 8192;
-    const int64_t units = chunk_bytes / 16;
-    int64_t piece_units = 1;
-    for (int64_t d = 1; d * d <= units; ++d) {
-        if (units % d) continue;
-        const int64_t a = d, b = units / d;
-        if (16 * a <= target && a > piece_units) piece_units = a;
-        if (16 * b <= target && b > piece_units) piece_units = b;
-    }
-    const int64_t piece = 16 * piece_units;
     // Shared memory per CTA when `cps` CTAs share an SM (228 KiB per SM, 1 KiB
     // reserved per CTA): more resident CTAs let clusters of 8 fill more SMs.
     const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
     const int64_t budget = std::min<int64_t>(di.smem_optin, kSmemPerSM / cps - 1024) - 512;
-    int64_t S = budget / (2 * piece);
-    if (S < 1) return AP_ERR_SMEM;
-    if (S > kExMaxSlots) S = kExMaxSlots;
-    const int64_t smem = 2 * S * piece + 3 * 8 * S + 16;
+    // A piece divides the chunk (all-to-all: the sub-block of chunk_bytes / cs).
+    const int64_t span = a2a ? chunk_bytes / cs : chunk_bytes;
+    const int64_t units = span / 16;
+    int64_t piece = 0, S = 0;
+    if (!a2a) {
+        int64_t piece_units = 1;
+        for (int64_t d = 1; d * d <= units; ++d) {
+            if (units % d) continue;
+            const int64_t a = d, b = units / d;
+            if (16 * a <= target && a > piece_units) piece_units = a;
+            if (16 * b <= target && b > piece_units) piece_units = b;
+        }
+        piece = 16 * piece_units;
+        S = std::min<int64_t>(budget / (2 * piece), kExMaxSlots);
+        if (S < 1) return AP_ERR_SMEM;
+    } else {
+        // All-to-all: S a multiple of cs and at least 2. Measured on GB300
+        // (2^28 floats, 32 KiB chunks): pieces under 4 KiB cost the
+        // single-thread loader and pusher more per byte than the ring hides,
+        // and at equal bytes in flight more slots win (the receiver warps
+        // take one item each). So: pieces that divide the sub-block and stay
+        // within the target, at least 4 KiB where the sub-block allows; the
+        // most bytes in flight (S x piece); on a tie the smaller piece.
+        int64_t largest = 0;
+        for (int64_t d = 1; d <= units; ++d)
+            if (units % d == 0 && 16 * d <= target) largest = 16 * d;
+        // (If no such piece leaves a ring of cs slots, any smaller piece.)
+        for (const int64_t floor_piece : {std::min<int64_t>(4096, largest), int64_t(16)}) {
+            for (int64_t d = 1; d <= units; ++d) {
+                if (units % d || 16 * d > target || 16 * d < floor_piece) continue;
+                const int64_t p = 16 * d;
+                int64_t slots = std::min<int64_t>(budget / (2 * p), kExMaxSlots);
+                slots -= slots % cs;
+                if (slots < 2) continue;
+                if (slots * p > S * piece) {
+                    piece = p;
+                    S = slots;
+                }
+            }
+            if (S > 0) break;
+        }
+        if (S == 0) return AP_ERR_SMEM;
+    }
+    const int64_t smem = 2 * S * piece + 3 * 8 * S + 16 + 4 * kExMaxSlots;  // + abort flag, taken[]
     if (smem > di.smem_optin) return AP_ERR_SMEM;
 
     static std::atomic<bool> configured[64];  // attributes set on this device (setting twice is harmless)
@@ -288,7 +415,9 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
                cs,
                static_cast<int>(((shift % cs) + cs) % cs),
                static_cast<int>(S),
-               o.ex_tma_store == 1 ? 1 : 0,
+               (o.ex_tma_store == 1 && !a2a) ? 1 : 0,
+               a2a ? 1 : 0,
+               static_cast<int>(a2a ? span / piece : 1),
                static_cast<uint32_t>(o.tx_extra),
                static_cast<uint64_t>(o.timeout_ns),
                di.status};

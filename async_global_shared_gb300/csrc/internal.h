@@ -104,9 +104,10 @@ ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, 
 ap_status launch_fma_probe(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
 
 // `groups` whole groups of cs chunks starting at in/out; rank r receives
-// rank (r + shift) mod cs.
+// rank (r + shift) mod cs, or with a2a every rank sends sub-block j of its
+// chunk (chunk_bytes / cs bytes each) to rank j (shift unused).
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t groups, int cs,
-                          int64_t chunk_bytes, int64_t shift, cudaStream_t stream);
+                          int64_t chunk_bytes, int64_t shift, bool a2a, cudaStream_t stream);
 
 // Largest chunk accepted by ap_cluster_exchange for this much shared memory.
 constexpr int64_t kSmemOptinGB300 = 232448;  // 227 KiB per CTA on compute capability 10.x

@@ -499,6 +499,9 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     for cs in (2, 4, 8):
         put(f"cluster exchange cs={cs}, 32 KiB chunks", 8 * n,
             lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768, stream))
+    for cs in (4, 16):
+        put(f"cluster all-to-all cs={cs}, 32 KiB chunks", 8 * n,
+            lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768, stream))
     codes = torch.full((n // 4,), 16, dtype=torch.int8, device=dev)
     # per 16-byte chunk: 16 read + 16 written + 1 code byte
     put("masked copy, all chunks copied", 33 * (n // 4), lambda: ap.ap_masked_copy(x, y, n // 4, codes, 4, stream))
@@ -590,7 +593,8 @@ def sweep(which: str, args):
     peak, _ = hbm_peak()
     steps, warm = max(5, min(args.steps, 50)), args.warmup
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    groups = ["scale", "poly", "roll", "exchange", "masked", "small"] if which == "all" else which.split(",")
+    groups = (["scale", "poly", "roll", "exchange", "alltoall", "masked", "small"] if which == "all"
+              else which.split(","))
 
     window = {}
 
@@ -811,6 +815,25 @@ def sweep(which: str, args):
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         del x, y
+    if "alltoall" in groups:
+        n = 1 << 28
+        x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
+        y = torch.empty_like(x)
+        for cs in (1, 2, 4, 8, 16):
+            for piece_kib, cps in ((0, 0), (2, 2), (4, 2), (8, 2), (16, 2), (4, 1), (8, 1), (16, 1)):
+                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
+                ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                try:
+                    ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
+                except ap.APError:
+                    continue
+                yield line("all-to-all 2^28 f32, 32 KiB chunks",
+                           f"cluster a2a cs={cs} piece<={piece_kib or 'auto '}KiB ctas/SM={cps or 'auto'}", 8 * n, ms,
+                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
+                           piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
+        del x, y
     if "autotune" in groups:
         n = 1 << 28
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
@@ -981,7 +1004,7 @@ def sweep(which: str, args):
 # ----------------------------------------------------------------------------- profiling cases
 
 PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
-                 "masked")
+                 "a2a4", "a2a16", "masked")
 
 
 def profile_case(name: str, args):
@@ -1006,6 +1029,8 @@ def profile_case(name: str, args):
         "roll_mis": lambda: ap.ap_row_roll(x[1:n + 1], y[:n], n // 4, 4, 1),
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
         "exchange16": lambda: ap.ap_cluster_exchange_ex(x[:n], y[:n], n, 16, 32768, 1),
+        "a2a4": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 4, 32768),
+        "a2a16": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 16, 32768),
         "roll_tensor": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "masked": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
     }

@@ -180,6 +180,34 @@ ap_status ap_cluster_exchange_ex(const float* in, float* out, int64_t n, int clu
                                  int64_t chunk_bytes, int64_t shift, cudaStream_t stream);
 
 /*
+ * ap_cluster_all_to_all: every CTA of a cluster sends a piece of its chunk to
+ * every CTA of the cluster. The input is cut into chunks of chunk_bytes and
+ * every cluster_size consecutive chunks form one group; each chunk is
+ * cluster_size equal sub-blocks of B = chunk_bytes / cluster_size bytes.
+ * CTA rank r of the group's cluster loads chunk r, bulk-copies its sub-block j
+ * into the shared memory of rank j (cp.async.bulk.shared::cluster, completed
+ * on rank j's transaction barrier, which expects the bytes of every sender),
+ * and each CTA stores what it received:
+ *     out chunk (g * cs + d), sub-block r = in chunk (g * cs + r), sub-block d,
+ * the block transpose of each group's cs x cs sub-blocks. Source: "Asynchronous
+ * Copies" (TVM TIRx guide), section Copies between CTAs (a CTA copies shared
+ * memory into another CTA of its cluster; the receiver waits on its own
+ * transaction barrier); the pages describe one sender and one receiver, and
+ * this call extends the pattern to all pairs of the cluster.
+ *  in, out       device arrays of n floats, 16-byte aligned (AP_ERR_ALIGN),
+ *                not overlapping (AP_ERR_ALIAS).
+ *  n             >= 0; n * 4 must be a multiple of cluster_size * chunk_bytes
+ *                (AP_ERR_SHAPE).
+ *  cluster_size  1..16 (AP_ERR_CLUSTER otherwise; sizes above 8 use the
+ *                non-portable cluster attribute and return AP_ERR_CLUSTER if
+ *                the device cannot place such a cluster). 1 is a plain copy.
+ *  chunk_bytes   a multiple of 16 * cluster_size (AP_ERR_SHAPE), so that every
+ *                sub-block is whole 16-byte units.
+ */
+ap_status ap_cluster_all_to_all(const float* in, float* out, int64_t n, int cluster_size,
+                                int64_t chunk_bytes, cudaStream_t stream);
+
+/*
  * ap_masked_copy: predicated / zero-filling copy of 16-byte chunks. For chunk
  * k (floats 4k .. 4k+3) with code c = codes[k]:
  *     0..16  the first c bytes of in chunk k are copied, the remaining

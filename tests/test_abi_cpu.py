@@ -116,6 +116,16 @@ def test_validation_before_cuda(ap):
     assert raw(ap, ex, FAKE_IN, FAKE_OUT, 0, 5, 32768, 7, None) == ap.AP_OK
     assert raw(ap, ex, FAKE_IN + 8, FAKE_OUT, 1 << 20, 5, 32768, 7, None) == ap.AP_ERR_ALIGN
     assert raw(ap, ex, FAKE_IN, FAKE_IN + 16, 1 << 20, 5, 32768, 7, None) == ap.AP_ERR_ALIAS
+    a2a = "ap_cluster_all_to_all"
+    assert raw(ap, a2a, FAKE_IN, FAKE_OUT, 1 << 20, 0, 32768, None) == ap.AP_ERR_CLUSTER
+    assert raw(ap, a2a, FAKE_IN, FAKE_OUT, 1 << 20, 17, 32768, None) == ap.AP_ERR_CLUSTER
+    assert raw(ap, a2a, FAKE_IN, FAKE_OUT, 1 << 20, 4, 32, None) == ap.AP_ERR_SHAPE  # sub-block of 8 bytes
+    assert raw(ap, a2a, FAKE_IN, FAKE_OUT, 1 << 20, 3, 32768, None) == ap.AP_ERR_SHAPE  # 32768 not a multiple of 48
+    assert raw(ap, a2a, FAKE_IN, FAKE_OUT, 3 * 8192, 4, 32768, None) == ap.AP_ERR_SHAPE  # 3 chunks: no whole group
+    assert raw(ap, a2a, FAKE_IN, FAKE_OUT, 0, 4, 32768, None) == ap.AP_OK
+    assert raw(ap, a2a, None, FAKE_OUT, 1 << 20, 4, 32768, None) == ap.AP_ERR_NULL
+    assert raw(ap, a2a, FAKE_IN + 8, FAKE_OUT, 1 << 20, 4, 32768, None) == ap.AP_ERR_ALIGN
+    assert raw(ap, a2a, FAKE_IN, FAKE_IN + 16, 1 << 20, 4, 32768, None) == ap.AP_ERR_ALIAS
 
 
 def test_debug_settings_roundtrip(ap):

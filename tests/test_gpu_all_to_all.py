@@ -1,0 +1,86 @@
+"""ap_cluster_all_to_all against the oracle, bit for bit: every CTA of a
+cluster sends sub-block j of its chunk to rank j (the block transpose of each
+group's sub-blocks), for cluster sizes 1..16 (above 8 with the non-portable
+cluster attribute), sub-blocks from one 16-byte unit to several pieces, and
+clusters that walk many groups through a ring reused many times."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def ap():
+    ap = lib()
+    reset_debug(ap)
+    yield ap
+    reset_debug(ap)
+
+
+@pytest.mark.parametrize("cs", [1, 2, 3, 4, 5, 8, 12, 16])
+@pytest.mark.parametrize("sub_bytes", [16, 48, 1024, 4096])
+def test_all_to_all_small(ap, orc, cs, sub_bytes):
+    dev = device()
+    chunk_bytes = cs * sub_bytes
+    for groups in (1, 3, 40):
+        n = groups * cs * chunk_bytes // 4
+        x = synth.uniform_pm1_torch(n + cs, n, dev)
+        want = orc.cluster_all_to_all(to_np(x), cs, chunk_bytes)
+        # defaults, then small pieces, few slots and one cluster (every slot
+        # goes through many phases, items of one sender spread over groups)
+        for piece, grid, cps in ((0, 0, 0), (16, cs, 0), (512, 2 * cs, 4), (2048, 0, 1)):
+            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece)
+            ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+            out = Guarded(n, 0, dev)
+            ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk_bytes)
+            assert ap.ap_check() == ap.AP_OK
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGES) % cs == 0, "ring depth must be a multiple of cs"
+            assert_bits(to_np(out.view), want, f"a2a cs={cs} sub={sub_bytes} groups={groups} piece={piece} grid={grid}")
+            assert out.intact()
+
+
+def test_all_to_all_twice_is_identity(ap):
+    import torch
+
+    dev = device()
+    n = 1 << 20
+    x = synth.uniform_pm1_torch(11, n, dev)
+    a = torch.empty_like(x)
+    b = torch.empty_like(x)
+    for cs in (2, 4, 8, 16):
+        ap.ap_cluster_all_to_all(x, a, n, cs, 16384)
+        ap.ap_cluster_all_to_all(a, b, n, cs, 16384)
+        assert ap.ap_check() == ap.AP_OK
+        assert torch.equal(b.view(torch.int32), x.view(torch.int32)), f"cs={cs}"
+
+
+def test_all_to_all_ignores_the_tma_store_setting(ap, orc):
+    import torch
+
+    dev = device()
+    n = 8 * 4 * 8192 // 4
+    x = synth.uniform_pm1_torch(12, n, dev)
+    y = torch.empty_like(x)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 1)
+    ap.ap_cluster_all_to_all(x, y, n, 4, 8192)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), 4, 8192), "a2a with the store setting at 1")
+
+
+@pytest.mark.parametrize("cs", [2, 4, 8, 16])
+def test_all_to_all_full_size(ap, orc, cs):
+    """2**28 floats in 32 KiB chunks (32768 chunks)."""
+    import torch
+
+    dev = device()
+    n = 1 << 28
+    x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
+    y = torch.full_like(x, float("nan"))
+    ap.ap_cluster_all_to_all(x, y, n, cs, 32768)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), cs, 32768), f"full all-to-all cs={cs}")

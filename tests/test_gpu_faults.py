@@ -63,6 +63,26 @@ def test_exchange_wait_times_out_and_recovers(ap, orc, store):
     assert_bits(to_np(y), orc.cluster_exchange(to_np(x), 4, 4096), "exchange after recovery")
 
 
+def test_all_to_all_wait_times_out_and_recovers(ap, orc):
+    """The all-to-all's bounded waits: no piece is ever loaded (the loader's
+    barrier expects bytes that never come), so nothing is pushed between CTAs,
+    every wait gives up, and the next call runs normally."""
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n = 4 * 4096 * 16 // 4
+    x = synth.uniform_pm1_torch(5, n, dev)
+    y = torch.empty_like(x)
+    _inject(ap)
+    ap.ap_cluster_all_to_all(x, y, n, 4, 4096)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    reset_debug(ap)
+    ap.ap_cluster_all_to_all(x, y, n, 4, 4096)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), 4, 4096), "all-to-all after recovery")
+
+
 def test_bad_arguments_raise(ap):
     import torch
 
