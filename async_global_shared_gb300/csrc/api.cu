@@ -33,6 +33,7 @@ std::atomic<int64_t> g_ex_tma_store{0};
 std::atomic<int64_t> g_cache_hints{0};
 std::atomic<int64_t> g_device_checks{0};
 std::atomic<int64_t> g_schedule{0};
+std::atomic<int64_t> g_ex_group{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0}, g_last_site{0};
@@ -121,6 +122,7 @@ Options options() {
     o.cache_hints = g_cache_hints.load();
     o.device_checks = g_device_checks.load();
     o.schedule = g_schedule.load();
+    o.ex_group = g_ex_group.load();
     return o;
 }
 
@@ -417,6 +419,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 1) return AP_ERR_ARG;
             g_schedule = value;
             return AP_OK;
+        case AP_DBG_EXCHANGE_GROUP:
+            if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return AP_ERR_ARG;
+            g_ex_group = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -436,6 +442,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_CACHE_HINTS: return o.cache_hints;
         case AP_DBG_DEVICE_CHECKS: return o.device_checks;
         case AP_DBG_SCHEDULE: return o.schedule;
+        case AP_DBG_EXCHANGE_GROUP: return o.ex_group;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

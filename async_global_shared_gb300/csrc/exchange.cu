@@ -62,8 +62,9 @@ struct ExParams {
     int cs;                // cluster size
     int shift;             // rank r receives from rank (r + shift) mod cs, 0 <= shift < cs
     int stages;            // ring slots per direction (a multiple of cs in the all-to-all form)
-    int tma_store;         // receiver stores with bulk copies (1) or with 8 warps (0)
+    int tma_store;         // receiver stores with bulk copies (1) or with the receiver warps (0)
     int a2a;               // 1: all-to-all (shift unused, pieces = cs x sub_pieces)
+    int rgroup;            // receiver warps per piece in the warp-store form: 1, 2, 4 or 8
     int sub_pieces;        // all-to-all: pieces per sub-block (chunk_bytes / cs / piece_bytes)
     uint32_t tx_extra;
     uint64_t timeout_ns;
@@ -111,8 +112,10 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
     unsigned char* recv = smem + static_cast<size_t>(S) * CB;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * static_cast<size_t>(S) * CB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * S);
-    // taken[s]: items of slot s the receivers have finished with (warp-store form)
+    // taken[s]: items of slot s the receivers have finished with; group_bad[g]:
+    // a wait of receiver group g failed (warp-store form)
     volatile uint32_t* taken = reinterpret_cast<volatile uint32_t*>(bars + 3 * S) + 4;
+    volatile uint32_t* group_bad = taken + kExMaxSlots;
     const uint32_t bar_base = ptx::smem_addr(bars);
     auto load_full = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(s); };
     auto credit = [&](int s) { return bar_base + 8u * static_cast<uint32_t>(S + s); };
@@ -126,11 +129,6 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
     const int64_t cid = ptx::cluster_id_x();
     const int64_t ncl = ptx::nclusters_x();
     const int64_t count = (cid < P.groups ? (P.groups - cid + ncl - 1) / ncl : 0) * NP;
-    // Byte offset of this CTA's piece for item i: chunk (group * cs + rank), piece i mod NP.
-    auto piece_off = [&](int64_t i) -> int64_t {
-        const int64_t grp = cid + (i / NP) * ncl;
-        return (grp * P.cs + rank) * static_cast<int64_t>(P.chunk_bytes) + (i % NP) * static_cast<int64_t>(CB);
-    };
     // Byte offset of the piece of item c (a cursor) in this CTA's chunk: piece
     // il; in the all-to-all form piece t of sub-block blk, where blk is the
     // receiver (rank + q) mod cs for the piece this CTA sends, and the sender
@@ -161,6 +159,7 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
         }
         *abort_flag = 0;
         for (int s = 0; s < S; ++s) taken[s] = 0;
+        for (int g = 0; g < kExConsumerWarps; ++g) group_bad[g] = 0;
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -228,27 +227,21 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
         // received piece to the bulk-copy engine (shared -> global); a slot is
         // credited back once the engine has finished reading it.
         if (warp == 2 && lane == 0) {
-            const uint32_t peer_credit = ptx::mapa(credit(0), src_rank);
-            const int64_t lag = S > 2 ? 2 : S - 1;  // bulk stores left reading before a slot is credited
+            const uint32_t credit0 = ptx::mapa(credit(0), src_rank);
+            const int lag = S > 2 ? 2 : S - 1;  // bulk stores left reading before a slot is credited
+            uint32_t prev1 = 0, prev2 = 0;      // peer credit addresses owed for items i - 1 and i - 2
+            ItemCursor c(cid);
             int64_t i = 0;
-            for (; i < count; ++i) {
-                const int s = static_cast<int>(i % S);
+            for (; i < count; ++i, c.next(S, NP, P.cs, ncl)) {
+                const int s = c.s;
                 ptx::mbar_arrive_expect_tx(recv_full(s), CB);
-                const int w = wait_phase<true>(recv_full(s), static_cast<uint32_t>((i / S) & 1), P.timeout_ns,
-                                               abort_flag);
+                const int w = wait_phase<true>(recv_full(s), c.ph, P.timeout_ns, abort_flag);
                 if (w != WAIT_OK) {
                     if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_RECEIVER_FULL, abort_flag);
-                    // Chunks a peer already sent may still be landing in recv[]:
-                    // wait for them (bounded) before the final cluster barrier.
-                    for (int64_t k = i; k < count && k < i + S; ++k) {
-                        if (k > i) ptx::mbar_arrive_expect_tx(recv_full(static_cast<int>(k % S)), CB);
-                        if (wait_phase<true>(recv_full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1),
-                                             P.timeout_ns, nullptr) != WAIT_OK)
-                            raise_timeout(P.status, SITE_EX_DRAIN, abort_flag);
-                    }
                     break;
                 }
-                ptx::bulk_s2g(out_bytes + piece_off(i), ptx::smem_addr(recv + static_cast<size_t>(s) * CB), CB);
+                ptx::bulk_s2g(out_bytes + item_off(c, a2a_src(c)), ptx::smem_addr(recv + static_cast<size_t>(s) * CB),
+                              CB);
                 ptx::bulk_commit();
                 if (lag == 2) {
                     ptx::bulk_wait_read<2>();
@@ -257,30 +250,50 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                 } else {
                     ptx::bulk_wait_read<0>();
                 }
-                if (i >= lag) ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>((i - lag) % S));
+                const uint32_t cur =
+                    (P.a2a ? ptx::mapa(credit(0), a2a_src(c)) : credit0) + 8u * static_cast<uint32_t>(s);
+                // credit the item whose store has now finished reading its slot
+                if (lag == 2) {
+                    if (i >= 2) ptx::mbar_arrive_remote_relaxed(prev2);
+                } else if (lag == 1) {
+                    if (i >= 1) ptx::mbar_arrive_remote_relaxed(prev1);
+                } else {
+                    ptx::mbar_arrive_remote_relaxed(cur);
+                }
+                prev2 = prev1;
+                prev1 = cur;
             }
             ptx::bulk_wait_read<0>();
-            for (int64_t k = i > lag ? i - lag : 0; k < i; ++k)
-                ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>(k % S));
+            if (lag == 2 && i >= 2) ptx::mbar_arrive_remote_relaxed(prev2);
+            if (lag >= 1 && i >= 1) ptx::mbar_arrive_remote_relaxed(prev1);
             ptx::bulk_wait_all();
         }
     } else {
-        // Receivers, one warp per item: warp cw takes items cw, cw + 8, ...,
-        // so eight items drain at once. The slot's expected bytes for item k
-        // are registered by the warp that consumed item k - S (the first S at
-        // the start), right after that phase completed and before the sender
-        // is credited, so every phase is armed exactly once. A warp waits on
-        // item k's phase only once taken[s] shows item k - S consumed: a
-        // barrier's phase is known by its parity alone, and a warp that ran
-        // two phases ahead would take the older completed phase for its own.
+        // Receivers in groups of G warps (G = 1, 2, 4 or 8), one piece per
+        // group in turn: group g takes items g, g + 8/G, ..., so 8/G pieces
+        // drain at once and each is split over 32 G threads. The slot's
+        // expected bytes for item k are registered by the group that consumed
+        // item k - S (the first S at the start), right after that phase
+        // completed and before the sender is credited, so every phase is
+        // armed exactly once. A group waits on item k's phase only once
+        // taken[s] shows item k - S consumed: a barrier's phase is known by its
+        // parity alone, and a group that ran two phases ahead would take the
+        // older completed phase for its own. The warps of a group agree on
+        // every wait's outcome at a named barrier before any of them goes on,
+        // so none is left waiting there.
+        const int G = P.rgroup;
+        const int NG = kExConsumerWarps / G;
         const int cw = warp - 2;
+        const int grp = cw / G;
+        const int gt = (cw % G) * 32 + lane;  // thread within the group
+        const bool head = (cw % G == 0) && lane == 0;
         if (cw == 0 && lane == 0) {
             for (int64_t k = 0; k < count && k < S; ++k) ptx::mbar_arrive_expect_tx(recv_full(static_cast<int>(k)), CB);
         }
         uint32_t peer_credit = ptx::mapa(credit(0), src_rank);
         ItemCursor c(cid);
-        for (int k = 0; k < cw; ++k) c.next(S, NP, P.cs, ncl);
-        for (int64_t i = cw; i < count; i += kExConsumerWarps) {
+        for (int k = 0; k < grp; ++k) c.next(S, NP, P.cs, ncl);
+        for (int64_t i = grp; i < count; i += NG) {
             const int s = c.s;
             int w = WAIT_OK;
             if (lane == 0) {
@@ -301,34 +314,44 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                 if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_RECEIVER_FULL, abort_flag);
             }
             w = __shfl_sync(0xffffffffu, w, 0);
+            if (G > 1) {
+                if (lane == 0 && w != WAIT_OK) group_bad[grp] = 1;
+                ptx::named_barrier_sync(1 + grp, 32 * G);
+                if (group_bad[grp]) w = WAIT_ABORTED;
+            }
             if (w != WAIT_OK) break;
             __syncwarp();
             const float4* src = reinterpret_cast<const float4*>(recv + static_cast<size_t>(s) * CB);
             float4* dst = reinterpret_cast<float4*>(out_bytes + item_off(c, a2a_src(c)));
             if (P.a2a) peer_credit = ptx::mapa(credit(0), a2a_src(c));
             const int64_t nq = CB / 16;
-            int64_t q = lane;
-            for (; q + 96 < nq; q += 128) {
+            const int stride = 32 * G;
+            int64_t q = gt;
+            for (; q + 3 * stride < nq; q += 4 * stride) {
                 const float4 a = src[q];
-                const float4 b = src[q + 32];
-                const float4 e = src[q + 64];
-                const float4 f = src[q + 96];
+                const float4 b = src[q + stride];
+                const float4 e = src[q + 2 * stride];
+                const float4 f = src[q + 3 * stride];
                 dst[q] = a;
-                dst[q + 32] = b;
-                dst[q + 64] = e;
-                dst[q + 96] = f;
+                dst[q + stride] = b;
+                dst[q + 2 * stride] = e;
+                dst[q + 3 * stride] = f;
             }
-            for (; q < nq; q += 32) dst[q] = src[q];
-            __syncwarp();
+            for (; q < nq; q += stride) dst[q] = src[q];
+            if (G > 1) {
+                ptx::named_barrier_sync(1 + grp, 32 * G);
+            } else {
+                __syncwarp();
+            }
             // The slot's values are in registers (the stores used them), so a
             // relaxed arrive suffices: it does not wait for the global stores.
-            if (lane == 0) {
+            if (head) {
                 if (i + S < count) ptx::mbar_arrive_expect_tx(recv_full(s), CB);
                 __threadfence_block();
                 taken[s] = c.round + 1;
                 ptx::mbar_arrive_remote_relaxed(peer_credit + 8u * static_cast<uint32_t>(s));
             }
-            for (int k = 0; k < kExConsumerWarps; ++k) c.next(S, NP, P.cs, ncl);
+            for (int k = 0; k < NG; ++k) c.next(S, NP, P.cs, ncl);
         }
     }
     __syncwarp();
@@ -393,8 +416,21 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
         }
         if (S == 0) return AP_ERR_SMEM;
     }
-    const int64_t smem = 2 * S * piece + 3 * 8 * S + 16 + 4 * kExMaxSlots;  // + abort flag, taken[]
+    const int64_t smem = 2 * S * piece + 3 * 8 * S + 16 + 4 * kExMaxSlots + 4 * kExConsumerWarps;  // + abort flag,
+                                                                                                 // taken[], group_bad[]
     if (smem > di.smem_optin) return AP_ERR_SMEM;
+
+    // Receiver form, unless set: measured on GB300 (2^28 floats, 32 KiB chunks).
+    // Fixed neighbour (one sender, pieces arrive in order): all eight warps on
+    // every piece for clusters of up to 8 (0.97-1.01 of the copy, against
+    // 0.87-0.92 with one warp per piece), one warp per piece for 16 (0.85
+    // against 0.76). All-to-all (pieces from every sender, in no fixed order,
+    // so in-order draining waits on the slowest sender): bulk stores for
+    // clusters of 1-2 (1.01-1.02), one warp per piece from 4 up (0.92-1.01;
+    // eight warps per piece: 0.53-0.56).
+    const bool tma_store = o.ex_tma_store == 1 || (o.ex_tma_store == 0 && a2a && cs <= 2);
+    const int64_t rgroup = o.ex_group > 0 ? o.ex_group : (!a2a && cs <= 8 ? kExConsumerWarps : 1);
+    if (rgroup != 1 && rgroup != 2 && rgroup != 4 && rgroup != 8) return AP_ERR_ARG;
 
     static std::atomic<bool> configured[64];  // attributes set on this device (setting twice is harmless)
     if (di.device < 0 || di.device >= 64) return AP_ERR_CUDA;
@@ -415,8 +451,9 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
                cs,
                static_cast<int>(((shift % cs) + cs) % cs),
                static_cast<int>(S),
-               (o.ex_tma_store == 1 && !a2a) ? 1 : 0,
+               tma_store ? 1 : 0,
                a2a ? 1 : 0,
+               static_cast<int>(rgroup),
                static_cast<int>(a2a ? span / piece : 1),
                static_cast<uint32_t>(o.tx_extra),
                static_cast<uint64_t>(o.timeout_ns),

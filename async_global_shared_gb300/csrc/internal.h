@@ -34,6 +34,7 @@ struct Options {
     int64_t cache_hints;
     int64_t device_checks;
     int64_t schedule;
+    int64_t ex_group;
 };
 
 Options options();

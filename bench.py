@@ -794,6 +794,23 @@ def sweep(which: str, args):
                            slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
+        # each receiver form at the default pieces and slots: bulk (TMA) stores,
+        # or 1/2/4/8 warps storing each piece together
+        for store, group in ((1, 0), (2, 1), (2, 2), (2, 4), (2, 8)):
+            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+            form = "tma" if store == 1 else f"warps x{group}"
+            for cs in (1, 2, 4, 8):
+                ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
+                yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster cs={cs} store={form} (default pieces)",
+                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
+                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+            ms = run(lambda: ap.ap_cluster_exchange_ex(x, y, n, 16, 32768, 1))
+            yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster_ex cs=16 store={form}", 8 * n, ms,
+                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, 0)
         for cps in (3, 4):
             ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
             for piece_kib in (4, 8):
@@ -819,6 +836,18 @@ def sweep(which: str, args):
         n = 1 << 28
         x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
         y = torch.empty_like(x)
+        for store, group in ((1, 0), (2, 1), (2, 2), (2, 4), (2, 8)):
+            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+            form = "tma" if store == 1 else f"warps x{group}"
+            for cs in (1, 2, 4, 8, 16):
+                ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
+                yield line("all-to-all 2^28 f32, 32 KiB chunks", f"cluster a2a cs={cs} store={form} (default pieces)",
+                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
+                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
+                           piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, 0)
         for cs in (1, 2, 4, 8, 16):
             for piece_kib, cps in ((0, 0), (2, 2), (4, 2), (8, 2), (16, 2), (4, 1), (8, 1), (16, 1)):
                 ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)

@@ -39,7 +39,8 @@ typedef enum ap_debug_key {
     AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 3) */
     AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8, 15 or 16 (0 = automatic) */
     AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
-                                   piece to a shared->global bulk copy, 2 eight warps of 16-byte stores */
+                                   piece to a shared->global bulk copy, 2 receiver warps with 16-byte
+                                   stores (AP_DBG_EXCHANGE_GROUP warps per piece) */
     AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: bit 0 bulk loads carry an L2 evict-first policy,
                                    bit 1 consumer stores are streaming (st.global.cs); 0 = none */
     AP_DBG_DEVICE_CHECKS = 11,  /* 1: ring kernels verify, before every stage, that each copy and each
@@ -55,6 +56,9 @@ typedef enum ap_debug_key {
     AP_DBG_LAST_STAGES = 104,   /* ring depth */
     AP_DBG_SCHEDULE = 12,       /* ring stage order: 0 CTA b takes stages b, b + grid, ... (all CTAs
                                    stream one window of memory); 1 each CTA takes a contiguous run */
+    AP_DBG_EXCHANGE_GROUP = 13, /* cluster exchange, warp-store receiver: warps that store one piece
+                                   together, 1, 2, 4 or 8 (the eight receiver warps take pieces in
+                                   turn, 8 / value at once); 0 = automatic */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar

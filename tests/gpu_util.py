@@ -42,6 +42,7 @@ def reset_debug(ap):
         ap.AP_DBG_CACHE_HINTS,
         ap.AP_DBG_DEVICE_CHECKS,
         ap.AP_DBG_SCHEDULE,
+        ap.AP_DBG_EXCHANGE_GROUP,
     ):
         ap.ap_debug_set(key, 0)
 

@@ -59,17 +59,26 @@ def test_all_to_all_twice_is_identity(ap):
         assert torch.equal(b.view(torch.int32), x.view(torch.int32)), f"cs={cs}"
 
 
-def test_all_to_all_ignores_the_tma_store_setting(ap, orc):
-    import torch
-
+@pytest.mark.parametrize("store,group", [(1, 0), (2, 1), (2, 2), (2, 4), (2, 8)])
+@pytest.mark.parametrize("cs", [1, 3, 4, 8, 16])
+def test_all_to_all_receiver_forms(ap, orc, cs, store, group):
+    """The TMA-store receiver and the warp receiver with 1, 2, 4 or 8 warps
+    per piece, over many groups and ring shapes."""
     dev = device()
-    n = 8 * 4 * 8192 // 4
-    x = synth.uniform_pm1_torch(12, n, dev)
-    y = torch.empty_like(x)
-    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 1)
-    ap.ap_cluster_all_to_all(x, y, n, 4, 8192)
-    assert ap.ap_check() == ap.AP_OK
-    assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), 4, 8192), "a2a with the store setting at 1")
+    for sub_bytes, groups, piece, grid in ((16, 9, 0, 0), (1024, 40, 0, cs), (4096, 7, 1024, 0), (2048, 33, 0, 3 * cs)):
+        chunk_bytes = cs * sub_bytes
+        n = groups * cs * chunk_bytes // 4
+        x = synth.uniform_pm1_torch(n + 7 * cs, n, dev)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece)
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), orc.cluster_all_to_all(to_np(x), cs, chunk_bytes),
+                    f"a2a cs={cs} sub={sub_bytes} groups={groups} store={store} group={group}")
+        assert out.intact()
 
 
 @pytest.mark.parametrize("cs", [2, 4, 8, 16])

@@ -18,15 +18,18 @@ def ap():
     reset_debug(ap)
 
 
-@pytest.mark.parametrize("store", [1, 2])
+@pytest.mark.parametrize("store,group", [(1, 0), (2, 0), (2, 1), (2, 2), (2, 4), (2, 8)])
 @pytest.mark.parametrize("cs", [1, 2, 4, 8])
 @pytest.mark.parametrize("chunk_bytes,groups", [(16, 1), (16, 37), (48, 5), (1024, 300), (32768, 3), (100000, 4)])
-def test_exchange_small(ap, orc, cs, chunk_bytes, groups, store):
+def test_exchange_small(ap, orc, cs, chunk_bytes, groups, store, group):
+    """Both receiver forms; the warp form with 1, 2, 4 or 8 warps per piece
+    (8, 4, 2 or 1 pieces draining at once) and its automatic choice."""
     dev = device()
     n = groups * cs * chunk_bytes // 4
     x = synth.uniform_pm1_torch(n + cs, n, dev)
     want = orc.cluster_exchange(to_np(x), cs, chunk_bytes)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
     for grid, piece in ((0, 0), (cs, 0), (cs, 16), (0, 4096)):  # grid cs: one cluster walks every group
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece)

@@ -63,10 +63,12 @@ def test_exchange_wait_times_out_and_recovers(ap, orc, store):
     assert_bits(to_np(y), orc.cluster_exchange(to_np(x), 4, 4096), "exchange after recovery")
 
 
-def test_all_to_all_wait_times_out_and_recovers(ap, orc):
+@pytest.mark.parametrize("store,group", [(1, 0), (2, 1), (2, 4)])
+def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group):
     """The all-to-all's bounded waits: no piece is ever loaded (the loader's
     barrier expects bytes that never come), so nothing is pushed between CTAs,
-    every wait gives up, and the next call runs normally."""
+    every wait gives up (receiver warps of a group agree before leaving), and
+    the next call runs normally."""
     import torch
 
     dev = device()
@@ -75,6 +77,8 @@ def test_all_to_all_wait_times_out_and_recovers(ap, orc):
     x = synth.uniform_pm1_torch(5, n, dev)
     y = torch.empty_like(x)
     _inject(ap)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
     ap.ap_cluster_all_to_all(x, y, n, 4, 4096)
     assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
     reset_debug(ap)
