@@ -4,6 +4,7 @@
 // movement.
 #include <atomic>
 #include <cstdlib>
+#include <string>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -34,6 +35,7 @@ std::atomic<int64_t> g_cache_hints{0};
 std::atomic<int64_t> g_device_checks{0};
 std::atomic<int64_t> g_schedule{0};
 std::atomic<int64_t> g_ex_group{0};
+std::atomic<int64_t> g_strict_align{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0}, g_last_site{0};
@@ -46,6 +48,21 @@ int64_t env_timeout() {
         if (s == nullptr || *s == '\0') return int64_t(0);
         const long long x = std::atoll(s);
         return x > 0 ? static_cast<int64_t>(x) : int64_t(0);
+    }();
+    return v;
+}
+
+// AP_FORCE_PATH=auto|ring|small|tensor (also bulk = ring, cpasync = small, or
+// 0..3): the path a call takes when ap_debug_set has not chosen one.
+int64_t env_force_path() {
+    static const int64_t v = [] {
+        const char* s = std::getenv("AP_FORCE_PATH");
+        if (s == nullptr || *s == '\0') return int64_t(0);
+        const std::string x(s);
+        if (x == "ring" || x == "bulk" || x == "1") return int64_t(1);
+        if (x == "small" || x == "cpasync" || x == "2") return int64_t(2);
+        if (x == "tensor" || x == "3") return int64_t(3);
+        return int64_t(0);
     }();
     return v;
 }
@@ -105,11 +122,16 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;  // keeps every byte offset far 
 
 bool valid_stages(int stages) { return stages >= AP_MIN_STAGES && stages <= AP_MAX_STAGES; }
 
+bool aligned16(const void* a, const void* b) {
+    return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15) == 0;
+}
+
 }  // namespace
 
 Options options() {
     Options o;
-    o.force_path = g_force_path.load();
+    const int64_t fp = g_force_path.load();
+    o.force_path = fp != 0 ? fp : env_force_path();
     o.tx_extra = g_tx_extra.load();
     const int64_t t = g_timeout_ns.load();
     o.timeout_ns = t > 0 ? t : (env_timeout() > 0 ? env_timeout() : kDefaultTimeoutNs);
@@ -123,6 +145,7 @@ Options options() {
     o.device_checks = g_device_checks.load();
     o.schedule = g_schedule.load();
     o.ex_group = g_ex_group.load();
+    o.strict_align = g_strict_align.load();
     return o;
 }
 
@@ -169,11 +192,12 @@ ap_status ap_scale(const float* in, float* out, int64_t n_tiles, int64_t tile_el
     if (in == nullptr || out == nullptr) return AP_ERR_NULL;
     if (!aligned4(in) || !aligned4(out)) return AP_ERR_ALIGN;
     if (in != out && overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    const Options o = options();
+    if (o.strict_align && !aligned16(in, out)) return AP_ERR_ALIGN;
     DeviceInfo di;
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     OpArgs op{OP_SCALE, alpha, 0, nullptr};
-    const Options o = options();
     return launch_ring(di, o, in, out, n, 0, tile_elems, stages, op, o.force_path == 3, stream);
 }
 
@@ -202,6 +226,7 @@ ap_status ap_row_roll(const float* A, float* B, int64_t rows, int64_t cols, int6
     if (!aligned4(A) || !aligned4(B)) return AP_ERR_ALIGN;
     if (overlap(A, 4 * n, B, 4 * n)) return AP_ERR_ALIAS;
     const Options o = options();
+    if (o.strict_align && !aligned16(A, B)) return AP_ERR_ALIGN;
     // Ring depth 3 (24 KiB stages) measured best for the 2^26 x 4 shift,
     // aligned and with a 4-byte offset base.
     const int stages = o.roll_stages > 0 ? static_cast<int>(o.roll_stages) : 3;
@@ -229,11 +254,12 @@ ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, i
     if (in == nullptr || out == nullptr || coeffs == nullptr) return AP_ERR_NULL;
     if (!aligned4(in) || !aligned4(out)) return AP_ERR_ALIGN;
     if (in != out && overlap(in, 4 * n, out, 4 * n)) return AP_ERR_ALIAS;
+    const Options o = options();
+    if (o.strict_align && !aligned16(in, out)) return AP_ERR_ALIGN;
     DeviceInfo di;
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
     OpArgs op{OP_POLY, 0.0f, degree, coeffs};
-    const Options o = options();
     return launch_ring(di, o, in, out, n, 0, 1, stages, op, o.force_path == 3, stream);
 }
 
@@ -423,6 +449,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return AP_ERR_ARG;
             g_ex_group = value;
             return AP_OK;
+        case AP_DBG_STRICT_ALIGN:
+            if (value > 1) return AP_ERR_ARG;
+            g_strict_align = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -443,6 +473,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_DEVICE_CHECKS: return o.device_checks;
         case AP_DBG_SCHEDULE: return o.schedule;
         case AP_DBG_EXCHANGE_GROUP: return o.ex_group;
+        case AP_DBG_STRICT_ALIGN: return o.strict_align;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

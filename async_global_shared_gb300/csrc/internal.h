@@ -35,6 +35,7 @@ struct Options {
     int64_t device_checks;
     int64_t schedule;
     int64_t ex_group;
+    int64_t strict_align;
 };
 
 Options options();

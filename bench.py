@@ -569,7 +569,7 @@ def run_reference(args, d: Dist):
         },
         "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line, "reference")
 
 
 # ----------------------------------------------------------------------------- sweep (per-kernel lines)
@@ -1075,6 +1075,53 @@ def profile_case(name: str, args):
         raise SystemExit(1)
 
 
+# ----------------------------------------------------------------------------- results log
+RESULTS_DIR = os.path.join(ROOT, "results")
+_PROVENANCE = None
+
+
+def provenance() -> dict:
+    """Where a result came from: GPU, git commit (when the tree has .git), a
+    hash of the CUDA sources, time and command line."""
+    global _PROVENANCE
+    if _PROVENANCE is None:
+        sha = None
+        try:
+            r = subprocess.run(["git", "rev-parse", "HEAD"], cwd=ROOT, capture_output=True, text=True, timeout=10)
+            if r.returncode == 0 and r.stdout.strip():
+                sha = r.stdout.strip()
+        except (OSError, subprocess.SubprocessError):
+            pass
+        h = hashlib.sha256()
+        src = os.path.join(ROOT, "async_global_shared_gb300", "csrc")
+        for f in sorted(os.listdir(src)):
+            with open(os.path.join(src, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+        gpu = None
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                gpu = torch.cuda.get_device_name(0)
+        except Exception:  # noqa: BLE001 - provenance is best effort
+            pass
+        _PROVENANCE = {"gpu": gpu, "git_sha": sha, "source_hash": h.hexdigest()[:16], "argv": sys.argv[1:]}
+    return dict(_PROVENANCE, time=datetime.datetime.now(datetime.timezone.utc).isoformat(timespec="seconds"))
+
+
+def emit(line: dict, kind: str) -> None:
+    """Print one JSON result line and append it, with its provenance, to
+    results/<kind>.jsonl (bench: the headline line; sweep: per-kernel lines;
+    reference: the oracle arm)."""
+    print(json.dumps(line), flush=True)
+    try:
+        os.makedirs(RESULTS_DIR, exist_ok=True)
+        with open(os.path.join(RESULTS_DIR, f"{kind}.jsonl"), "a") as f:
+            f.write(json.dumps(dict(line, provenance=provenance())) + "\n")
+    except OSError:
+        pass
+
+
 def main(argv=None):
     ap_ = argparse.ArgumentParser()
     ap_.add_argument("--gpus", type=int, default=1)
@@ -1102,7 +1149,7 @@ def main(argv=None):
         elif args.workload == "scale":
             res = bench_scale(args, d)
             if d.rank == 0:
-                print(json.dumps(res), flush=True)
+                emit(res, "bench")
         elif d.rank == 0:
             with ClockSampler(0) as clk:
                 lines = list(sweep(args.workload, args))
@@ -1113,7 +1160,7 @@ def main(argv=None):
                 w = line.pop("_window", None)
                 if w is not None:
                     line["clocks"] = clk.window(w[0], w[1], rows)
-                print(json.dumps(line), flush=True)
+                emit(line, "sweep")
     finally:
         d.close()
 

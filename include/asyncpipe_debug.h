@@ -20,7 +20,8 @@ extern "C" {
 
 typedef enum ap_debug_key {
     /* settable */
-    AP_DBG_FORCE_PATH = 1,      /* 0 auto; 1 always the ring (also for small row shifts);
+    AP_DBG_FORCE_PATH = 1,      /* (when 0, the environment variable AP_FORCE_PATH = auto, ring or
+                                   bulk, small or cpasync, tensor, or 0..3, read once, decides) 0 auto; 1 always the ring (also for small row shifts);
                                    2 small one-CTA row shift when it fits; 3 ring with a tensor-map
                                    producer (cp.async.bulk.tensor) for ap_row_roll, ap_scale and
                                    ap_poly where input and output are 16-byte aligned and every span
@@ -59,6 +60,9 @@ typedef enum ap_debug_key {
     AP_DBG_EXCHANGE_GROUP = 13, /* cluster exchange, warp-store receiver: warps that store one piece
                                    together, 1, 2, 4 or 8 (the eight receiver warps take pieces in
                                    turn, 8 / value at once); 0 = automatic */
+    AP_DBG_STRICT_ALIGN = 14,   /* 1: ap_scale, ap_poly and ap_row_roll return AP_ERR_ALIGN for
+                                   buffers that are not 16-byte aligned instead of taking the
+                                   cp.async edge fallback (checked before any CUDA call) */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar

@@ -43,6 +43,7 @@ def reset_debug(ap):
         ap.AP_DBG_DEVICE_CHECKS,
         ap.AP_DBG_SCHEDULE,
         ap.AP_DBG_EXCHANGE_GROUP,
+        ap.AP_DBG_STRICT_ALIGN,
     ):
         ap.ap_debug_set(key, 0)
 

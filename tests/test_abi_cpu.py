@@ -128,6 +128,44 @@ def test_validation_before_cuda(ap):
     assert raw(ap, a2a, FAKE_IN, FAKE_IN + 16, 1 << 20, 4, 32768, None) == ap.AP_ERR_ALIAS
 
 
+def test_strict_alignment_switch(ap):
+    """With AP_DBG_STRICT_ALIGN the ring calls refuse buffers off the 16-byte
+    grid (before any CUDA call) instead of taking the cp.async fallback."""
+    lib = ap.load()
+    try:
+        assert lib.ap_debug_set(ap.AP_DBG_STRICT_ALIGN, 2) == ap.AP_ERR_ARG
+        ap.ap_debug_set(ap.AP_DBG_STRICT_ALIGN, 1)
+        assert raw(ap, "ap_scale", FAKE_IN + 4, FAKE_OUT, 4, 256, 2.0, 2, None) == ap.AP_ERR_ALIGN
+        assert raw(ap, "ap_scale", FAKE_IN, FAKE_OUT + 8, 4, 256, 2.0, 2, None) == ap.AP_ERR_ALIGN
+        c = np.zeros(4, dtype=np.float32).ctypes.data
+        assert raw(ap, "ap_poly", FAKE_IN + 12, FAKE_OUT, 100, c, 3, 2, None) == ap.AP_ERR_ALIGN
+        assert raw(ap, "ap_row_roll", FAKE_IN, FAKE_OUT + 4, 64, 4, 1, None) == ap.AP_ERR_ALIGN
+        assert raw(ap, "ap_scale", FAKE_IN + 4, FAKE_OUT, 0, 256, 2.0, 2, None) == ap.AP_OK  # empty stays a no-op
+    finally:
+        ap.ap_debug_set(ap.AP_DBG_STRICT_ALIGN, 0)
+    if not __import__("torch").cuda.is_available():
+        # without the switch a misaligned buffer passes validation (and fails at the first CUDA call here)
+        assert raw(ap, "ap_scale", FAKE_IN + 4, FAKE_OUT, 4, 256, 2.0, 2, None) == ap.AP_ERR_CUDA
+
+
+@pytest.mark.parametrize("value,want", [("tensor", 3), ("cpasync", 2), ("small", 2), ("bulk", 1), ("ring", 1),
+                                        ("auto", 0), ("bogus", 0), ("3", 3)])
+def test_force_path_environment_variable(value, want):
+    """AP_FORCE_PATH chooses the path when ap_debug_set has not; an explicit
+    setting still wins."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import async_global_shared_gb300 as ap; print(ap.ap_debug_get(ap.AP_DBG_FORCE_PATH)); "
+            "ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 1); print(ap.ap_debug_get(ap.AP_DBG_FORCE_PATH))")
+    env = dict(os.environ, AP_FORCE_PATH=value, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(want), "1"]
+
+
 def test_debug_settings_roundtrip(ap):
     lib = ap.load()
     assert lib.ap_debug_set(ap.AP_DBG_STAGE_BYTES, -5) == ap.AP_ERR_ARG

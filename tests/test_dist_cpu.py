@@ -65,3 +65,24 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_results_log_appends_with_provenance(tmp_path, monkeypatch, capsys):
+    """Every printed bench line is also appended to results/<kind>.jsonl with
+    the GPU name, git commit, a hash of the CUDA sources, time and argv."""
+    import json
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setattr(bench, "RESULTS_DIR", str(tmp_path))
+    bench.emit({"metric": "m", "value": 1.5}, "sweep")
+    bench.emit({"metric": "m", "value": 2.5}, "sweep")
+    printed = [json.loads(l) for l in capsys.readouterr().out.splitlines()]
+    assert printed == [{"metric": "m", "value": 1.5}, {"metric": "m", "value": 2.5}]
+    rows = [json.loads(l) for l in (tmp_path / "sweep.jsonl").read_text().splitlines()]
+    assert [r["value"] for r in rows] == [1.5, 2.5]
+    prov = rows[0]["provenance"]
+    assert set(prov) >= {"gpu", "git_sha", "source_hash", "argv", "time"}
+    assert len(prov["source_hash"]) == 16
