@@ -13,18 +13,19 @@
 // equal pieces (each a ring item), so the load, the hand-off and the store
 // of one chunk overlap each other; piece q of a chunk lands as piece q of the
 // receiver's output chunk, so the result is the same as moving whole chunks.
-// CTA rank r has three roles, one warp each for the two single-thread roles:
+// CTA rank r has three roles, one warp each for the two single-thread roles
+// (rank r receives from rank r + shift, 1 for ap_cluster_exchange):
 //   loader   (warp 0): waits credit[s], loads the next piece of its chunk of
 //            the group from global memory into send[s] (bulk copy, load_full[s]).
 //   pusher   (warp 1): waits load_full[s], pushes send[s] into recv[s] of
-//            rank (r-1) mod cs, completing on that CTA's recv_full[s].
-//   receiver (8 warps, one item each in turn): waits on recv_full[s],
-//            stores recv[s] to its output chunk with 16-byte stores, arms
-//            recv_full[s] with the bytes of the slot's next item, then
-//            arrives (remote) on credit[s] of rank (r+1) mod cs, the CTA
-//            that sends to it. In the TMA-store form one thread instead
-//            hands recv[s] to a shared->global bulk copy and credits the
-//            slot once that copy has read it.
+//            rank (r - shift) mod cs, completing on that CTA's recv_full[s].
+//   receiver (8 warps in groups of 1, 2, 4 or 8, a piece per group in turn):
+//            waits on recv_full[s], stores recv[s] to its output chunk with
+//            16-byte stores, arms recv_full[s] with the bytes of the slot's
+//            next item, then arrives (remote) on credit[s] of rank
+//            (r + shift) mod cs, the CTA that sends to it. In the TMA-store
+//            form one thread instead hands recv[s] to a shared->global bulk
+//            copy and credits the slot once that copy has read it.
 // Before the final cluster barrier each pusher waits (bounded) for the
 // credits of its last S pieces, so no copy is in flight when a CTA leaves.
 // credit[s] therefore tells a sender both that its send[s] has been read

@@ -1027,6 +1027,23 @@ def sweep(which: str, args):
         yield {"workload": "roll 64x4 f32 (one CTA, 64 threads)", "kernel": "roll_small",
                "us_per_call": round(ms * 1e3, 2), "note": "launch-latency bound; no roofline",
                "_window": (window["t0"], window["t1"])}
+        # the same calls replayed from a CUDA graph (100 calls per graph),
+        # captured on a side stream and replayed on the timed stream
+        calls = 100
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            ap.ap_row_roll(A, B, 64, 4, 1, gs)
+        gs.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            for _ in range(calls):
+                ap.ap_row_roll(A, B, 64, 4, 1, gs)
+        ms = run(g.replay) / calls
+        yield {"workload": "roll 64x4 f32 (one CTA, 64 threads)", "kernel": "roll_small, 100 calls per CUDA graph",
+               "us_per_call": round(ms * 1e3, 2), "note": "graph replay removes the per-call launch cost",
+               "_window": (window["t0"], window["t1"])}
+        del g
     yield {"workload": "device", "sms": sms, "hbm_peak_gbs": peak}
 
 

@@ -28,6 +28,12 @@
  *    a kernel (a bounded wait that gave up) are reported by ap_check().
  *  - A call with zero elements is a no-op that returns AP_OK and touches no
  *    pointer.
+ *  - The streaming calls (scale, sync scale, row shift, poly, the cluster
+ *    calls, the masked copy) may be captured into a CUDA graph on a capturing
+ *    stream once each has run on the device outside capture (the first call
+ *    sets one-time kernel attributes); a replay runs them with the pointers
+ *    and sizes of the capture. ap_check synchronises its stream and
+ *    ap_autotune times launches, so neither may be captured.
  *  - The library allocates no device memory. Its only device state is one
  *    status word per device, a static __device__ variable of the library.
  *  - Runs only on compute capability 10.3 devices (GB300):
