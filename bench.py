@@ -726,6 +726,23 @@ def sweep(which: str, args):
                                    fp32_tflops=round(tflops, 2), fma_per_elem=K)
             ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 0)
             ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
+        if "polyocc" in groups:
+            # degree 128 (fma-bound): consumer warps x CTAs per SM x stage size
+            c = synth.coeffs_np(128).tolist()
+            for warps, cps, S, kib in ((16, 1, 3, 64), (16, 1, 2, 96), (8, 1, 3, 64), (8, 2, 3, 32), (8, 2, 2, 48),
+                                       (8, 3, 2, 32), (8, 3, 3, 24), (15, 1, 3, 64), (8, 2, 3, 24), (16, 1, 6, 32)):
+                ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+                ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
+                try:
+                    ms = run(lambda: ap.ap_poly(x, y, n, c, 128, S))
+                except ap.APError:
+                    continue
+                yield line("poly 2^30 f32", f"ring S={S} K=128 warps={warps} ctas/SM={cps} stage={kib}KiB", 8 * n, ms,
+                           fp32_tflops=round(2.0 * 128 * n / (ms * 1e-3) / 1e12, 2),
+                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+            for key in (ap.AP_DBG_CONSUMER_WARPS, ap.AP_DBG_CTAS_PER_SM, ap.AP_DBG_STAGE_BYTES):
+                ap.ap_debug_set(key, 0)
         if "polytune" in groups:
             for K in (32, 128):
                 c = synth.coeffs_np(K).tolist()
