@@ -36,6 +36,7 @@ std::atomic<int64_t> g_device_checks{0};
 std::atomic<int64_t> g_schedule{0};
 std::atomic<int64_t> g_ex_group{0};
 std::atomic<int64_t> g_strict_align{0};
+std::atomic<int64_t> g_ex_lanes{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0}, g_last_site{0};
@@ -146,6 +147,7 @@ Options options() {
     o.schedule = g_schedule.load();
     o.ex_group = g_ex_group.load();
     o.strict_align = g_strict_align.load();
+    o.ex_lanes = g_ex_lanes.load();
     return o;
 }
 
@@ -453,6 +455,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 1) return AP_ERR_ARG;
             g_strict_align = value;
             return AP_OK;
+        case AP_DBG_EXCHANGE_LANES:
+            if (value != 0 && value != 1 && value != 2 && value != 4) return AP_ERR_ARG;
+            g_ex_lanes = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -474,6 +480,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_SCHEDULE: return o.schedule;
         case AP_DBG_EXCHANGE_GROUP: return o.ex_group;
         case AP_DBG_STRICT_ALIGN: return o.strict_align;
+        case AP_DBG_EXCHANGE_LANES: return o.ex_lanes;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

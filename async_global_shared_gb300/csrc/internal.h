@@ -36,6 +36,7 @@ struct Options {
     int64_t schedule;
     int64_t ex_group;
     int64_t strict_align;
+    int64_t ex_lanes;
 };
 
 Options options();

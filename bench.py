@@ -828,6 +828,19 @@ def sweep(which: str, args):
                        grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, 0)
+        # loader and pusher lanes with smaller pieces (ring depths that 2 and 4 divide)
+        for piece_kib, cps in ((4, 2), (2, 2), (8, 1)):
+            for lanes in (1, 2, 4):
+                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
+                ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+                ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
+                for cs in (2, 8):
+                    ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
+                    yield line("exchange 2^28 f32, 32 KiB chunks",
+                               f"cluster cs={cs} piece={piece_kib}KiB ctas/SM={cps} lanes={lanes}", 8 * n, ms,
+                               slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
+        for key in (ap.AP_DBG_STAGE_BYTES, ap.AP_DBG_CTAS_PER_SM, ap.AP_DBG_EXCHANGE_LANES):
+            ap.ap_debug_set(key, 0)
         for cps in (3, 4):
             ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
             for piece_kib in (4, 8):
@@ -879,6 +892,15 @@ def sweep(which: str, args):
                            piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
+        # loader and pusher lanes, at the default receiver and pieces
+        for lanes in (1, 2, 4):
+            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
+            for cs in (1, 2, 4, 8, 16):
+                ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
+                yield line("all-to-all 2^28 f32, 32 KiB chunks", f"cluster a2a cs={cs} lanes={lanes} (default pieces)",
+                           8 * n, ms, slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
+                           piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, 0)
         del x, y
     if "autotune" in groups:
         n = 1 << 28

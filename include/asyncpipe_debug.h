@@ -63,6 +63,9 @@ typedef enum ap_debug_key {
     AP_DBG_STRICT_ALIGN = 14,   /* 1: ap_scale, ap_poly and ap_row_roll return AP_ERR_ALIGN for
                                    buffers that are not 16-byte aligned instead of taking the
                                    cp.async edge fallback (checked before any CUDA call) */
+    AP_DBG_EXCHANGE_LANES = 15, /* cluster exchange: threads that load and threads that push, 1, 2
+                                   or 4 each, lane l taking items l, l + lanes, ... (reduced to a
+                                   divisor of the ring depth); 0 = automatic */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar

@@ -44,6 +44,7 @@ def reset_debug(ap):
         ap.AP_DBG_SCHEDULE,
         ap.AP_DBG_EXCHANGE_GROUP,
         ap.AP_DBG_STRICT_ALIGN,
+        ap.AP_DBG_EXCHANGE_LANES,
     ):
         ap.ap_debug_set(key, 0)
 

@@ -178,6 +178,10 @@ def test_debug_settings_roundtrip(ap):
     assert ap.ap_debug_get(ap.AP_DBG_TIMEOUT_NS) > 0  # default limit applies when unset
     for bad in (3, 5, 16):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, bad) == ap.AP_ERR_ARG
+    for bad in (3, 8):
+        assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, bad) == ap.AP_ERR_ARG
+    for good in (1, 2, 4, 0):
+        assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, good) == ap.AP_OK
     for good in (1, 2, 4, 8, 0):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, good) == ap.AP_OK
 

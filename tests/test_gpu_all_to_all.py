@@ -59,11 +59,13 @@ def test_all_to_all_twice_is_identity(ap):
         assert torch.equal(b.view(torch.int32), x.view(torch.int32)), f"cs={cs}"
 
 
+@pytest.mark.parametrize("lanes", [1, 2, 4])
 @pytest.mark.parametrize("store,group", [(1, 0), (2, 1), (2, 2), (2, 4), (2, 8)])
 @pytest.mark.parametrize("cs", [1, 3, 4, 8, 16])
-def test_all_to_all_receiver_forms(ap, orc, cs, store, group):
+def test_all_to_all_receiver_forms(ap, orc, cs, store, group, lanes):
     """The TMA-store receiver and the warp receiver with 1, 2, 4 or 8 warps
-    per piece, over many groups and ring shapes."""
+    per piece, with 1, 2 or 4 loader and pusher lanes, over many groups and
+    ring shapes."""
     dev = device()
     for sub_bytes, groups, piece, grid in ((16, 9, 0, 0), (1024, 40, 0, cs), (4096, 7, 1024, 0), (2048, 33, 0, 3 * cs)):
         chunk_bytes = cs * sub_bytes
@@ -71,13 +73,14 @@ def test_all_to_all_receiver_forms(ap, orc, cs, store, group):
         x = synth.uniform_pm1_torch(n + 7 * cs, n, dev)
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         out = Guarded(n, 0, dev)
         ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk_bytes)
         assert ap.ap_check() == ap.AP_OK
         assert_bits(to_np(out.view), orc.cluster_all_to_all(to_np(x), cs, chunk_bytes),
-                    f"a2a cs={cs} sub={sub_bytes} groups={groups} store={store} group={group}")
+                    f"a2a cs={cs} sub={sub_bytes} groups={groups} store={store} group={group} lanes={lanes}")
         assert out.intact()
 
 

@@ -30,15 +30,20 @@ def test_exchange_small(ap, orc, cs, chunk_bytes, groups, store, group):
     want = orc.cluster_exchange(to_np(x), cs, chunk_bytes)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
-    for grid, piece in ((0, 0), (cs, 0), (cs, 16), (0, 4096)):  # grid cs: one cluster walks every group
+    # grid cs: one cluster walks every group; CTAs/SM 3 gives a ring depth the
+    # loader and pusher lanes (2 or 4) divide
+    for grid, piece, lanes, cps in ((0, 0, 0, 0), (cs, 0, 2, 0), (cs, 16, 4, 0), (0, 4096, 4, 3), (0, 1024, 2, 3)):
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
         out = Guarded(n, 0, dev)
         ap.ap_cluster_exchange(x, out.view, n, cs, chunk_bytes)
         assert ap.ap_check() == ap.AP_OK
         assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 4
         assert_bits(to_np(out.view), want,
-                    f"exchange cs={cs} chunk={chunk_bytes} groups={groups} grid={grid} piece={piece} store={store}")
+                    f"exchange cs={cs} chunk={chunk_bytes} groups={groups} grid={grid} piece={piece} store={store} "
+                    f"lanes={lanes} cps={cps}")
         assert out.intact()
 
 

@@ -63,8 +63,8 @@ def test_exchange_wait_times_out_and_recovers(ap, orc, store):
     assert_bits(to_np(y), orc.cluster_exchange(to_np(x), 4, 4096), "exchange after recovery")
 
 
-@pytest.mark.parametrize("store,group", [(1, 0), (2, 1), (2, 4)])
-def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group):
+@pytest.mark.parametrize("store,group,lanes", [(1, 0, 1), (2, 1, 2), (2, 4, 4)])
+def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group, lanes):
     """The all-to-all's bounded waits: no piece is ever loaded (the loader's
     barrier expects bytes that never come), so nothing is pushed between CTAs,
     every wait gives up (receiver warps of a group agree before leaving), and
@@ -79,6 +79,7 @@ def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group):
     _inject(ap)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
     ap.ap_cluster_all_to_all(x, y, n, 4, 4096)
     assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
     reset_debug(ap)

@@ -96,6 +96,7 @@ def test_exchange_fuzz(ap, orc, seed):
         ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, int(rng.choice([0, 1, 2])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
         out = Guarded(n, 0, dev)
         ap.ap_cluster_exchange(x, out.view, n, cs, chunk)
         what = f"seed={seed} case={case} cs={cs} chunk={chunk} groups={groups}"
