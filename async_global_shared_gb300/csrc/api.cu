@@ -37,6 +37,7 @@ std::atomic<int64_t> g_schedule{0};
 std::atomic<int64_t> g_ex_group{0};
 std::atomic<int64_t> g_strict_align{0};
 std::atomic<int64_t> g_ex_lanes{0};
+std::atomic<int64_t> g_ex_batch{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0}, g_last_site{0};
@@ -129,6 +130,20 @@ bool aligned16(const void* a, const void* b) {
 
 }  // namespace
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
 Options options() {
     Options o;
     const int64_t fp = g_force_path.load();
@@ -148,6 +163,7 @@ Options options() {
     o.ex_group = g_ex_group.load();
     o.strict_align = g_strict_align.load();
     o.ex_lanes = g_ex_lanes.load();
+    o.ex_batch = g_ex_batch.load();
     return o;
 }
 
@@ -459,6 +475,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value != 0 && value != 1 && value != 2 && value != 4) return AP_ERR_ARG;
             g_ex_lanes = value;
             return AP_OK;
+        case AP_DBG_EXCHANGE_BATCH:
+            if (value > 256) return AP_ERR_ARG;
+            g_ex_batch = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -481,6 +501,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_EXCHANGE_GROUP: return o.ex_group;
         case AP_DBG_STRICT_ALIGN: return o.strict_align;
         case AP_DBG_EXCHANGE_LANES: return o.ex_lanes;
+        case AP_DBG_EXCHANGE_BATCH: return o.ex_batch;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

@@ -41,6 +41,7 @@
 // credit protocol above holds unchanged, with the peer chosen per item.
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -54,9 +55,16 @@ constexpr int kExThreads = 64 + kExConsumers;
 constexpr int64_t kExMaxSlots = 16;
 
 struct ExParams {
+    // Batched form: the input and output as 5-D tensors {e0, e1, nsub, cs,
+    // groups} (e0 * e1 floats = one sub-block; nsub = cs sub-blocks per chunk
+    // in the all-to-all, else 1), so that one box gathers a rank's sub-block
+    // from `batch` consecutive groups.
+    CUtensorMap tin;
+    CUtensorMap tout;
+    int batch;             // groups per item in the batched form; 0: items are pieces of chunks
     const float* in;
     float* out;
-    int64_t groups;        // whole groups of cluster_size chunks
+    int64_t groups;        // whole groups of cluster_size chunks (batched form: batches of `batch` groups)
     uint32_t chunk_bytes;  // multiple of 16
     uint32_t piece_bytes;  // divides chunk_bytes, multiple of 16
     int pieces;            // chunk_bytes / piece_bytes
@@ -117,6 +125,10 @@ struct ItemCursor {
     }
 };
 
+// kBatched: items are batches of groups moved with tensor-map boxes (a
+// separate instantiation, so that the single-thread roles of the plain form
+// carry no branch for it: they are bound by their per-item latency).
+template <bool kBatched>
 __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_constant__ ExParams P) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = P.stages;
@@ -164,6 +176,17 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
     };
     const unsigned char* in_bytes = reinterpret_cast<const unsigned char*>(P.in);
     unsigned char* out_bytes = reinterpret_cast<unsigned char*>(P.out);
+    // Load item c into send slot s: one box of this rank's (sub-block of its)
+    // chunk from `batch` groups, or one bulk copy of a piece.
+    auto load_item = [&](const ItemCursor& c, int s) {
+        const uint32_t dst = ptx::smem_addr(send + static_cast<size_t>(s) * CB);
+        if constexpr (kBatched) {
+            ptx::tensor_g2s_5d(dst, &P.tin, 0, 0, P.a2a ? static_cast<int32_t>(a2a_dst(c)) : 0,
+                               static_cast<int32_t>(rank), static_cast<int32_t>(c.grp * P.batch), load_full(s));
+        } else {
+            ptx::bulk_g2s(dst, in_bytes + item_off(c, a2a_dst(c)), CB, load_full(s));
+        }
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -175,6 +198,10 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
         for (int s = 0; s < S; ++s) taken[s] = 0;
         for (int g = 0; g < kExConsumerWarps; ++g) group_bad[g] = 0;
         ptx::fence_mbar_init();
+    }
+    if (kBatched && threadIdx.x == 0) {
+        ptx::prefetch_tensormap(&P.tin);
+        ptx::prefetch_tensormap(&P.tout);
     }
     __syncthreads();
     ptx::cluster_sync();  // every CTA's barriers exist before anyone sends
@@ -207,8 +234,7 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                     break;
                 }
                 ptx::mbar_arrive_expect_tx(load_full(s), CB + P.tx_extra);
-                ptx::bulk_g2s(ptx::smem_addr(send + static_cast<size_t>(s) * CB), in_bytes + item_off(c, a2a_dst(c)),
-                              CB, load_full(s));
+                load_item(c, s);
             }
             for (int64_t k = i > S ? i - S : 0; k < i; ++k) {
                 if (wait_phase<false>(load_full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1),
@@ -227,8 +253,7 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                     break;
                 }
                 ptx::mbar_arrive_expect_tx(load_full(s), CB + P.tx_extra);
-                ptx::bulk_g2s(ptx::smem_addr(send + static_cast<size_t>(s) * CB), in_bytes + item_off(c, a2a_dst(c)),
-                              CB, load_full(s));
+                load_item(c, s);
                 c.advance(L, S, NP, P.cs, ncl);
             }
             for (int64_t k = lane_first(i - S); k < i; k += L) {
@@ -319,8 +344,14 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                     if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_EX_RECEIVER_FULL, abort_flag);
                     break;
                 }
-                ptx::bulk_s2g(out_bytes + item_off(c, a2a_src(c)), ptx::smem_addr(recv + static_cast<size_t>(s) * CB),
-                              CB);
+                const uint32_t src = ptx::smem_addr(recv + static_cast<size_t>(s) * CB);
+                if constexpr (kBatched) {
+                    // the sender's sub-block lands as sub-block `sender` of this rank's chunks
+                    ptx::tensor_s2g_5d(&P.tout, 0, 0, P.a2a ? static_cast<int32_t>(a2a_src(c)) : 0,
+                                       static_cast<int32_t>(rank), static_cast<int32_t>(c.grp * P.batch), src);
+                } else {
+                    ptx::bulk_s2g(out_bytes + item_off(c, a2a_src(c)), src, CB);
+                }
                 ptx::bulk_commit();
                 if (lag == 2) {
                     ptx::bulk_wait_read<2>();
@@ -495,6 +526,40 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
         }
         if (S == 0) return AP_ERR_SMEM;
     }
+    // Batched form: a sub-block (the chunk, outside the all-to-all) under
+    // 8 KiB makes items too small for the single-thread roles (256-byte chunks:
+    // 0.04 of the copy as pieces), so an item gathers a rank's sub-block from
+    // `batch` consecutive groups with one tensor-map box (about 8 KiB), pushes
+    // it as one bulk copy and stores it with one tensor-map box; the engine
+    // clips the last, partial batch at the tensor's edge. Needs a sub-block of
+    // at most 256 floats or a multiple of 256 (a box extent is at most 256),
+    // and a batch of whole 128-byte multiples (box destinations).
+    const int64_t nsub = a2a ? cs : 1;
+    const int64_t sub = chunk_bytes / nsub;
+    const int64_t sub_e = sub / 4;
+    int64_t batch = 0;
+    // Automatic: fixed neighbour for chunks under 8 KiB, items of 8 KiB; the
+    // all-to-all for sub-blocks under 4 KiB (at 4 KiB plain pieces already run
+    // at the copy's rate), items sized for a ring of about 2 cs slots.
+    const int64_t item_target = a2a ? std::min<int64_t>(8192, budget / (4 * cs)) : 8192;
+    if (o.ex_batch != 1 && (o.ex_batch >= 2 || sub < (a2a ? 4096 : 8192)) && (sub_e <= 256 || sub_e % 256 == 0) &&
+        groups < (int64_t(1) << 31) && tensor_map_encoder() != nullptr) {
+        int64_t m = 128;  // smallest batch step keeping batch * sub a multiple of 128
+        while (m > 1 && (sub * (m / 2)) % 128 == 0) m /= 2;
+        int64_t b = o.ex_batch >= 2 ? o.ex_batch : std::max<int64_t>(1, item_target / sub);
+        b = std::min<int64_t>(256, (b + m - 1) / m * m);
+        if (b > 256 - 256 % m) b = 256 - 256 % m;
+        const int64_t min_slots = a2a ? std::max<int64_t>(2, cs) : 2;
+        while (b > m && 2 * min_slots * b * sub > budget) b -= m;
+        if (b >= 2 && 2 * min_slots * b * sub <= budget) batch = b;
+    }
+    int64_t work = groups;  // what the clusters walk: groups, or batches of groups
+    if (batch > 0) {
+        piece = batch * sub;
+        S = std::min<int64_t>(budget / (2 * piece), kExMaxSlots);
+        if (a2a) S -= S % cs;
+        work = (groups + batch - 1) / batch;
+    }
     const int64_t smem = 2 * S * piece + 3 * 8 * S + 16 + 4 * kExMaxSlots + 4 * kExConsumerWarps;  // + abort flag,
                                                                                                  // taken[], group_bad[]
     if (smem > di.smem_optin) return AP_ERR_SMEM;
@@ -507,7 +572,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     // so in-order draining waits on the slowest sender): bulk stores for
     // clusters of 1-2 (1.01-1.02), one warp per piece from 4 up (0.92-1.01;
     // eight warps per piece: 0.53-0.56).
-    const bool tma_store = o.ex_tma_store == 1 || (o.ex_tma_store == 0 && a2a && cs <= 2);
+    const bool tma_store = batch > 0 || o.ex_tma_store == 1 || (o.ex_tma_store == 0 && a2a && cs <= 2);
     const int64_t rgroup = o.ex_group > 0 ? o.ex_group : (!a2a && cs <= 8 ? kExConsumerWarps : 1);
     if (rgroup != 1 && rgroup != 2 && rgroup != 4 && rgroup != 8) return AP_ERR_ARG;
     // Loader and pusher lanes, unless set: four for all-to-all pieces of 2 KiB
@@ -521,19 +586,48 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     static std::atomic<bool> configured[64];  // attributes set on this device (setting twice is harmless)
     if (di.device < 0 || di.device >= 64) return AP_ERR_CUDA;
     if (!configured[di.device].load()) {
-        if (cudaFuncSetAttribute(exchange_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(exchange_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-            return AP_ERR_CUDA;
+        for (auto kernel : {exchange_kernel<false>, exchange_kernel<true>}) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                return AP_ERR_CUDA;
+        }
         configured[di.device] = true;
     }
+    auto kernel = batch > 0 ? exchange_kernel<true> : exchange_kernel<false>;
 
-    ExParams P{in,
+    CUtensorMap tin, tout;
+    std::memset(&tin, 0, sizeof(tin));
+    std::memset(&tout, 0, sizeof(tout));
+    if (batch > 0) {
+        const int64_t e0 = std::min<int64_t>(sub_e, 256);
+        const cuuint64_t dims[5] = {static_cast<cuuint64_t>(e0), static_cast<cuuint64_t>(sub_e / e0),
+                                    static_cast<cuuint64_t>(nsub), static_cast<cuuint64_t>(cs),
+                                    static_cast<cuuint64_t>(groups)};
+        const cuuint64_t strides[4] = {static_cast<cuuint64_t>(4 * e0), static_cast<cuuint64_t>(sub),
+                                       static_cast<cuuint64_t>(chunk_bytes),
+                                       static_cast<cuuint64_t>(cs) * static_cast<cuuint64_t>(chunk_bytes)};
+        const cuuint32_t box[5] = {static_cast<cuuint32_t>(e0), static_cast<cuuint32_t>(sub_e / e0), 1, 1,
+                                   static_cast<cuuint32_t>(batch)};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        auto encode = tensor_map_encoder();
+        for (int k = 0; k < 2; ++k) {
+            if (encode(k == 0 ? &tin : &tout, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
+                       k == 0 ? const_cast<float*>(in) : out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return AP_ERR_CUDA;
+        }
+    }
+    ExParams P{tin,
+               tout,
+               static_cast<int>(batch),
+               in,
                out,
-               groups,
+               work,
                static_cast<uint32_t>(chunk_bytes),
                static_cast<uint32_t>(piece),
-               static_cast<int>(chunk_bytes / piece),
+               static_cast<int>(batch > 0 ? nsub : chunk_bytes / piece),
                cs,
                static_cast<int>(((shift % cs) + cs) % cs),
                static_cast<int>(S),
@@ -541,7 +635,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
                a2a ? 1 : 0,
                static_cast<int>(rgroup),
                static_cast<int>(lanes),
-               static_cast<int>(a2a ? span / piece : 1),
+               static_cast<int>(a2a && batch == 0 ? span / piece : 1),
                static_cast<uint32_t>(o.tx_extra),
                static_cast<uint64_t>(o.timeout_ns),
                di.status};
@@ -559,16 +653,16 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
     int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, exchange_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess) {
         cudaGetLastError();  // clear: an unsupported cluster shape is an argument error, not a sticky one
         return cs > AP_MAX_CLUSTER ? AP_ERR_CLUSTER : AP_ERR_CUDA;
     }
     if (max_clusters < 1) return AP_ERR_CLUSTER;
-    int64_t ncl = std::min<int64_t>(groups, max_clusters);
+    int64_t ncl = std::min<int64_t>(work, max_clusters);
     if (o.grid > 0) ncl = std::max<int64_t>(1, std::min<int64_t>(ncl, o.grid / cs));
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs), 1, 1);
-    record_launch(PATH_EXCHANGE, ncl * cs, piece / 4, smem, S, 0);
-    if (cudaLaunchKernelEx(&cfg, exchange_kernel, P) != cudaSuccess) return AP_ERR_CUDA;
+    record_launch(PATH_EXCHANGE, ncl * cs, piece / 4, smem, S, batch > 0 ? 4 : 0);
+    if (cudaLaunchKernelEx(&cfg, kernel, P) != cudaSuccess) return AP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
 }
 

@@ -2,6 +2,8 @@
 // per-kernel launchers (one translation unit per kernel family).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,9 +39,14 @@ struct Options {
     int64_t ex_group;
     int64_t strict_align;
     int64_t ex_lanes;
+    int64_t ex_batch;
 };
 
 Options options();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if
+// the driver lacks it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // What a launcher reports about the launch it made (AP_DBG_LAST_*).
 void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem, int64_t stages, int64_t flags);

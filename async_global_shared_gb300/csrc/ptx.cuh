@@ -116,6 +116,30 @@ __device__ __forceinline__ void tensor_g2s_2d(uint32_t dst, const void* tmap, in
         : "memory");
 }
 
+// Global -> shared copy of one 5-D box described by a tensor map, box at
+// coordinates {c0 .. c4} (c0 * element size a multiple of 16); elements
+// outside the tensor arrive as zeros. Completes `box bytes` of transactions
+// on bar; dst 128-byte aligned.
+__device__ __forceinline__ void tensor_g2s_5d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                              int32_t c3, int32_t c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+        "%6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// Shared -> global store of one 5-D box into a tensor map's tensor; elements
+// of the box outside the tensor are not written. Tracked by bulk groups
+// (bulk_commit, bulk_wait_read); src 128-byte aligned.
+__device__ __forceinline__ void tensor_s2g_5d(const void* tmap, int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                              int32_t c4, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(tmap),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
+        : "memory");
+}
+
 // Global -> shared copy of one 1-D box described by a tensor map: box_elems
 // consecutive elements from element c0 (c0 * element size a multiple of 16);
 // elements past the tensor's end arrive as zeros. Completes `box bytes` of

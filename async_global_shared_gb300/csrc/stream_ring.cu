@@ -512,20 +512,6 @@ RingShape auto_ring_shape(OpKind kind, int stages) {
 
 namespace {
 
-// cuTensorMapEncodeTiled, looked up once through the runtime (no -lcuda).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
 template <class Op>
 void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeom& g, int stages, uint32_t tx_extra,
                  uint64_t timeout, uint32_t* status, int64_t coef_off, uint32_t hints, const CUtensorMap& tmap,

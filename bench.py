@@ -828,6 +828,23 @@ def sweep(which: str, args):
                        grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, 0)
+        # small chunks (the pages' example moves 256 bytes): batched against plain pieces
+        for chunk in (256, 1024, 4096):
+            for batch in (0, 1):
+                ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, batch)
+                for cs in (2, 4, 8):
+                    ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, chunk))
+                    yield line(f"exchange 2^28 f32, {chunk} B chunks",
+                               f"cluster cs={cs} {'batched (auto)' if batch == 0 else 'pieces'}", 8 * n, ms,
+                               slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
+                               item_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+                    if chunk % (16 * cs) == 0:
+                        ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, chunk))
+                        yield line(f"all-to-all 2^28 f32, {chunk} B chunks",
+                                   f"cluster a2a cs={cs} {'batched (auto)' if batch == 0 else 'pieces'}", 8 * n, ms,
+                                   slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
+                                   item_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, 0)
         # loader and pusher lanes with smaller pieces (ring depths that 2 and 4 divide)
         for piece_kib, cps in ((4, 2), (2, 2), (8, 1)):
             for lanes in (1, 2, 4):
@@ -1089,7 +1106,7 @@ def sweep(which: str, args):
 # ----------------------------------------------------------------------------- profiling cases
 
 PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
-                 "a2a4", "a2a16", "masked")
+                 "a2a4", "a2a16", "exchange4_256B", "masked")
 
 
 def profile_case(name: str, args):
@@ -1115,6 +1132,7 @@ def profile_case(name: str, args):
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
         "exchange16": lambda: ap.ap_cluster_exchange_ex(x[:n], y[:n], n, 16, 32768, 1),
         "a2a4": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 4, 32768),
+        "exchange4_256B": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 256),
         "a2a16": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 16, 32768),
         "roll_tensor": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "masked": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),

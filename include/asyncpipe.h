@@ -156,6 +156,9 @@ ap_status ap_poly(const float* in, float* out, int64_t n, const float* coeffs, i
  *  cluster_size  1, 2, 4 or 8 (AP_ERR_CLUSTER otherwise).
  *  chunk_bytes   multiple of 16, >= 16; two chunks per ring stage must fit in
  *                shared memory (AP_ERR_SMEM otherwise, about 113 KiB max).
+ *                Chunks under 8 KiB move in batches: one tensor-map box gathers
+ *                a rank's chunk from several consecutive groups (chunks of at
+ *                most 256 floats or a multiple of 256).
  */
 ap_status ap_cluster_exchange(const float* in, float* out, int64_t n, int cluster_size,
                               int64_t chunk_bytes, cudaStream_t stream);

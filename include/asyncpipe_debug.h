@@ -66,6 +66,11 @@ typedef enum ap_debug_key {
     AP_DBG_EXCHANGE_LANES = 15, /* cluster exchange: threads that load and threads that push, 1, 2
                                    or 4 each, lane l taking items l, l + lanes, ... (reduced to a
                                    divisor of the ring depth); 0 = automatic */
+    AP_DBG_EXCHANGE_BATCH = 16, /* cluster exchange, batched form (one tensor-map box gathers a rank's
+                                   chunk, or sub-block, from several consecutive groups): 0 automatic
+                                   (sub-blocks under 8 KiB), 1 never, 2..256 groups per item (rounded
+                                   so an item is whole 128-byte units); applies where a sub-block is at
+                                   most 256 floats or a multiple of 256 */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar

@@ -45,6 +45,7 @@ def reset_debug(ap):
         ap.AP_DBG_EXCHANGE_GROUP,
         ap.AP_DBG_STRICT_ALIGN,
         ap.AP_DBG_EXCHANGE_LANES,
+        ap.AP_DBG_EXCHANGE_BATCH,
     ):
         ap.ap_debug_set(key, 0)
 

@@ -182,6 +182,9 @@ def test_debug_settings_roundtrip(ap):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, bad) == ap.AP_ERR_ARG
     for good in (1, 2, 4, 0):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, good) == ap.AP_OK
+    assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, 257) == ap.AP_ERR_ARG
+    for good in (1, 2, 256, 0):
+        assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, good) == ap.AP_OK
     for good in (1, 2, 4, 8, 0):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, good) == ap.AP_OK
 

@@ -96,3 +96,26 @@ def test_all_to_all_full_size(ap, orc, cs):
     ap.ap_cluster_all_to_all(x, y, n, cs, 32768)
     assert ap.ap_check() == ap.AP_OK
     assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), cs, 32768), f"full all-to-all cs={cs}")
+
+
+@pytest.mark.parametrize("batch", [0, 1, 8, 32])
+@pytest.mark.parametrize("cs", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("sub_bytes,groups", [(16, 3), (16, 700), (48, 51), (256, 129), (1024, 33), (2048, 12)])
+def test_all_to_all_batched(ap, orc, cs, sub_bytes, groups, batch):
+    """The batched all-to-all: one box gathers a rank's sub-block j from
+    `batch` consecutive groups and lands as sub-block r of rank j's chunks."""
+    dev = device()
+    chunk_bytes = cs * sub_bytes
+    n = groups * cs * chunk_bytes // 4
+    x = synth.uniform_pm1_torch(n + 5 * cs, n, dev)
+    want = orc.cluster_all_to_all(to_np(x), cs, chunk_bytes)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, batch)
+    for grid in (0, cs):
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        if batch == 1:
+            assert not ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4
+        assert_bits(to_np(out.view), want, f"batched a2a cs={cs} sub={sub_bytes} groups={groups} batch={batch}")
+        assert out.intact()

@@ -74,3 +74,32 @@ def test_exchange_full_size(ap, orc, cs):
         ap.ap_cluster_exchange(x, y, n, cs, 32768)
         assert ap.ap_check() == ap.AP_OK
         assert_bits(to_np(y), want, f"full exchange cs={cs} store={store}")
+
+
+@pytest.mark.parametrize("batch", [0, 1, 2, 8, 64, 256])
+@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+@pytest.mark.parametrize("chunk_bytes,groups", [(16, 1), (16, 1000), (48, 37), (256, 513), (1024, 300), (4096, 77),
+                                                (2064, 9)])
+def test_exchange_batched(ap, orc, cs, chunk_bytes, groups, batch):
+    """The batched form: one tensor-map box gathers a rank's chunk from
+    `batch` consecutive groups (0: automatic for chunks under 8 KiB, 1: never),
+    and the last, partial batch is clipped at the tensor's edge."""
+    dev = device()
+    n = groups * cs * chunk_bytes // 4
+    x = synth.uniform_pm1_torch(n + 3 * cs, n, dev)
+    want = orc.cluster_exchange(to_np(x), cs, chunk_bytes)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, batch)
+    for grid in (0, cs):
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_exchange(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        batched = bool(ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4)
+        eligible = chunk_bytes // 4 <= 256 or chunk_bytes // 4 % 256 == 0
+        if batch == 1 or not eligible:
+            assert not batched
+        elif batch >= 2 or chunk_bytes < 8192:
+            assert batched
+        assert_bits(to_np(out.view), want,
+                    f"batched exchange cs={cs} chunk={chunk_bytes} groups={groups} batch={batch} grid={grid}")
+        assert out.intact()

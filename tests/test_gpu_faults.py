@@ -88,6 +88,25 @@ def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group, lanes):
     assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), 4, 4096), "all-to-all after recovery")
 
 
+def test_batched_exchange_wait_times_out_and_recovers(ap, orc):
+    """The batched form's bounded waits (its loader barrier never completes)."""
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n = 4 * 256 * 64 // 4
+    x = synth.uniform_pm1_torch(6, n, dev)
+    y = torch.empty_like(x)
+    _inject(ap)
+    ap.ap_cluster_exchange(x, y, n, 4, 256)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    reset_debug(ap)
+    ap.ap_cluster_exchange(x, y, n, 4, 256)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4
+    assert_bits(to_np(y), orc.cluster_exchange(to_np(x), 4, 256), "batched exchange after recovery")
+
+
 def test_bad_arguments_raise(ap):
     import torch
 
