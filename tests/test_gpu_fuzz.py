@@ -1,7 +1,10 @@
 """Randomised parity of the ring and the cluster exchange against the oracle:
 random sizes, 4-byte offsets of input and output, ring depths, stage sizes,
 grid caps, CTAs per SM and consumer-warp counts, bit for bit, with sentinels
-around every output."""
+around every output. AP_FUZZ_SEEDS (default 3) sets how many seeds each test
+runs, for longer stress runs."""
+
+import os
 
 import numpy as np
 import pytest
@@ -10,6 +13,8 @@ import synth
 from gpu_util import Guarded, assert_bits, device, lib, reset_debug, to_np
 
 pytestmark = pytest.mark.gpu
+
+SEEDS = range(int(os.environ.get("AP_FUZZ_SEEDS", "3")))
 
 
 @pytest.fixture
@@ -81,7 +86,7 @@ def _run_op(ap, orc, rng, op, src, out, x, n, stages):
     return want
 
 
-@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("seed", SEEDS)
 def test_exchange_fuzz(ap, orc, seed):
     dev = device()
     rng = np.random.default_rng(2000 + seed)
@@ -97,10 +102,46 @@ def test_exchange_fuzz(ap, orc, seed):
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, int(rng.choice([0, 1, 2])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, int(rng.choice([0, 0, 1, 2, 8, 100])))
         out = Guarded(n, 0, dev)
         ap.ap_cluster_exchange(x, out.view, n, cs, chunk)
         what = f"seed={seed} case={case} cs={cs} chunk={chunk} groups={groups}"
         assert ap.ap_check() == ap.AP_OK, what
         assert_bits(to_np(out.view), orc.cluster_exchange(to_np(x), cs, chunk), what)
+        assert out.intact(), what
+        reset_debug(ap)
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_all_to_all_fuzz(ap, orc, seed):
+    """Random cluster sizes 1-16, sub-block sizes, group counts and every
+    exchange setting (receiver form, warps per piece, lanes, batch, pieces,
+    grid, CTAs per SM) against the oracle."""
+    dev = device()
+    rng = np.random.default_rng(3000 + seed)
+    for case in range(25):
+        cs = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16]))
+        sub = 16 * int(rng.integers(1, 257))
+        chunk = cs * sub
+        groups = int(rng.integers(1, 60))
+        n = groups * cs * chunk // 4
+        x = synth.uniform_pm1_torch(seed * 1000 + case, n, dev)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, int(rng.choice([0, 0, 512, 2048, 8192])))
+        ap.ap_debug_set(ap.AP_DBG_GRID, int(rng.choice([0, 0, cs, 2 * cs])))
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, int(rng.choice([0, 1, 2])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, int(rng.choice([0, 0, 1, 2, 8, 100])))
+        out = Guarded(n, 0, dev)
+        what = f"seed={seed} case={case} cs={cs} sub={sub} groups={groups}"
+        try:
+            ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk)
+        except ap.APError as e:  # a shape the settings cannot fit in shared memory
+            assert e.status == ap.AP_ERR_SMEM, what
+            reset_debug(ap)
+            continue
+        assert ap.ap_check() == ap.AP_OK, what
+        assert_bits(to_np(out.view), orc.cluster_all_to_all(to_np(x), cs, chunk), what)
         assert out.intact(), what
         reset_debug(ap)
