@@ -326,10 +326,11 @@ __global__ void __launch_bounds__(kExThreads, 1) exchange_kernel(const __grid_co
                 }
             }
         }
-    } else if (P.tma_store) {
-        // Receiver, TMA-store form: one thread registers, waits and hands each
-        // received piece to the bulk-copy engine (shared -> global); a slot is
-        // credited back once the engine has finished reading it.
+    } else if (kBatched || P.tma_store) {
+        // Receiver, TMA-store form (always, in the batched form): one thread
+        // registers, waits and hands each received piece to the bulk-copy
+        // engine (shared -> global); a slot is credited back once the engine
+        // has finished reading it.
         if (warp == 2 && lane == 0) {
             const uint32_t credit0 = ptx::mapa(credit(0), src_rank);
             const int lag = S > 2 ? 2 : S - 1;  // bulk stores left reading before a slot is credited
