@@ -150,7 +150,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
 
 
 def _addr(buf) -> int | None:
-    """Device address of a tensor (checked: float32, CUDA, contiguous) or an int."""
+    """Device-accessible address of a tensor (checked: float32, contiguous, on
+    the GPU or in pinned host memory, which the GPU reads and writes over the
+    host link) or an int."""
     if buf is None:
         return None
     if isinstance(buf, int):
@@ -160,8 +162,8 @@ def _addr(buf) -> int | None:
 
         if buf.dtype != torch.float32:
             raise TypeError("libasyncpipe works on float32 tensors")
-        if not buf.is_cuda:
-            raise TypeError("libasyncpipe needs CUDA tensors (device memory)")
+        if not buf.is_cuda and not buf.is_pinned():
+            raise TypeError("libasyncpipe needs CUDA tensors or pinned host tensors")
         if not buf.is_contiguous():
             raise TypeError("libasyncpipe needs contiguous tensors")
         return buf.data_ptr()

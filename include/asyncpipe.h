@@ -13,8 +13,11 @@
  * and compute instead of overlapping them.
  *
  * Conventions shared by every call:
- *  - Pointers named in/out/A/B are DEVICE pointers to float32 data owned by
- *    the caller. They must be 4-byte aligned (AP_ERR_ALIGN otherwise). Any
+ *  - Pointers named in/out/A/B point to float32 data owned by the caller that
+ *    the device can access: device memory, or pinned host memory mapped into
+ *    the device's address space (as cudaHostAlloc memory is under unified
+ *    addressing), which the kernels then read and write over the host link.
+ *    They must be 4-byte aligned (AP_ERR_ALIGN otherwise). Any
  *    other misalignment is not an error: the bulk path needs 16-byte aligned
  *    addresses, so the few elements before the first and after the last
  *    16-byte boundary of a buffer are fetched with 4-byte cp.async.ca and one

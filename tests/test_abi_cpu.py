@@ -286,3 +286,15 @@ def test_emulated_tensor_ring_large_line_view(ap, orc):
         y = np.full(rows * cols, np.nan, dtype=np.float32)
         assert ap.ap_debug_emulate_ring_tensor(A.ravel(), y, rows, cols, shift, 1, se) == ap.AP_OK
         assert np.array_equal(y.reshape(rows, cols).view(np.uint32), orc.row_roll(A, shift).view(np.uint32))
+
+
+def test_binding_refuses_pageable_host_tensors(ap):
+    """The binding passes CUDA tensors and pinned host tensors; an ordinary
+    (pageable) host tensor is refused before any library call."""
+    import torch
+
+    x = torch.zeros(256)
+    with pytest.raises(TypeError):
+        ap.ap_scale(x, x, 1, 256, 2.0, 2)
+    with pytest.raises(TypeError):
+        ap.ap_scale(torch.zeros(256, dtype=torch.float64), x, 1, 256, 2.0, 2)
