@@ -82,6 +82,7 @@ EXPORTED = (
     "ap_debug_emulate_ring",
     "ap_debug_emulate_ring_tensor",
     "ap_debug_fma_probe",
+    "ap_debug_fma_probe_horner",
     "ap_debug_scale_pages_async",
 )
 
@@ -137,12 +138,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.ap_debug_get.restype = _i64
     lib.ap_debug_emulate_ring.argtypes = [vp, vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _i64]
     lib.ap_debug_fma_probe.argtypes = [vp, _i64, _i64, vp]
+    lib.ap_debug_fma_probe_horner.argtypes = [vp, _i64, _i64, vp]
     lib.ap_debug_scale_pages_async.argtypes = [vp, vp, _i64, _i64, ctypes.c_float, vp]
     lib.ap_debug_emulate_ring_tensor.argtypes = [vp, vp, _i64, _i64, _i64, _i64, _i64]
     for name in ("ap_scale", "ap_scale_sync", "ap_row_roll", "ap_poly", "ap_cluster_exchange",
                  "ap_cluster_exchange_ex", "ap_cluster_all_to_all", "ap_masked_copy", "ap_autotune", "ap_autotune_reset", "ap_check",
                  "ap_debug_set", "ap_debug_emulate_ring", "ap_debug_emulate_ring_tensor", "ap_debug_fma_probe",
-                 "ap_debug_scale_pages_async"):
+                 "ap_debug_fma_probe_horner", "ap_debug_scale_pages_async"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -290,6 +292,11 @@ def ap_debug_emulate_ring_tensor(in_host, out_host, rows: int, cols: int, shift:
 
 def ap_debug_fma_probe(out, out_elems: int, iters: int, stream=None):
     _check(load().ap_debug_fma_probe(_addr(out), out_elems, iters, _stream(stream)), "ap_debug_fma_probe")
+
+
+def ap_debug_fma_probe_horner(out, out_elems: int, iters: int, stream=None):
+    _check(load().ap_debug_fma_probe_horner(_addr(out), out_elems, iters, _stream(stream)),
+           "ap_debug_fma_probe_horner")
 
 
 def ap_debug_scale_pages_async(inp, out, n_tiles: int, tile_elems: int, alpha: float, stream=None):

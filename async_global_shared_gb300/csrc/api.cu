@@ -537,6 +537,16 @@ ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaS
     return launch_fma_probe(di, out, out_elems, iters, stream);
 }
 
+ap_status ap_debug_fma_probe_horner(float* out, int64_t out_elems, int64_t iters, cudaStream_t stream) {
+    if (out == nullptr) return AP_ERR_NULL;
+    if (out_elems < 1 || iters < 1 || iters > (int64_t(1) << 20)) return AP_ERR_SHAPE;
+    if (!aligned4(out)) return AP_ERR_ALIGN;
+    DeviceInfo di;
+    const ap_status st = current_device(&di);
+    if (st != AP_OK) return st;
+    return launch_fma_probe_horner(di, out, out_elems, iters, stream);
+}
+
 }  // extern "C"
 
 namespace {

@@ -112,6 +112,8 @@ ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, 
                              const signed char* codes, int stages, cudaStream_t stream);
 
 ap_status launch_fma_probe(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
+ap_status launch_fma_probe_horner(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters,
+                                  cudaStream_t stream);
 
 // `groups` whole groups of cs chunks starting at in/out; rank r receives
 // rank (r + shift) mod cs, or with a2a every rank sends sub-block j of its

@@ -69,6 +69,7 @@ struct OpScaleDev {
 struct OpPolyDev {
     static constexpr int kGroups = 8;
     int degree;
+    int six_groups;  // 1: 16 consumer warps take six groups (24 chains) a round
     float c[AP_POLY_MAX_DEGREE + 1];
     __device__ __forceinline__ void stage(float* cs, int tid, int nthreads) const {
         for (int k = tid; k <= degree; k += nthreads) cs[k] = c[k];
@@ -235,8 +236,16 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         float4* dst = reinterpret_cast<float4*>(out + d.e_al);
         int64_t q = ct;
         // 17 warps (16 consumers + producer) leave at most 96 registers a
-        // thread, too few for 32 chains: 16 chains there.
+        // thread, too few for 32 chains: 16 chains there, or 24 (six groups)
+        // where the op asks for them (a polynomial of degree 64 or more whose
+        // stages are whole rounds of six groups a thread: 1.5-2.5 % faster;
+        // the 16-chain loop stays faster at low degree and for a six-plus-two
+        // split). The choice is the host's: a per-stage test here cost the
+        // low-degree loop 2 %.
         constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
+        if constexpr (kConsumers >= 512 && Op::kGroups > 4) {
+            if (P.op.six_groups) vec_groups<6, kConsumers>(P, src, dst, q, ngroups, cs);
+        }
         vec_groups<kG, kConsumers>(P, src, dst, q, ngroups, cs);
         if (kG > 4) vec_groups<4, kConsumers>(P, src, dst, q, ngroups, cs);
         vec_groups<2, kConsumers>(P, src, dst, q, ngroups, cs);
@@ -617,6 +626,7 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
             P.schedule = static_cast<uint32_t>(o.schedule);
             P.op.degree = op.degree;
+            P.op.six_groups = op.degree >= 64 && warps == 16 && (se / 4) % (6 * 32 * 16) == 0 ? 1 : 0;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }

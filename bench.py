@@ -530,6 +530,23 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
         ms = out[f"poly K={K}, 2^30, S=2"]["ms"]
         out[f"poly K={K}, 2^30, S=2"]["fp32_tflops"] = round(2.0 * K * (1 << 30) / (ms * 1e-3) / 1e12, 2)
     del xp, yp
+    # The FP32 roofs under the same clocks: register-only fma chains, and the
+    # operand pattern of the Horner loop (a coefficient read from shared memory
+    # as the third operand), which is what a run-time polynomial can reach.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    probe = torch.empty(sms * 1024, dtype=torch.float32, device=dev)
+    roofs = {}
+    for key, fn, fma in (("fp32 fma probe, registers only", ap.ap_debug_fma_probe, sms * 1024 * 32 * (1 << 14)),
+                         ("fp32 fma probe, Horner operands", ap.ap_debug_fma_probe_horner,
+                          sms * 512 * 24 * 128 * (1 << 10))):
+        iters = 1 << 14 if fn is ap.ap_debug_fma_probe else 1 << 10
+        ms = time_steps(lambda: fn(probe, probe.numel(), iters, stream), 20, 3, stream) / 20
+        roofs[key] = 2.0 * fma / (ms * 1e-3) / 1e12
+        out[key] = {"fp32_tflops": round(roofs[key], 2), "ms": round(ms, 4)}
+    del probe
+    k128 = out["poly K=128, 2^30, S=2"]
+    k128["frac_of_register_probe"] = round(k128["fp32_tflops"] / roofs["fp32 fma probe, registers only"], 4)
+    k128["frac_of_horner_probe"] = round(k128["fp32_tflops"] / roofs["fp32 fma probe, Horner operands"], 4)
     st = ap.ap_check()
     if st != 0:
         raise RuntimeError(f"device status {ap.ap_status_string(st)}")
@@ -1141,7 +1158,7 @@ def profile_case(name: str, args):
         "scale": lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, 2),
         "sync": lambda: ap.ap_scale_sync(x[:n], y[:n], n // 256, 256, 2.0),
         "poly32": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 3),
-        "poly128": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(128).tolist(), 128, 3),
+        "poly128": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(128).tolist(), 128, 2),
         "roll": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "roll_mis": lambda: ap.ap_row_roll(x[1:n + 1], y[:n], n // 4, 4, 1),
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),

@@ -107,6 +107,18 @@ ap_status ap_debug_scale_pages_async(const float* in, float* out, int64_t n_tile
 ap_status ap_debug_fma_probe(float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
 
 /*
+ * As ap_debug_fma_probe, in the operand pattern of ap_poly's Horner loop:
+ * 24 chains a thread, each step fmaf(p_t, x_t, c_k) with a distinct x_t per
+ * chain and the coefficient c_k read from shared memory four at a time, 128
+ * steps per iteration. One CTA of 512 threads per SM; the number of threads
+ * launched is min(out_elems, SMs * 512) rounded down to whole CTAs, each
+ * running iters * 128 * 24 fmaf and writing one float to out[thread]. iters
+ * at most 2^20 (else AP_ERR_SHAPE). The rate it reaches is the compute roof
+ * of a polynomial whose coefficients are only known at run time.
+ */
+ap_status ap_debug_fma_probe_horner(float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);
+
+/*
  * Host emulation of one ring call's data movement, for checking the
  * kernel's index arithmetic without a GPU. It runs the same tile planning
  * code the kernel runs (stage ranges, bulk spans, cp.async edges, shared

@@ -37,6 +37,30 @@ def test_poly_small(ap, orc, degree, stages):
         assert out.intact()
 
 
+@pytest.mark.parametrize("degree", [63, 64, 127, 128, 200])
+def test_poly_six_group_rounds(ap, orc, degree):
+    """Stages that are whole rounds of six 16-byte groups per consumer thread
+    (16 consumer warps: 48 KiB and 96 KiB) take 24 Horner chains a thread
+    from degree 64 on; five whole stages and a ragged sixth, element by
+    element."""
+    dev = device()
+    c = synth.coeffs_np(degree)
+    for stage_bytes in (0, 48 * 1024, 96 * 1024):
+        per = (stage_bytes or 96 * 1024) // 4
+        n = 5 * per + 1234
+        x = synth.uniform_pm1_torch(n + degree + 7, n, dev)
+        want = orc.poly(to_np(x), c)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        for grid in (0, 2):
+            ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+            out = Guarded(n, 0, dev)
+            ap.ap_poly(x, out.view, n, c.tolist(), degree, 2)
+            assert ap.ap_check() == ap.AP_OK
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS) == per
+            assert_bits(to_np(out.view), want, f"poly K={degree} stage={stage_bytes} grid={grid}")
+            assert out.intact()
+
+
 @pytest.mark.parametrize("degree", [0, 3, 8, 128])
 def test_poly_tensor_map_producer(ap, orc, degree):
     """Horner over the tensor-map producer's boxes, ragged lengths."""
@@ -104,3 +128,25 @@ def test_poly_full_size_sweep_sampled(ap, orc):
             ap.ap_poly(x, y, n, c.tolist(), degree, stages)
             assert ap.ap_check() == ap.AP_OK
             assert_bits(to_np(y[idx]), want, f"full poly K={degree} S={stages}")
+
+
+def test_fma_probes_cover_their_threads(ap):
+    """Both FP32 probes write one finite float per launched thread (whole
+    CTAs of 512, at most 1024 a SM for the register-only form and 512 for the
+    Horner form) and nothing past them; bad sizes are refused."""
+    import torch
+
+    dev = device()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for fn, per_sm in ((ap.ap_debug_fma_probe, 1024), (ap.ap_debug_fma_probe_horner, 512)):
+        for elems in (sms * 1024 + 7, 3 * 512 + 100):
+            out = torch.full((elems,), float("nan"), dtype=torch.float32, device=dev)
+            fn(out, elems, 8)
+            assert ap.ap_check() == ap.AP_OK
+            launched = min(elems, sms * per_sm) // 512 * 512
+            o = to_np(out)
+            assert np.isfinite(o[:launched]).all(), fn.__name__
+            assert np.isnan(o[launched:]).all(), fn.__name__
+        for elems, iters in ((100, 8), (512, 0)):
+            with pytest.raises(ap.APError):
+                fn(out, elems, iters)
