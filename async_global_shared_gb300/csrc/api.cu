@@ -452,7 +452,7 @@ ap_status ap_debug_set(int key, int64_t value) {
             g_ex_tma_store = value;
             return AP_OK;
         case AP_DBG_CACHE_HINTS:
-            if (value > 3) return AP_ERR_ARG;
+            if (value > 1) return AP_ERR_ARG;  // bit 1 (streaming stores) was measured and removed
             g_cache_hints = value;
             return AP_OK;
         case AP_DBG_DEVICE_CHECKS:

@@ -123,18 +123,11 @@ struct RingParams {
     uint64_t timeout_ns;
     uint32_t* status;
     uint32_t coef_off;  // byte offset of the op's staged data in dynamic shared memory
-    uint32_t hints;     // bit 0: loads marked L2 evict-first; bit 1: streaming (.cs) stores
+    uint32_t hints;     // bit 0: loads marked L2 evict-first
     uint32_t schedule;  // 0: CTA b takes stages b, b + grid, ...; 1: a contiguous run of stages
     Op op;
 };
 
-__device__ __forceinline__ void store4(float4* p, float4 v, uint32_t hints) {
-    if (hints & 2u) {
-        __stcs(p, v);
-    } else {
-        *p = v;
-    }
-}
 
 __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off) {
     return *reinterpret_cast<const float*>(slot + off);
@@ -158,9 +151,38 @@ __device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4
         P.op.apply(v, cs);
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            store4(&dst[q + u * kConsumers], make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]),
-                   P.hints);
+            dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
     }
+}
+
+// Relatively misaligned stage: output group q takes floats kSkip .. kSkip + 3
+// of the aligned 16-byte words q and q + 1 of the slot, U groups a round.
+template <int U, int kSkip, int kConsumers, class Op>
+__device__ __forceinline__ void shifted_groups(const RingParams<Op>& P, const float4* w, float4* dst, int64_t& q,
+                                               int64_t ngroups, const float* cs) {
+    for (; q + (U - 1) * kConsumers < ngroups; q += U * kConsumers) {
+        float v[4 * U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float4 a = w[q + u * kConsumers];
+            const float4 b = w[q + u * kConsumers + 1];
+            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) v[4 * u + t] = f[kSkip + t];
+        }
+        P.op.apply(v, cs);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            dst[q + u * kConsumers] = make_float4(v[4 * u + 0], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    }
+}
+
+template <int kSkip, int kConsumers, class Op>
+__device__ __forceinline__ void shifted_stage(const RingParams<Op>& P, const float4* w, float4* dst, int64_t ngroups,
+                                              const float* cs, int ct) {
+    int64_t q = ct;
+    shifted_groups<4, kSkip, kConsumers>(P, w, dst, q, ngroups, cs);
+    shifted_groups<1, kSkip, kConsumers>(P, w, dst, q, ngroups, cs);
 }
 
 // ---------------------------------------------------------------- checked build
@@ -253,22 +275,36 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
     } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
         // 16-byte shared loads per group (bank-conflict free) instead of four
-        // 4-byte loads that conflict four ways across the warp.
+        // 4-byte loads that conflict four ways across the warp. Copy and
+        // scale take four groups a round with the shift a compile-time
+        // constant (2-3 % faster than one group a round). The polynomial
+        // keeps one group a round: the larger loop changed the register
+        // allocation of its whole kernel and cost the aligned loop 2-4 % at
+        // degree 32.
         const uint32_t sh = o0 & 15u;
-        const unsigned char* wbase = slot + (o0 - sh);
-        for (int64_t q = ct; q < ngroups; q += kConsumers) {
-            const float4 a = *reinterpret_cast<const float4*>(wbase + 16 * q);
-            const float4 b = *reinterpret_cast<const float4*>(wbase + 16 * q + 16);
-            float v[4];
-            if (sh == 4) {
-                v[0] = a.y, v[1] = a.z, v[2] = a.w, v[3] = b.x;
-            } else if (sh == 8) {
-                v[0] = a.z, v[1] = a.w, v[2] = b.x, v[3] = b.y;
-            } else {
-                v[0] = a.w, v[1] = b.x, v[2] = b.y, v[3] = b.z;
+        const float4* w = reinterpret_cast<const float4*>(slot + (o0 - sh));
+        float4* dst = reinterpret_cast<float4*>(out + d.e_al);
+        if constexpr (Op::kGroups > 4) {
+            for (int64_t q = ct; q < ngroups; q += kConsumers) {
+                const float4 a = w[q];
+                const float4 b = w[q + 1];
+                float v[4];
+                if (sh == 4) {
+                    v[0] = a.y, v[1] = a.z, v[2] = a.w, v[3] = b.x;
+                } else if (sh == 8) {
+                    v[0] = a.z, v[1] = a.w, v[2] = b.x, v[3] = b.y;
+                } else {
+                    v[0] = a.w, v[1] = b.x, v[2] = b.y, v[3] = b.z;
+                }
+                P.op.apply(v, cs);
+                dst[q] = make_float4(v[0], v[1], v[2], v[3]);
             }
-            P.op.apply(v, cs);
-            store4(reinterpret_cast<float4*>(out + d.e_al + 4 * q), make_float4(v[0], v[1], v[2], v[3]), P.hints);
+        } else if (sh == 4) {
+            shifted_stage<1, kConsumers>(P, w, dst, ngroups, cs, ct);
+        } else if (sh == 8) {
+            shifted_stage<2, kConsumers>(P, w, dst, ngroups, cs, ct);
+        } else {
+            shifted_stage<3, kConsumers>(P, w, dst, ngroups, cs, ct);
         }
     } else {
         for (int64_t q = ct; q < ngroups; q += kConsumers) {

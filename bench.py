@@ -688,7 +688,7 @@ def sweep(which: str, args):
                 yield line("scale 2^28 f32", f"ring S={S} schedule={sched} stage={kib or 'auto'}KiB ctas/SM={cps or 'auto'}",
                            8 * n, v[2], min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
         if "hints" in groups:
-            reps = {h: [] for h in (0, 1, 2, 3)}
+            reps = {h: [] for h in (0, 1)}
             for _ in range(5):
                 for h in reps:
                     ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, h)

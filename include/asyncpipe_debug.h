@@ -42,8 +42,9 @@ typedef enum ap_debug_key {
     AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
                                    piece to a shared->global bulk copy, 2 receiver warps with 16-byte
                                    stores (AP_DBG_EXCHANGE_GROUP warps per piece) */
-    AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: bit 0 bulk loads carry an L2 evict-first policy,
-                                   bit 1 consumer stores are streaming (st.global.cs); 0 = none */
+    AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: 1 = bulk loads carry an L2 evict-first policy,
+                                   0 = none; any other value is AP_ERR_ARG (streaming consumer
+                                   stores, once bit 1, gained nothing and were removed) */
     AP_DBG_DEVICE_CHECKS = 11,  /* 1: ring kernels verify, before every stage, that each copy and each
                                    shared/global range they touch lies inside the caller's buffers and
                                    the stage slot; a violation makes ap_check report AP_ERR_SHAPE (site

@@ -182,9 +182,9 @@ def test_device_generator_matches_host(ap):
     assert_bits(got, synth.uniform_pm1_np(synth.SEED_POLY, n)[idx], "device generator")
 
 
-@pytest.mark.parametrize("hints", [1, 2, 3])
+@pytest.mark.parametrize("hints", [1])
 def test_scale_cache_hints(ap, orc, hints):
-    """L2 evict-first loads and streaming stores change no result."""
+    """L2 evict-first loads change no result."""
     import torch
 
     dev = device()
