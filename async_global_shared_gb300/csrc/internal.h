@@ -80,7 +80,7 @@ struct RingShape {
     int64_t ctas_per_sm;
     int64_t consumer_warps;
 };
-RingShape auto_ring_shape(OpKind kind, int stages);
+RingShape auto_ring_shape(OpKind kind, int stages, int degree);
 
 // Shapes installed by ap_autotune, per device, operation and ring depth;
 // they take the place of auto_ring_shape's defaults.

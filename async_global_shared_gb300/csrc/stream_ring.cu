@@ -533,18 +533,27 @@ int64_t stage_elems_for(int64_t payload_bytes, int64_t unit) {
     return se / 4 * 4;
 }
 
-RingShape auto_ring_shape(OpKind kind, int stages) {
+RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // Measured on GB300 (2^28-float scale and 2^30-float polynomial, medians of
     // interleaved repetitions): data movement peaks with about 64-96 KiB of
     // ring per SM in 16-24 KiB stages for depths 2-4; larger rings lose
-    // bandwidth. The fma-heavy polynomial wants 16 consumer warps and the
+    // bandwidth. The polynomial runs 16 consumer warps. Up to degree 16 it is
+    // HBM-bound and, like the plain stream, prefers a ring of about 128 KiB
+    // (64 KiB stages at depth 2, 32 KiB at 3-6). Above, the fma work wants the
     // largest stages that fit, since every stage costs each consumer warp a
-    // barrier wait, a descriptor read and a release; in multiples of 32 KiB
-    // (512 consumers x 16 chains x 4 bytes), so that every chain of every
-    // thread is busy for the whole stage.
+    // barrier wait, a descriptor read and a release: 96 KiB at depth 2, 64 KiB
+    // at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples of 16 KiB (512 consumers
+    // x 8 floats) so that every thread takes whole pairs of groups. Degree 32:
+    // 0.98 / 0.97 / 0.88 / 0.81 of the copy at depths 2 / 3 / 4 / 6; degree 8:
+    // 1.0 / 1.02 / 0.94 / 0.92.
     if (kind == OP_POLY) {
-        const int64_t per = (196 * 1024) / stages / (32 * 1024) * (32 * 1024);
-        return RingShape{std::min<int64_t>(96 * 1024, per), 1, 16};
+        if (degree <= 16) return RingShape{stages == 2 ? 64 * 1024 : 32 * 1024, 1, 16};
+        switch (stages) {
+            case 2: return RingShape{96 * 1024, 1, 16};
+            case 3: return RingShape{64 * 1024, 1, 16};
+            case 4: return RingShape{48 * 1024, 1, 16};
+            default: return RingShape{32 * 1024, 1, 16};
+        }
     }
     switch (stages) {
         case 2: return RingShape{16 * 1024, 2, 8};
@@ -580,7 +589,7 @@ void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeo
 ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n, int64_t off,
                       int64_t unit, int stages, const OpArgs& op, bool tensor, cudaStream_t stream) {
     RingShape shape;
-    if (tensor || !tuned_shape(di.device, op.kind, stages, &shape)) shape = auto_ring_shape(op.kind, stages);
+    if (tensor || !tuned_shape(di.device, op.kind, stages, &shape)) shape = auto_ring_shape(op.kind, stages, op.kind == OP_POLY ? op.degree : 0);
     const int64_t payload = o.stage_bytes > 0 ? o.stage_bytes : shape.payload;
     const int64_t cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : shape.ctas_per_sm;
     const int64_t warps = o.consumer_warps > 0 ? o.consumer_warps : shape.consumer_warps;
