@@ -541,11 +541,13 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     // Automatic: fixed neighbour for chunks under 8 KiB, items of 8 KiB; the
     // all-to-all for sub-blocks under 4 KiB (at 4 KiB plain pieces already run
     // at the copy's rate), items sized for a ring of min(16, 2 cs) slots.
-    auto plan_batch = [&](int64_t bud) -> int64_t {
+    // tight: items sized for a ring of cs slots instead of about 2 cs
+    auto plan_batch = [&](int64_t bud, bool tight) -> int64_t {
         if (o.ex_batch == 1 || (o.ex_batch < 2 && sub >= (a2a ? 4096 : 8192)) || !(sub_e <= 256 || sub_e % 256 == 0) ||
             groups >= (int64_t(1) << 31) || tensor_map_encoder() == nullptr)
             return 0;
-        const int64_t item_target = a2a ? std::min<int64_t>(8192, bud / (2 * std::min<int64_t>(16, 2 * cs))) : 8192;
+        const int64_t ring = tight ? cs : std::min<int64_t>(16, 2 * cs);
+        const int64_t item_target = a2a ? std::min<int64_t>(8192, bud / (2 * ring)) : 8192;
         int64_t m = 128;  // smallest batch step keeping batch * sub a multiple of 128
         while (m > 1 && (sub * (m / 2)) % 128 == 0) m /= 2;
         int64_t b = o.ex_batch >= 2 ? o.ex_batch : std::max<int64_t>(1, item_target / sub);
@@ -555,13 +557,20 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
         while (b > m && 2 * min_slots * b * sub > bud) b -= m;
         return (b >= 2 && 2 * min_slots * b * sub <= bud) ? b : 0;
     };
-    int64_t batch = plan_batch(budget);
-    if (batch == 0 && a2a && o.ctas_per_sm == 0 && plan_batch(kSmemPerSM - 1024 - 512) > 0) {
+    int64_t batch = plan_batch(budget, false);
+    if (batch == 0 && a2a && cs >= 8) {
+        // Large clusters: a ring of cs slots still leaves room for batches at
+        // two CTAs per SM (8 CTAs, 16 KiB chunks: 0.96 of the copy against
+        // 0.85 at one CTA per SM); where the usual ring fits a batch it is
+        // faster (smaller chunks lost 1-5 % with cs slots).
+        batch = plan_batch(budget, true);
+    }
+    if (batch == 0 && a2a && o.ctas_per_sm == 0 && plan_batch(kSmemPerSM - 1024 - 512, false) > 0) {
         // Large clusters with small sub-blocks: one CTA per SM leaves room for
         // batches (16 CTAs, 32 KiB chunks: 0.79 of the copy against 0.68 as
         // 2 KiB pieces at two CTAs per SM).
         budget = std::min<int64_t>(di.smem_optin, kSmemPerSM - 1024) - 512;
-        batch = plan_batch(budget);
+        batch = plan_batch(budget, false);
     }
     int64_t work = groups;  // what the clusters walk: groups, or batches of groups
     if (batch > 0) {
