@@ -545,8 +545,11 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples of 16 KiB (512 consumers
     // x 8 floats) so that every thread takes whole pairs of groups. Degree 32:
     // 0.98 / 0.97 / 0.88 / 0.81 of the copy at depths 2 / 3 / 4 / 6; degree 8:
-    // 1.0 / 1.02 / 0.94 / 0.92.
+    // 1.0 / 1.02 / 1.01 / 0.92. The best stage size is jagged between
+    // neighbouring degrees (ap_autotune finds it for one workload); these
+    // bands are the measured compromise.
     if (kind == OP_POLY) {
+        if (degree <= 8 && stages == 4) return RingShape{24 * 1024, 1, 16};  // 0.98-1.01 against 0.94-0.96
         if (degree <= 16) return RingShape{stages == 2 ? 64 * 1024 : 32 * 1024, 1, 16};
         switch (stages) {
             case 2: return RingShape{96 * 1024, 1, 16};
