@@ -58,6 +58,8 @@ def hbm_peak() -> tuple[float, str]:
     return FALLBACK_HBM_GBS, "fallback"
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (~8 TB/s)
+
 RING_SOURCES = ["stream_ring.cu", "stream_plan.h", "ptx.cuh", "device_common.cuh"]
 
 
@@ -69,19 +71,29 @@ def ring_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(profile: str) -> float | None:
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (the summary records the source hash)."""
+def _profiled(profile: str, pattern: str) -> float | None:
+    """A figure from a committed ncu summary, if the summary was taken on the
+    current kernel source (it records the source hash)."""
     p = os.path.join(ROOT, "profiles", profile)
     try:
         text = open(p).read()
     except OSError:
         return None
     m_hash = re.search(r"^source_hash:\s*(\w+)", text, re.M)
-    m_tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    if not m_hash or not m_tr or m_hash.group(1) != ring_source_hash():
+    m_val = re.search(pattern, text, re.M)
+    if not m_hash or not m_val or m_hash.group(1) != ring_source_hash():
         return None
-    return float(m_tr.group(1))
+    return float(m_val.group(1))
+
+
+def profiled_traffic(profile: str) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary (see _profiled)."""
+    return _profiled(profile, r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)")
+
+
+def profiled_dram_pct(profile: str) -> float | None:
+    """ncu's gpu__dram_throughput (% of its DRAM peak) for the same launch."""
+    return _profiled(profile, r"^\s*gpu__dram_throughput\s+([0-9.]+)\s*%")
 
 
 class ClockSampler:
@@ -423,6 +435,11 @@ def bench_scale(args, d: Dist) -> dict:
             "frac": round(achieved / peak, 4),
             "peak_kind": f"{peak_kind} copy bandwidth",
             "traffic": profiled_traffic("ring_scale_2p28.txt"),
+            # the other two denominators: the nominal HBM3e figure, and ncu's own
+            # DRAM peak for the full-size launch (from the same capture as traffic)
+            "nominal_peak": NOMINAL_HBM_GBS,
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "ncu_dram_pct_of_peak": profiled_dram_pct("ring_scale_2p28.txt"),
             "kernel": "ring_kernel<OpScaleDev>",
             "algorithmic_bytes_per_launch": nbytes,
         },
