@@ -85,11 +85,13 @@ def test_poly_automatic_stage_sizes(ap, orc):
 
 @pytest.mark.parametrize("degree", [0, 3, 8, 128])
 def test_poly_tensor_map_producer(ap, orc, degree):
-    """Horner over the tensor-map producer's boxes, ragged lengths."""
+    """Horner over the tensor-map producer's boxes, ragged lengths; three whole
+    automatic stages and a ragged fourth at depth 2 (degree 128: 96 KiB stages
+    in rounds of six groups, 24 chains a thread)."""
     dev = device()
     c = synth.coeffs_np(degree)
     ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
-    for n, stages in ((1, 2), (7, 3), (256, 4), (20011, 2), (20011, 6), (1 << 18, 3)):
+    for n, stages in ((1, 2), (7, 3), (256, 4), (20011, 2), (20011, 6), (1 << 18, 3), (3 * 24576 + 17, 2)):
         x = synth.uniform_pm1_torch(n + degree, n, dev)
         out = Guarded(n, 0, dev)
         ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
