@@ -128,7 +128,6 @@ struct RingParams {
     Op op;
 };
 
-
 __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off) {
     return *reinterpret_cast<const float*>(slot + off);
 }
@@ -237,7 +236,7 @@ __device__ __forceinline__ bool consumer_desc_ok(const StreamGeom& g, const Slot
     if (d.mode == MODE_VEC) {
         if (o0 % 16 || o0 + 16 * ngroups > g.slot_bytes) return false;
     } else if (d.mode == MODE_SHIFTED) {
-        if (o0 % 4 == 0 && o0 % 16 == 0) return false;
+        if (o0 % 4 != 0 || o0 % 16 == 0) return false;  // 4, 8 or 12 bytes off the 16-byte grid
         if ((o0 & ~15ull) + 16 * ngroups + 16 > g.slot_bytes) return false;
     }
     const uint64_t L = static_cast<uint64_t>(d.hi - d.lo);
