@@ -583,16 +583,24 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
                                                                                                  // taken[], group_bad[]
     if (smem > di.smem_optin) return AP_ERR_SMEM;
 
-    // Receiver form, unless set: measured on GB300 (2^28 floats, 32 KiB chunks).
-    // Fixed neighbour (one sender, pieces arrive in order): all eight warps on
-    // every piece for clusters of up to 8 (0.97-1.01 of the copy, against
-    // 0.87-0.92 with one warp per piece), one warp per piece for 16 (0.85
-    // against 0.76). All-to-all (pieces from every sender, in no fixed order,
-    // so in-order draining waits on the slowest sender): bulk stores for
-    // clusters of 1-2 (1.01-1.02), one warp per piece from 4 up (0.92-1.01;
-    // eight warps per piece: 0.53-0.56).
-    const bool tma_store = batch > 0 || o.ex_tma_store == 1 || (o.ex_tma_store == 0 && a2a && cs <= 2);
-    const int64_t rgroup = o.ex_group > 0 ? o.ex_group : (!a2a && cs <= 8 ? kExConsumerWarps : 1);
+    // Receiver form, unless set: measured on GB300 (2^28 floats, 32 KiB chunks;
+    // 8-64 KiB for clusters of 4 and 8). Fixed neighbour (one sender, pieces
+    // arrive in order): all eight warps on every piece for clusters of 1-2
+    // (1.01 of the copy; bulk stores 0.96-1.0), bulk stores for 3-5 and 8
+    // (0.97-1.0 and 0.99, against 0.95-0.99 and 0.95-0.96 with eight warps),
+    // four warps per piece for 6-7 (0.96, against 0.87-0.94 either other
+    // way), one warp per piece from 9 (16: 0.85, against 0.76). All-to-all
+    // (pieces from every sender, in no fixed order, so in-order draining waits
+    // on the slowest sender): bulk stores for clusters of 1-2 (1.01-1.02), one
+    // warp per piece from 4 up (0.92-1.01; eight warps per piece: 0.53-0.56).
+    const bool fixed_bulk = !a2a && (cs == 3 || cs == 4 || cs == 5 || cs == 8);
+    const bool tma_store =
+        batch > 0 || o.ex_tma_store == 1 || (o.ex_tma_store == 0 && ((a2a && cs <= 2) || fixed_bulk));
+    const int64_t rgroup = o.ex_group > 0        ? o.ex_group
+                           : a2a                 ? 1
+                           : (cs <= 5 || cs == 8) ? kExConsumerWarps
+                           : cs <= 7             ? 4
+                                                 : 1;
     if (rgroup != 1 && rgroup != 2 && rgroup != 4 && rgroup != 8) return AP_ERR_ARG;
     // Loader and pusher lanes, unless set: four for all-to-all pieces of 2 KiB
     // or less, where the single-thread roles' per-item latency sets the rate
