@@ -592,7 +592,7 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     // way), one warp per piece from 9 (16: 0.85, against 0.76). All-to-all
     // (pieces from every sender, in no fixed order, so in-order draining waits
     // on the slowest sender): bulk stores for clusters of 1-2 (1.01-1.02), one
-    // warp per piece from 4 up (0.92-1.01; eight warps per piece: 0.53-0.56).
+    // warp per piece from 3 up (0.91-1.01; eight warps per piece: 0.53-0.56).
     const bool fixed_bulk = !a2a && (cs == 3 || cs == 4 || cs == 5 || cs == 8);
     const bool tma_store =
         batch > 0 || o.ex_tma_store == 1 || (o.ex_tma_store == 0 && ((a2a && cs <= 2) || fixed_bulk));
