@@ -44,8 +44,8 @@ def test_ring_wait_times_out_and_recovers(ap, orc):
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "after recovery")
 
 
-@pytest.mark.parametrize("store", [1, 2])
-def test_exchange_wait_times_out_and_recovers(ap, orc, store):
+@pytest.mark.parametrize("store,group", [(1, 0), (2, 8), (2, 4), (2, 1)])
+def test_exchange_wait_times_out_and_recovers(ap, orc, store, group):
     import torch
 
     dev = device()
@@ -55,6 +55,7 @@ def test_exchange_wait_times_out_and_recovers(ap, orc, store):
     y = torch.empty_like(x)
     _inject(ap)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
     ap.ap_cluster_exchange(x, y, n, 4, 4096)
     assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
     reset_debug(ap)
