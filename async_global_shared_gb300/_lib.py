@@ -55,6 +55,7 @@ AP_DBG_EXCHANGE_GROUP = 13
 AP_DBG_STRICT_ALIGN = 14
 AP_DBG_EXCHANGE_LANES = 15
 AP_DBG_EXCHANGE_BATCH = 16
+AP_DBG_EXCHANGE_SEND_SLOTS = 17
 AP_DBG_LAST_PATH = 100
 AP_DBG_LAST_GRID = 101
 AP_DBG_LAST_STAGE_ELEMS = 102

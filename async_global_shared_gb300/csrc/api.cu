@@ -38,6 +38,7 @@ std::atomic<int64_t> g_ex_group{0};
 std::atomic<int64_t> g_strict_align{0};
 std::atomic<int64_t> g_ex_lanes{0};
 std::atomic<int64_t> g_ex_batch{0};
+std::atomic<int64_t> g_ex_send_slots{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
     g_last_flags{0}, g_last_site{0};
@@ -164,6 +165,7 @@ Options options() {
     o.strict_align = g_strict_align.load();
     o.ex_lanes = g_ex_lanes.load();
     o.ex_batch = g_ex_batch.load();
+    o.ex_send_slots = g_ex_send_slots.load();
     return o;
 }
 
@@ -479,6 +481,10 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 256) return AP_ERR_ARG;
             g_ex_batch = value;
             return AP_OK;
+        case AP_DBG_EXCHANGE_SEND_SLOTS:
+            if (value > 16 || (value & (value - 1)) != 0) return AP_ERR_ARG;  // 0, 1 or a power of two up to 16
+            g_ex_send_slots = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -502,6 +508,7 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_STRICT_ALIGN: return o.strict_align;
         case AP_DBG_EXCHANGE_LANES: return o.ex_lanes;
         case AP_DBG_EXCHANGE_BATCH: return o.ex_batch;
+        case AP_DBG_EXCHANGE_SEND_SLOTS: return o.ex_send_slots;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();

@@ -26,6 +26,7 @@ enum WaitSite : uint32_t {
     SITE_MASKED_CODE = 9,
     SITE_CHECK_PRODUCER = 10,
     SITE_CHECK_CONSUMER = 11,
+    SITE_EX_PUSHER_CREDIT = 12,
 };
 
 constexpr uint32_t kStatusTimeout = 9;  // AP_ERR_DEVICE_TIMEOUT

@@ -40,6 +40,7 @@ struct Options {
     int64_t strict_align;
     int64_t ex_lanes;
     int64_t ex_batch;
+    int64_t ex_send_slots;
 };
 
 Options options();

@@ -72,6 +72,12 @@ typedef enum ap_debug_key {
                                    (sub-blocks under 8 KiB), 1 never, 2..256 groups per item (rounded
                                    so an item is whole 128-byte units); applies where a sub-block is at
                                    most 256 floats or a multiple of 256 */
+    AP_DBG_EXCHANGE_SEND_SLOTS = 17, /* cluster exchange, split rings: 2, 4, 8 or 16 send buffers, each
+                                   freed as soon as its piece has landed, beside as many receive slots
+                                   as fit (a multiple of it, and of the cluster size in the
+                                   all-to-all; where none fits, one ring depth); 1 never split;
+                                   0 automatic (the all-to-all splits where its ring depth is a power
+                                   of two, with that many send buffers) */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar

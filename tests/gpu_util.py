@@ -43,6 +43,7 @@ def reset_debug(ap):
         ap.AP_DBG_DEVICE_CHECKS,
         ap.AP_DBG_SCHEDULE,
         ap.AP_DBG_EXCHANGE_GROUP,
+        ap.AP_DBG_EXCHANGE_SEND_SLOTS,
         ap.AP_DBG_STRICT_ALIGN,
         ap.AP_DBG_EXCHANGE_LANES,
         ap.AP_DBG_EXCHANGE_BATCH,

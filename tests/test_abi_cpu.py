@@ -187,6 +187,10 @@ def test_debug_settings_roundtrip(ap):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, good) == ap.AP_OK
     for good in (1, 2, 4, 8, 0):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, good) == ap.AP_OK
+    for bad in (3, 5, 6, 32):
+        assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, bad) == ap.AP_ERR_ARG
+    for good in (1, 2, 4, 8, 16, 0):
+        assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, good) == ap.AP_OK
     for bad in (2, 3):  # streaming stores were removed: only the evict-first load hint remains
         assert lib.ap_debug_set(ap.AP_DBG_CACHE_HINTS, bad) == ap.AP_ERR_ARG
     for good in (1, 0):

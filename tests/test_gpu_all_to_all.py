@@ -84,6 +84,32 @@ def test_all_to_all_receiver_forms(ap, orc, cs, store, group, lanes):
         assert out.intact()
 
 
+@pytest.mark.parametrize("send", [0, 1, 2, 4, 8, 16])
+@pytest.mark.parametrize("store,group,lanes", [(1, 0, 1), (2, 1, 1), (2, 2, 2), (2, 8, 4)])
+@pytest.mark.parametrize("cs", [2, 4, 8, 16])
+def test_all_to_all_split_rings(ap, orc, cs, store, group, lanes, send):
+    """Send rings of 2-16 buffers beside deeper receive rings (freed when a
+    piece lands), never split (1) and automatic (0), under every receiver
+    form, plain pieces and batches, over many groups."""
+    dev = device()
+    for sub_bytes, groups, batch, grid in ((1024, 40, 0, cs), (4096, 9, 1, 0), (256, 130, 0, 2 * cs), (2048, 33, 0, 0)):
+        chunk_bytes = cs * sub_bytes
+        n = groups * cs * chunk_bytes // 4
+        x = synth.uniform_pm1_torch(n + 11 * cs, n, dev)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, send)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, batch)
+        ap.ap_debug_set(ap.AP_DBG_GRID, grid)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), orc.cluster_all_to_all(to_np(x), cs, chunk_bytes),
+                    f"a2a cs={cs} sub={sub_bytes} groups={groups} send={send} store={store} group={group}")
+        assert out.intact()
+
+
 @pytest.mark.parametrize("cs", [2, 4, 8, 16])
 def test_all_to_all_full_size(ap, orc, cs):
     """2**28 floats in 32 KiB chunks (32768 chunks)."""

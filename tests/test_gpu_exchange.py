@@ -59,6 +59,28 @@ def test_exchange_worked_example(ap, orc):
     assert to_np(y).tolist() == [4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 0, 1, 2, 3]
 
 
+@pytest.mark.parametrize("send", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("store,group", [(1, 0), (2, 8), (2, 1)])
+@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+def test_exchange_split_rings(ap, orc, cs, store, group, send):
+    """The fixed-neighbour hand-off with a split send ring (forced: it is
+    automatic only for the all-to-all), plain pieces and batches."""
+    dev = device()
+    for chunk_bytes, groups, batch in ((32768, 5, 0), (4096, 61, 0), (256, 700, 0), (1024, 90, 8)):
+        n = groups * cs * chunk_bytes // 4
+        x = synth.uniform_pm1_torch(n + 3 * cs, n, dev)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, send)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, batch)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_exchange(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), orc.cluster_exchange(to_np(x), cs, chunk_bytes),
+                    f"exchange cs={cs} chunk={chunk_bytes} send={send} store={store} group={group}")
+        assert out.intact()
+
+
 @pytest.mark.parametrize("cs", [2, 4, 8])
 def test_exchange_full_size(ap, orc, cs):
     """2**28 floats (1 GiB) in 32 KiB chunks: 32768 chunks, 32768/cs groups."""

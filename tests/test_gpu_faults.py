@@ -44,8 +44,9 @@ def test_ring_wait_times_out_and_recovers(ap, orc):
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "after recovery")
 
 
+@pytest.mark.parametrize("send", [1, 4])
 @pytest.mark.parametrize("store,group", [(1, 0), (2, 8), (2, 4), (2, 1)])
-def test_exchange_wait_times_out_and_recovers(ap, orc, store, group):
+def test_exchange_wait_times_out_and_recovers(ap, orc, store, group, send):
     import torch
 
     dev = device()
@@ -56,6 +57,7 @@ def test_exchange_wait_times_out_and_recovers(ap, orc, store, group):
     _inject(ap)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, send)
     ap.ap_cluster_exchange(x, y, n, 4, 4096)
     assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
     reset_debug(ap)
@@ -64,8 +66,9 @@ def test_exchange_wait_times_out_and_recovers(ap, orc, store, group):
     assert_bits(to_np(y), orc.cluster_exchange(to_np(x), 4, 4096), "exchange after recovery")
 
 
+@pytest.mark.parametrize("send", [0, 1, 4])
 @pytest.mark.parametrize("store,group,lanes", [(1, 0, 1), (2, 1, 2), (2, 4, 4)])
-def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group, lanes):
+def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group, lanes, send):
     """The all-to-all's bounded waits: no piece is ever loaded (the loader's
     barrier expects bytes that never come), so nothing is pushed between CTAs,
     every wait gives up (receiver warps of a group agree before leaving), and
@@ -81,6 +84,7 @@ def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group, lanes):
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
     ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
+    ap.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, send)
     ap.ap_cluster_all_to_all(x, y, n, 4, 4096)
     assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
     reset_debug(ap)

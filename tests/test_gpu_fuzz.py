@@ -105,6 +105,7 @@ def test_exchange_fuzz(ap, orc, seed):
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, int(rng.choice([0, 0, 1, 2, 8, 100])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, int(rng.choice([0, 0, 1, 2, 4, 8, 16])))
         out = Guarded(n, 0, dev)
         ap.ap_cluster_exchange(x, out.view, n, cs, chunk)
         what = f"seed={seed} case={case} cs={cs} chunk={chunk} groups={groups}"
@@ -135,6 +136,7 @@ def test_all_to_all_fuzz(ap, orc, seed):
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, int(rng.choice([0, 0, 1, 2, 8, 100])))
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, int(rng.choice([0, 0, 1, 2, 4, 8, 16])))
         out = Guarded(n, 0, dev)
         what = f"seed={seed} case={case} cs={cs} sub={sub} groups={groups}"
         try:
