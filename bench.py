@@ -531,7 +531,7 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     for cs in (2, 4, 8):
         put(f"cluster exchange cs={cs}, 32 KiB chunks", 8 * n,
             lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768, stream))
-    for cs in (4, 16):
+    for cs in (4, 8, 16):
         put(f"cluster all-to-all cs={cs}, 32 KiB chunks", 8 * n,
             lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768, stream))
     codes = torch.full((n // 4,), 16, dtype=torch.int8, device=dev)
@@ -1155,7 +1155,7 @@ def sweep(which: str, args):
 # ----------------------------------------------------------------------------- profiling cases
 
 PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
-                 "a2a4", "a2a16", "exchange4_256B", "masked")
+                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked")
 
 
 def profile_case(name: str, args):
@@ -1181,6 +1181,7 @@ def profile_case(name: str, args):
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
         "exchange16": lambda: ap.ap_cluster_exchange_ex(x[:n], y[:n], n, 16, 32768, 1),
         "a2a4": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 4, 32768),
+        "a2a8": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 8, 32768),
         "exchange4_256B": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 256),
         "a2a16": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 16, 32768),
         "roll_tensor": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
