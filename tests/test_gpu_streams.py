@@ -77,3 +77,17 @@ def test_many_small_calls(ap, orc):
     assert ap.ap_check() == ap.AP_OK
     assert_bits(to_np(B), orc.row_roll(to_np(A), 199), "last roll")
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "last scale")
+
+
+def test_binding_follows_torch_current_stream():
+    """Calls without a stream argument go to torch's current stream: the
+    default one, and the one a `torch.cuda.stream` block selects."""
+    import torch
+
+    from async_global_shared_gb300 import _lib
+
+    assert _lib._stream(None) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert _lib._stream(None) == side.cuda_stream
+    assert _lib._stream(None) == torch.cuda.current_stream().cuda_stream
