@@ -81,10 +81,9 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
         ptx::cp_async_commit();
     }
     load_codes(P, first + (S - 1) * stride, tid, c);
-    int64_t base = first;
-    for (int64_t t = 0; base < P.n_chunks; ++t, base += stride) {
-        const int slot = static_cast<int>(t % S);
-        const int next = static_cast<int>((t + S - 1) % S);
+    int slot = 0;  // stage t's slot, t mod S
+    for (int64_t base = first; base < P.n_chunks; base += stride, slot = slot + 1 == S ? 0 : slot + 1) {
+        const int next = slot == 0 ? S - 1 : slot - 1;  // (t + S - 1) mod S
         // acquire + commit the stage S - 1 ahead (its slot was released last iteration)
         issue_stage(P, base_addr + next * kMcStageChunks * 16u, codes + next * kMcStageChunks, base + (S - 1) * stride,
                     tid, c);

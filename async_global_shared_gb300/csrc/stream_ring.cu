@@ -77,11 +77,19 @@ struct OpPolyDev {
     }
     template <int N>
     __device__ __forceinline__ void apply(float (&v)[N], const float* cs) const {
-        float p[N];
         const float top = cs[degree];
+        if (degree == 0) {
 #pragma unroll
-        for (int t = 0; t < N; ++t) p[t] = top;
-        int k = degree - 1;
+            for (int t = 0; t < N; ++t) v[t] = top;
+            return;
+        }
+        // The first step reads c[K] straight from `top`, so no chain starts
+        // with a register copy.
+        float p[N];
+        const float c1 = cs[degree - 1];
+#pragma unroll
+        for (int t = 0; t < N; ++t) p[t] = fmaf(top, v[t], c1);
+        int k = degree - 2;
         for (; k >= 0 && ((k + 1) & 3) != 0; --k) {  // until k + 1 is a multiple of 4
             const float ck = cs[k];
 #pragma unroll
@@ -133,10 +141,10 @@ __device__ __forceinline__ float lds_f32(const unsigned char* slot, uint32_t off
 }
 
 // Groups q, q + kConsumers, ..., U at a time while U whole groups remain;
-// advances q past them.
-template <int U, int kConsumers, class Op>
-__device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4* src, float4* dst, int64_t& q,
-                                           int64_t ngroups, const float* cs) {
+// advances q past them. Idx is the index type (see consume_stage).
+template <int U, int kConsumers, class Idx, class Op>
+__device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4* src, float4* dst, Idx& q, Idx ngroups,
+                                           const float* cs) {
     for (; q + (U - 1) * kConsumers < ngroups; q += U * kConsumers) {
         float v[4 * U];
 #pragma unroll
@@ -157,8 +165,8 @@ __device__ __forceinline__ void vec_groups(const RingParams<Op>& P, const float4
 // Relatively misaligned stage: output group q takes floats kSkip .. kSkip + 3
 // of the aligned 16-byte words q and q + 1 of the slot, U groups a round.
 template <int U, int kSkip, int kConsumers, class Op>
-__device__ __forceinline__ void shifted_groups(const RingParams<Op>& P, const float4* w, float4* dst, int64_t& q,
-                                               int64_t ngroups, const float* cs) {
+__device__ __forceinline__ void shifted_groups(const RingParams<Op>& P, const float4* w, float4* dst, int& q,
+                                               int ngroups, const float* cs) {
     for (; q + (U - 1) * kConsumers < ngroups; q += U * kConsumers) {
         float v[4 * U];
 #pragma unroll
@@ -177,9 +185,9 @@ __device__ __forceinline__ void shifted_groups(const RingParams<Op>& P, const fl
 }
 
 template <int kSkip, int kConsumers, class Op>
-__device__ __forceinline__ void shifted_stage(const RingParams<Op>& P, const float4* w, float4* dst, int64_t ngroups,
+__device__ __forceinline__ void shifted_stage(const RingParams<Op>& P, const float4* w, float4* dst, int ngroups,
                                               const float* cs, int ct) {
-    int64_t q = ct;
+    int q = ct;
     shifted_groups<4, kSkip, kConsumers>(P, w, dst, q, ngroups, cs);
     shifted_groups<1, kSkip, kConsumers>(P, w, dst, q, ngroups, cs);
 }
@@ -249,13 +257,14 @@ __device__ __forceinline__ bool consumer_desc_ok(const StreamGeom& g, const Slot
 template <int kConsumers, class Op>
 __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const SlotDesc& d, const unsigned char* slot,
                                               const float* cs, int ct) {
-    const int64_t ngroups = (d.e_end - d.e_al) >> 2;
+    // A stage holds fewer than 2^31 16-byte groups (it fits in shared memory).
+    const int ngroups = static_cast<int>((d.e_end - d.e_al) >> 2);
     float* __restrict__ out = P.out;
     const uint32_t o0 = d.off0 + static_cast<uint32_t>(4 * (d.e_al - d.lo));  // input of the first group
     if (d.mode == MODE_VEC) {
         const float4* src = reinterpret_cast<const float4*>(slot + o0);
         float4* dst = reinterpret_cast<float4*>(out + d.e_al);
-        int64_t q = ct;
+        int q = ct;
         // 17 warps (16 consumers + producer) leave at most 96 registers a
         // thread, too few for 32 chains: 16 chains there, or 24 (six groups)
         // where the op asks for them (a polynomial of degree 64 or more whose
@@ -263,14 +272,22 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         // the 16-chain loop stays faster at low degree and for a six-plus-two
         // split). The choice is the host's: a per-stage test here cost the
         // low-degree loop 2 %.
+        // Group indices are 32-bit, except in the 24-chain rounds: measured
+        // on the 2^30-float polynomial, 32-bit indices made the other rounds
+        // 1-8 % faster at degrees 8-128 but the 24-chain rounds 9 % slower
+        // (degree 128, 96 KiB stages), so those keep 64-bit ones.
         constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
         if constexpr (kConsumers >= 512 && Op::kGroups > 4) {
-            if (P.op.six_groups) vec_groups<6, kConsumers>(P, src, dst, q, ngroups, cs);
+            if (P.op.six_groups) {
+                int64_t q6 = q;
+                vec_groups<6, kConsumers, int64_t>(P, src, dst, q6, static_cast<int64_t>(ngroups), cs);
+                q = static_cast<int>(q6);
+            }
         }
-        vec_groups<kG, kConsumers>(P, src, dst, q, ngroups, cs);
-        if (kG > 4) vec_groups<4, kConsumers>(P, src, dst, q, ngroups, cs);
-        vec_groups<2, kConsumers>(P, src, dst, q, ngroups, cs);
-        vec_groups<1, kConsumers>(P, src, dst, q, ngroups, cs);
+        vec_groups<kG, kConsumers, int>(P, src, dst, q, ngroups, cs);
+        if (kG > 4) vec_groups<4, kConsumers, int>(P, src, dst, q, ngroups, cs);
+        vec_groups<2, kConsumers, int>(P, src, dst, q, ngroups, cs);
+        vec_groups<1, kConsumers, int>(P, src, dst, q, ngroups, cs);
     } else if (d.mode == MODE_SHIFTED) {
         // Input 4/8/12 bytes off the output's 16-byte grid: two aligned
         // 16-byte shared loads per group (bank-conflict free) instead of four
@@ -284,7 +301,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         const float4* w = reinterpret_cast<const float4*>(slot + (o0 - sh));
         float4* dst = reinterpret_cast<float4*>(out + d.e_al);
         if constexpr (Op::kGroups > 4) {
-            for (int64_t q = ct; q < ngroups; q += kConsumers) {
+            for (int q = ct; q < ngroups; q += kConsumers) {
                 const float4 a = w[q];
                 const float4 b = w[q + 1];
                 float v[4];
@@ -385,9 +402,9 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             if (P.g.line_h > 0) ptx::prefetch_tensormap(&P.tmap_lines);
         }
         int64_t issued = 0;
+        int s = 0;        // slot of stage `issued`: issued mod S
+        uint32_t ph = 0;  // its phase: (issued / S) mod 2
         for (int64_t j = j0; issued < count; j += step, ++issued) {
-            const int s = static_cast<int>(issued % S);
-            const uint32_t ph = static_cast<uint32_t>((issued / S) & 1);
             const int w = wait_phase<false>(empty(s), ph ^ 1u, P.timeout_ns, abort_flag);
             if (w != WAIT_OK) {
                 if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_RING_PRODUCER_EMPTY, abort_flag);
@@ -445,6 +462,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
                                   full(s));
                 }
             }
+            if (++s == S) s = 0, ph ^= 1u;
         }
         // Never leave with copies in flight: wait (bounded) for the last
         // S tiles issued. Tiles already consumed return at once.
@@ -458,10 +476,9 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
 
     // ---------------------------------------------------- consumers
     const int ct = threadIdx.x - 32;
-    int64_t i = 0;
-    for (int64_t j = j0; i < count; j += step, ++i) {
-        const int s = static_cast<int>(i % S);
-        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+    int s = 0;        // slot of stage i: i mod S
+    uint32_t ph = 0;  // its phase: (i / S) mod 2
+    for (int64_t i = 0; i < count; ++i) {
         int w = WAIT_OK;
         if (lane == 0) {
             w = wait_phase<false>(full(s), ph, P.timeout_ns, abort_flag);
@@ -478,6 +495,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
         consume_stage<kConsumers>(P, d, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty(s));
+        if (++s == S) s = 0, ph ^= 1u;
     }
 }
 
@@ -543,7 +561,7 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // barrier wait, a descriptor read and a release: 96 KiB at depth 2, 64 KiB
     // at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples of 16 KiB (512 consumers
     // x 8 floats) so that every thread takes whole pairs of groups. Degree 32:
-    // 0.98 / 0.97 / 0.88 / 0.81 of the copy at depths 2 / 3 / 4 / 6; degree 8:
+    // 0.98 / 0.99 / 0.92 / 0.875 of the copy at depths 2 / 3 / 4 / 6; degree 8:
     // 1.0 / 1.02 / 1.01 / 0.92. The best stage size is jagged between
     // neighbouring degrees (ap_autotune finds it for one workload); these
     // bands are the measured compromise.

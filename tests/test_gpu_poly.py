@@ -37,6 +37,28 @@ def test_poly_small(ap, orc, degree, stages):
         assert out.intact()
 
 
+@pytest.mark.parametrize("degree", [6, 9, 12, 13, 15, 16, 17, 31, 33, 124, 125, 126, 129, 130, 131, 132, 133, 255, 511])
+def test_poly_degree_boundaries(ap, orc, degree):
+    """Degrees on both sides of the coefficient loop's four-step words (a
+    scalar lead-in until k + 1 is a multiple of four, then four steps per
+    16-byte word with the next word loaded ahead), in rounds of 8 to 32
+    chains a thread: element by element against the oracle, under 8, 15 and
+    16 consumer warps and stages that do and do not take six groups a round."""
+    dev = device()
+    n = 3 * 96 * 1024 // 4 + 4099
+    x = synth.uniform_pm1_torch(n + degree + 11, n, dev)
+    c = synth.coeffs_np(degree)
+    want = orc.poly(to_np(x), c)
+    for stage_bytes, warps in ((0, 0), (48 * 1024, 16), (64 * 1024, 16), (32 * 1024, 8), (16 * 1024, 15)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+        out = Guarded(n, 0, dev)
+        ap.ap_poly(x, out.view, n, c.tolist(), degree, 2)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"poly K={degree} stage={stage_bytes} warps={warps}")
+        assert out.intact()
+
+
 @pytest.mark.parametrize("degree", [63, 64, 127, 128, 200])
 def test_poly_six_group_rounds(ap, orc, degree):
     """Stages that are whole rounds of six 16-byte groups per consumer thread
@@ -117,12 +139,15 @@ def test_poly_misaligned_and_edges(ap, orc, in_shift, out_shift):
 
 
 def test_poly_special_values(ap, orc):
+    """Zeros of both signs, infinities, NaN, a subnormal and a large finite
+    value; 9 * 5000 elements, so that the wide rounds (16 and 24 chains a
+    thread) see them as well as the one-group rounds and the tails."""
     import torch
 
     dev = device()
     vals = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 1e-40, 65504.0], dtype=np.float32)
-    x = torch.from_numpy(np.tile(vals, 50)).to(dev)
-    for degree in (0, 1, 3):
+    x = torch.from_numpy(np.tile(vals, 5000)).to(dev)
+    for degree in (0, 1, 3, 16, 128, 130):
         c = synth.coeffs_np(degree)
         y = torch.empty_like(x)
         ap.ap_poly(x, y, x.numel(), c.tolist(), degree, 2)
