@@ -564,9 +564,13 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // 0.98 / 0.99 / 0.92 / 0.875 of the copy at depths 2 / 3 / 4 / 6; degree 8:
     // 1.0 / 1.02 / 1.01 / 0.92. The best stage size is jagged between
     // neighbouring degrees (ap_autotune finds it for one workload); these
-    // bands are the measured compromise.
+    // bands are the measured compromise. Degrees 4-8 at depths 5-6 take
+    // 16 KiB stages with 8 consumer warps (16 values a thread per stage
+    // instead of 8): 0.98-1.02 of the copy against 0.92-0.96; below degree 4
+    // that shape is no better at depth 6.
     if (kind == OP_POLY) {
         if (degree <= 8 && stages == 4) return RingShape{24 * 1024, 1, 16};  // 0.98-1.01 against 0.94-0.96
+        if (degree >= 4 && degree <= 8 && stages >= 5) return RingShape{16 * 1024, 1, 8};
         if (degree <= 16) return RingShape{stages == 2 ? 64 * 1024 : 32 * 1024, 1, 16};
         switch (stages) {
             case 2: return RingShape{96 * 1024, 1, 16};

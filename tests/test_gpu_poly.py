@@ -85,14 +85,15 @@ def test_poly_six_group_rounds(ap, orc, degree):
 
 def test_poly_automatic_stage_sizes(ap, orc):
     """Automatic stages: a ring of about 128 KiB up to degree 16 (24 KiB
-    stages at depth 4 up to degree 8), the largest stages that fit above
-    (96 / 64 / 48 / 32 / 32 KiB at depths 2-6)."""
+    stages at depth 4 up to degree 8, 16 KiB for degrees 4-8 at depths 5-6),
+    the largest stages that fit above (96 / 64 / 48 / 32 / 32 KiB at depths
+    2-6)."""
     dev = device()
     n = 3 * 24576 + 5
     x = synth.uniform_pm1_torch(n, n, dev)
     want_kib = {(2, False): 64, (3, False): 32, (4, False): 32, (5, False): 32, (6, False): 32,
                 (2, True): 96, (3, True): 64, (4, True): 48, (5, True): 32, (6, True): 32}
-    for degree in (0, 8, 9, 16, 17, 128):
+    for degree in (0, 3, 4, 8, 9, 16, 17, 128):
         c = synth.coeffs_np(degree)
         want = orc.poly(to_np(x), c)
         for stages in (2, 3, 4, 5, 6):
@@ -100,6 +101,8 @@ def test_poly_automatic_stage_sizes(ap, orc):
             ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
             assert ap.ap_check() == ap.AP_OK
             kib = 24 if (stages == 4 and degree <= 8) else want_kib[(stages, degree > 16)]
+            if 4 <= degree <= 8 and stages >= 5:
+                kib = 16
             assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS) == kib * 256
             assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} automatic stages")
             assert out.intact()
