@@ -268,7 +268,8 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         // 17 warps (16 consumers + producer) leave at most 96 registers a
         // thread, too few for 32 chains: 16 chains there, or 24 (six groups)
         // where the op asks for them (a polynomial of degree 64 or more whose
-        // stages are whole rounds of six groups a thread: 1.5-2.5 % faster;
+        // stages are whole rounds of six groups a thread, or of degree 32 or
+        // more whose stages are exactly one such round: 1.5-4 % faster;
         // the 16-chain loop stays faster at low degree and for a six-plus-two
         // split). The choice is the host's: a per-stage test here cost the
         // low-degree loop 2 %.
@@ -561,8 +562,8 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // barrier wait, a descriptor read and a release: 96 KiB at depth 2, 64 KiB
     // at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples of 16 KiB (512 consumers
     // x 8 floats) so that every thread takes whole pairs of groups. Degree 32:
-    // 0.98 / 0.99 / 0.92 / 0.875 of the copy at depths 2 / 3 / 4 / 6; degree 8:
-    // 1.0 / 1.02 / 1.01 / 0.92. The best stage size is jagged between
+    // 0.99 / 0.99 / 0.95 / 0.87 of the copy at depths 2 / 3 / 4 / 6; degree 8:
+    // 1.0 / 1.02 / 1.02 / 1.02. The best stage size is jagged between
     // neighbouring degrees (ap_autotune finds it for one workload); these
     // bands are the measured compromise. Degrees 4-8 at depths 5-6 take
     // 16 KiB stages with 8 consumer warps (16 values a thread per stage
@@ -695,7 +696,13 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
             P.schedule = static_cast<uint32_t>(o.schedule);
             P.op.degree = op.degree;
-            P.op.six_groups = op.degree >= 64 && warps == 16 && (se / 4) % (6 * 32 * 16) == 0 ? 1 : 0;
+            // 24-chain rounds: from degree 64 wherever stages are whole
+            // rounds; from degree 32 only where a stage is exactly one round
+            // (48 KiB: degrees 32-48 gain 3-4 %, while two rounds of 96 KiB
+            // lose 4-11 % there).
+            const int64_t round_groups = 6 * 32 * 16;
+            const bool whole_rounds = warps == 16 && (se / 4) % round_groups == 0;
+            P.op.six_groups = whole_rounds && (op.degree >= 64 || (op.degree >= 32 && se / 4 == round_groups)) ? 1 : 0;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }

@@ -59,12 +59,12 @@ def test_poly_degree_boundaries(ap, orc, degree):
         assert out.intact()
 
 
-@pytest.mark.parametrize("degree", [63, 64, 127, 128, 200])
+@pytest.mark.parametrize("degree", [31, 32, 48, 63, 64, 127, 128, 200])
 def test_poly_six_group_rounds(ap, orc, degree):
     """Stages that are whole rounds of six 16-byte groups per consumer thread
     (16 consumer warps: 48 KiB and 96 KiB) take 24 Horner chains a thread
-    from degree 64 on; five whole stages and a ragged sixth, element by
-    element."""
+    from degree 64 on, and from degree 32 where a stage is one round (48 KiB);
+    five whole stages and a ragged sixth, element by element."""
     dev = device()
     c = synth.coeffs_np(degree)
     for stage_bytes in (0, 48 * 1024, 96 * 1024):
