@@ -30,6 +30,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -133,6 +134,7 @@ struct RingParams {
     uint32_t coef_off;  // byte offset of the op's staged data in dynamic shared memory
     uint32_t hints;     // bit 0: loads marked L2 evict-first
     uint32_t schedule;  // 0: CTA b takes stages b, b + grid, ...; 1: a contiguous run of stages
+    uint32_t groups;    // consumer groups taking alternate stages: 1, or 2 (see ring_kernel)
     Op op;
 };
 
@@ -254,7 +256,9 @@ __device__ __forceinline__ bool consumer_desc_ok(const StreamGeom& g, const Slot
     return true;
 }
 
-template <int kConsumers, class Op>
+// kConsumers threads take the stage; kRegLimited: the kernel runs 16
+// consumer warps, whose register budget caps a thread at 24 chains.
+template <int kConsumers, bool kRegLimited, class Op>
 __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const SlotDesc& d, const unsigned char* slot,
                                               const float* cs, int ct) {
     // A stage holds fewer than 2^31 16-byte groups (it fits in shared memory).
@@ -277,8 +281,8 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         // on the 2^30-float polynomial, 32-bit indices made the other rounds
         // 1-8 % faster at degrees 8-128 but the 24-chain rounds 9 % slower
         // (degree 128, 96 KiB stages), so those keep 64-bit ones.
-        constexpr int kG = kConsumers >= 512 ? 4 : Op::kGroups;
-        if constexpr (kConsumers >= 512 && Op::kGroups > 4) {
+        constexpr int kG = kRegLimited ? 4 : Op::kGroups;
+        if constexpr (kRegLimited && Op::kGroups > 4) {
             if (P.op.six_groups) {
                 int64_t q6 = q;
                 vec_groups<6, kConsumers, int64_t>(P, src, dst, q6, static_cast<int64_t>(ngroups), cs);
@@ -345,9 +349,16 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
 }
 
 // kConsumerWarps consumer warps plus one producer warp per CTA.
-template <class Op, int kConsumerWarps, bool kChecks>
+// kGroups consumer groups take alternate stages: 1, or 2 groups of 8 warps
+// for the 16-warp polynomial at even ring depths of 4 or more (chosen on the
+// host). With two, a thread takes twice the values of a stage, and one
+// group's wait and release overlap the other's fma work: degree 32 at depth
+// 4 goes from 0.95 to 1.0 of the copy; at depth 2 one group is faster.
+template <class Op, int kConsumerWarps, bool kChecks, int kGroups>
 __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(const __grid_constant__ RingParams<Op> P) {
     constexpr int kConsumers = 32 * kConsumerWarps;
+    constexpr bool kRegLimited = kConsumerWarps >= 16;
+    constexpr int groups = kGroups;
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = P.stages;
     const uint32_t slot_bytes = P.g.slot_bytes;
@@ -363,7 +374,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), kConsumerWarps);
+            ptx::mbar_init(empty(s), kConsumerWarps / groups);
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -476,10 +487,16 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     }
 
     // ---------------------------------------------------- consumers
-    const int ct = threadIdx.x - 32;
-    int s = 0;        // slot of stage i: i mod S
+    // With two groups, group g takes stages g, g + 2, ...; for an even ring
+    // depth (the host's condition) every use of a slot then falls to the
+    // same group, so each group waits on its slots' phases in order exactly
+    // as a single group does. (With an odd depth a group could see the phase
+    // of the slot's use two laps back as complete.)
+    const int grp = (warp - 1) / (kConsumerWarps / groups);
+    const int ct = threadIdx.x - 32 - grp * (kConsumers / groups);
+    int s = grp;      // slot of stage i: i mod S
     uint32_t ph = 0;  // its phase: (i / S) mod 2
-    for (int64_t i = 0; i < count; ++i) {
+    for (int64_t i = grp; i < count; i += groups) {
         int w = WAIT_OK;
         if (lane == 0) {
             w = wait_phase<false>(full(s), ph, P.timeout_ns, abort_flag);
@@ -493,21 +510,22 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
             if (lane == 0) check_fail(P.status, SITE_CHECK_CONSUMER, abort_flag);
             break;
         }
-        consume_stage<kConsumers>(P, d, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
+        consume_stage<kConsumers / groups, kRegLimited>(P, d, smem + static_cast<size_t>(s) * slot_bytes, cs, ct);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty(s));
-        if (++s == S) s = 0, ph ^= 1u;
+        s += groups;
+        if (s >= S) s -= S, ph ^= 1u;
     }
 }
 
-template <class Op, int kConsumerWarps, bool kChecks>
+template <class Op, int kConsumerWarps, bool kChecks, int kGroups = 1>
 ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t grid, int64_t smem,
                          cudaStream_t stream) {
     // Raise the kernel's dynamic shared-memory limit once per device.
     static std::atomic<int64_t> configured[64];  // limit already set on this device (setting twice is harmless)
     const int d = di.device;
     if (d < 0 || d >= 64) return AP_ERR_CUDA;
-    auto kernel = ring_kernel<Op, kConsumerWarps, kChecks>;
+    auto kernel = ring_kernel<Op, kConsumerWarps, kChecks, kGroups>;
     if (configured[d].load() < smem) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
             return AP_ERR_CUDA;
@@ -520,7 +538,12 @@ ap_status launch_ring_op(const DeviceInfo& di, const RingParams<Op>& P, int64_t 
 template <class Op, bool kChecks>
 ap_status launch_ring_checks(const DeviceInfo& di, int64_t warps, const RingParams<Op>& P, int64_t grid, int64_t smem,
                              cudaStream_t stream) {
-    if (warps == 16) return launch_ring_op<Op, 16, kChecks>(di, P, grid, smem, stream);
+    if (warps == 16) {
+        if constexpr (std::is_same<Op, OpPolyDev>::value) {
+            if (P.groups == 2) return launch_ring_op<Op, 16, kChecks, 2>(di, P, grid, smem, stream);
+        }
+        return launch_ring_op<Op, 16, kChecks>(di, P, grid, smem, stream);
+    }
     if (warps == 15) return launch_ring_op<Op, 15, kChecks>(di, P, grid, smem, stream);
     return launch_ring_op<Op, 8, kChecks>(di, P, grid, smem, stream);
 }
@@ -562,7 +585,7 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // barrier wait, a descriptor read and a release: 96 KiB at depth 2, 64 KiB
     // at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples of 16 KiB (512 consumers
     // x 8 floats) so that every thread takes whole pairs of groups. Degree 32:
-    // 0.99 / 0.99 / 0.95 / 0.87 of the copy at depths 2 / 3 / 4 / 6; degree 8:
+    // 0.99 / 0.99 / 1.0 / 0.89 of the copy at depths 2 / 3 / 4 / 6; degree 8:
     // 1.0 / 1.02 / 1.02 / 1.02. The best stage size is jagged between
     // neighbouring degrees (ap_autotune finds it for one workload); these
     // bands are the measured compromise. Degrees 4-8 at depths 5-6 take
@@ -607,6 +630,7 @@ void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeo
     P.coef_off = static_cast<uint32_t>(coef_off);
     P.hints = hints;
     P.schedule = 0;
+    P.groups = 1;
 }
 
 }  // namespace
@@ -700,7 +724,8 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             // rounds; from degree 32 only where a stage is exactly one round
             // (48 KiB: degrees 32-48 gain 3-4 %, while two rounds of 96 KiB
             // lose 4-11 % there).
-            const int64_t round_groups = 6 * 32 * 16;
+            P.groups = warps == 16 && stages % 2 == 0 && stages >= 4 ? 2 : 1;
+            const int64_t round_groups = 6 * 32 * 16 / P.groups;
             const bool whole_rounds = warps == 16 && (se / 4) % round_groups == 0;
             P.op.six_groups = whole_rounds && (op.degree >= 64 || (op.degree >= 32 && se / 4 == round_groups)) ? 1 : 0;
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;

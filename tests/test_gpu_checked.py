@@ -83,7 +83,9 @@ def test_checked_scale_and_poly_full_size(ap, orc):
         assert ap.ap_check() == ap.AP_OK
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "checked scale")
     c = synth.coeffs_np(32)
-    ap.ap_poly(x, y, n, c.tolist(), 32, 3)
-    assert ap.ap_check() == ap.AP_OK
     idx = np.random.default_rng(0).integers(0, n, 1 << 16)
-    assert_bits(to_np(y)[idx], orc.poly(to_np(x)[idx], c), "checked poly (sampled)")
+    for stages in (3, 4):  # one consumer group, then two groups taking alternate stages
+        y.zero_()
+        ap.ap_poly(x, y, n, c.tolist(), 32, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(y)[idx], orc.poly(to_np(x)[idx], c), f"checked poly S={stages} (sampled)")

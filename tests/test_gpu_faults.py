@@ -44,6 +44,30 @@ def test_ring_wait_times_out_and_recovers(ap, orc):
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "after recovery")
 
 
+@pytest.mark.parametrize("stages", [3, 4])
+def test_poly_wait_times_out_and_recovers(ap, orc, stages):
+    """The polynomial's 16 consumer warps, as one group (depth 3) and as two
+    groups taking alternate stages (depth 4)."""
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n = 64 * 8192
+    x = synth.uniform_pm1_torch(5, n, dev)
+    y = torch.empty_like(x)
+    c = synth.coeffs_np(32)
+    _inject(ap)
+    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 16 * 1024)
+    ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 16)
+    ap.ap_poly(x, y, n, c.tolist(), 32, stages)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    assert ap.ap_check() == ap.AP_OK
+    reset_debug(ap)
+    ap.ap_poly(x, y, n, c.tolist(), 32, stages)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y), orc.poly(to_np(x), c), f"poly S={stages} after recovery")
+
+
 @pytest.mark.parametrize("send", [1, 4])
 @pytest.mark.parametrize("store,group", [(1, 0), (2, 8), (2, 4), (2, 1)])
 def test_exchange_wait_times_out_and_recovers(ap, orc, store, group, send):

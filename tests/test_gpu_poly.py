@@ -59,6 +59,31 @@ def test_poly_degree_boundaries(ap, orc, degree):
         assert out.intact()
 
 
+@pytest.mark.parametrize("stages", [4, 6])
+@pytest.mark.parametrize("degree", [7, 9, 32, 64, 128])
+def test_poly_two_consumer_groups(ap, orc, degree, stages):
+    """16 consumer warps at even depths of 4 or more split into two groups of
+    8 that take alternate stages (group g: stages g, g + 2, ...). Two CTAs
+    of about 20 stages each run many laps of the ring, with an odd stage
+    count on one CTA and a ragged last stage; element by element."""
+    dev = device()
+    c = synth.coeffs_np(degree)
+    for stage_bytes in (32 * 1024, 16 * 1024):
+        per = stage_bytes // 4
+        n = 41 * per + 1237
+        x = synth.uniform_pm1_torch(n + degree + 3, n, dev)
+        want = orc.poly(to_np(x), c)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_GRID, 2)
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 16)
+        out = Guarded(n, 0, dev)
+        ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert ap.ap_debug_get(ap.AP_DBG_LAST_GRID) == 2
+        assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} stage={stage_bytes} two groups")
+        assert out.intact()
+
+
 @pytest.mark.parametrize("degree", [31, 32, 48, 63, 64, 127, 128, 200])
 def test_poly_six_group_rounds(ap, orc, degree):
     """Stages that are whole rounds of six 16-byte groups per consumer thread
