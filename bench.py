@@ -1154,7 +1154,7 @@ def sweep(which: str, args):
 
 # ----------------------------------------------------------------------------- profiling cases
 
-PROFILE_CASES = ("scale", "sync", "poly32", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
+PROFILE_CASES = ("scale", "sync", "poly32", "poly32_s4", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
                  "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked")
 
 
@@ -1176,6 +1176,7 @@ def profile_case(name: str, args):
         "sync": lambda: ap.ap_scale_sync(x[:n], y[:n], n // 256, 256, 2.0),
         "poly32": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 3),
         "poly128": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(128).tolist(), 128, 2),
+        "poly32_s4": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 4),
         "roll": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "roll_mis": lambda: ap.ap_row_roll(x[1:n + 1], y[:n], n // 4, 4, 1),
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
