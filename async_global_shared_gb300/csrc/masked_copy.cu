@@ -112,7 +112,10 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
 template <int S>
 ap_status launch_masked_s(const DeviceInfo& di, const McParams& P, cudaStream_t stream) {
     const int64_t stages_total = (P.n_chunks + kMcStageChunks - 1) / kMcStageChunks;
-    int64_t grid = static_cast<int64_t>(di.sms) * (S <= 3 ? 4 : 2);
+    // Two CTAs per SM at every depth: measured on 2^26 plain chunks, one CTA
+    // per SM reached 0.73 of the copy, two 0.95, three 0.86-0.92 and four (the
+    // earlier choice at depths 2-3) 0.93.
+    int64_t grid = static_cast<int64_t>(di.sms) * 2;
     if (grid > stages_total) grid = stages_total;
     if (grid < 1) grid = 1;
     const size_t smem = static_cast<size_t>(S) * kMcStageChunks * 17;  // data + one code byte per chunk
