@@ -87,3 +87,48 @@ def test_graph_of_many_small_rolls(ap, orc):
     Ah = to_np(A)
     for k, b in enumerate(bufs):
         assert_bits(to_np(b), orc.row_roll(Ah, k), f"roll by {k} in graph")
+
+
+def test_graph_of_polynomial_shapes_and_masked_copy(ap, orc):
+    """Polynomial launches of every consumer form in one graph (one group at
+    depth 3, two groups taking alternate stages at depths 4 and 6, eight
+    warps for degree 8 at depth 6) and a masked copy, replayed with new input
+    data each time."""
+    import torch
+
+    dev = device()
+    n = 1 << 20
+    x = torch.empty(n, device=dev)
+    ys = [torch.empty(n, device=dev) for _ in range(4)]
+    m = torch.empty(n, device=dev)
+    codes = torch.from_numpy(np.random.default_rng(7).integers(-2, 17, n // 4).astype(np.int8)).to(dev)
+    calls = [(32, 3), (32, 4), (128, 6), (8, 6)]
+    coeffs = {k: synth.coeffs_np(k) for k, _ in calls}
+    s = torch.cuda.Stream()
+
+    def chain():
+        for (k, stages), y in zip(calls, ys):
+            ap.ap_poly(x, y, n, coeffs[k].tolist(), k, stages, s)
+        ap.ap_masked_copy(x, m, n // 4, codes, 3, s)
+
+    with torch.cuda.stream(s):
+        x.copy_(synth.uniform_pm1_torch(11, n, dev))
+        m.zero_()
+        chain()  # warm-up outside capture
+    s.synchronize()
+    assert ap.ap_check(s) == ap.AP_OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    for rep in range(2):
+        with torch.cuda.stream(s):
+            x.copy_(synth.uniform_pm1_torch(300 + rep, n, dev))
+        s.synchronize()
+        before = to_np(m).copy()
+        g.replay()
+        s.synchronize()
+        assert ap.ap_check(s) == ap.AP_OK
+        xh = to_np(x)
+        for (k, stages), y in zip(calls, ys):
+            assert_bits(to_np(y), orc.poly(xh, coeffs[k]), f"graph poly K={k} S={stages}, replay {rep}")
+        assert_bits(to_np(m), orc.masked_copy(xh, before, to_np(codes)), f"graph masked copy, replay {rep}")
