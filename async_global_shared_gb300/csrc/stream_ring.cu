@@ -578,24 +578,50 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // Measured on GB300 (2^28-float scale and 2^30-float polynomial, medians of
     // interleaved repetitions): data movement peaks with about 64-96 KiB of
     // ring per SM in 16-24 KiB stages for depths 2-4; larger rings lose
-    // bandwidth. The polynomial runs 16 consumer warps. Up to degree 16 it is
-    // HBM-bound and, like the plain stream, prefers a ring of about 128 KiB
-    // (64 KiB stages at depth 2, 32 KiB at 3-6). Above, the fma work wants the
-    // largest stages that fit, since every stage costs each consumer warp a
-    // barrier wait, a descriptor read and a release: 96 KiB at depth 2, 64 KiB
-    // at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples of 16 KiB (512 consumers
-    // x 8 floats) so that every thread takes whole pairs of groups. Degree 32:
-    // 0.99 / 0.99 / 1.0 / 0.89 of the copy at depths 2 / 3 / 4 / 6; degree 8:
-    // 1.0 / 1.02 / 1.02 / 1.02. The best stage size is jagged between
-    // neighbouring degrees (ap_autotune finds it for one workload); these
-    // bands are the measured compromise. Degrees 4-8 at depths 5-6 take
-    // 16 KiB stages with 8 consumer warps (16 values a thread per stage
-    // instead of 8): 0.98-1.02 of the copy against 0.92-0.96; below degree 4
-    // that shape is no better at depth 6.
+    // bandwidth. The polynomial runs 16 consumer warps unless stated. Up to
+    // degree 8 it is HBM-bound and, like the plain stream, prefers a ring of
+    // about 128 KiB (64 KiB stages at depth 2, 32 KiB at 3-6). Above degree 24
+    // the fma work wants the largest stages that fit, since every stage costs
+    // each consumer warp a barrier wait, a descriptor read and a release:
+    // 96 KiB at depth 2, 64 KiB at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples
+    // of 16 KiB (512 consumers x 8 floats) so that every thread takes whole
+    // pairs of groups. Degree 32: 0.99 / 0.99 / 1.0 / 0.89 of the copy at
+    // depths 2 / 3 / 4 / 6; degree 8: 1.0 / 1.02 / 1.02 / 1.02. Degrees 9-24
+    // are still HBM-bound but carry enough fma work that neither family of
+    // shapes holds: there the bands below are the per-band best of a sweep of every degree 9-24 at
+    // depths 2-6 over 16-32 KiB stages and 8 or 16 warps (2^30 floats; the
+    // former 32-64 KiB defaults ran 0.90-0.97 of the copy in the cells that
+    // changed, these run 0.91-1.03; degrees 11 and 13 at depth 6 lose 1 %). The best stage
+    // size stays jagged between neighbouring degrees (ap_autotune finds it for
+    // one workload). Degrees 4-10 at depths 5-6 take 16 KiB stages with 8
+    // consumer warps (16 values a thread per stage instead of 8): 0.94-1.02 of
+    // the copy against 0.92-0.96; below degree 4 that shape is no better at
+    // depth 6.
     if (kind == OP_POLY) {
         if (degree <= 8 && stages == 4) return RingShape{24 * 1024, 1, 16};  // 0.98-1.01 against 0.94-0.96
-        if (degree >= 4 && degree <= 8 && stages >= 5) return RingShape{16 * 1024, 1, 8};
-        if (degree <= 16) return RingShape{stages == 2 ? 64 * 1024 : 32 * 1024, 1, 16};
+        if (degree >= 4 && degree <= 10 && stages >= 5) return RingShape{16 * 1024, 1, 8};
+        if (degree <= 8) return RingShape{stages == 2 ? 64 * 1024 : 32 * 1024, 1, 16};
+        if (degree <= 16) {
+            switch (stages) {
+                case 2: return RingShape{64 * 1024, 1, 16};
+                case 3: return RingShape{32 * 1024, 1, 16};
+                case 4: return RingShape{24 * 1024, 1, 16};
+                default: return RingShape{24 * 1024, 1, 8};
+            }
+        }
+        if (degree <= 24) {
+            switch (stages) {
+                case 2: return RingShape{96 * 1024, 1, 16};
+                case 3: return RingShape{48 * 1024, 1, 16};
+                case 4: return RingShape{32 * 1024, 1, 16};
+                case 5:
+                    if (degree <= 18) return RingShape{24 * 1024, 1, 8};
+                    return RingShape{32 * 1024, 1, degree <= 22 ? 8 : 16};
+                default:
+                    if (degree <= 20) return RingShape{24 * 1024, 1, 16};
+                    return RingShape{32 * 1024, 1, degree <= 22 ? 8 : 16};
+            }
+        }
         switch (stages) {
             case 2: return RingShape{96 * 1024, 1, 16};
             case 3: return RingShape{64 * 1024, 1, 16};

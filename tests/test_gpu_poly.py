@@ -108,26 +108,41 @@ def test_poly_six_group_rounds(ap, orc, degree):
             assert out.intact()
 
 
+def _auto_stage_kib(degree: int, stages: int) -> int:
+    """The documented automatic stage sizes of ap_poly, band by band."""
+    if degree <= 8 and stages == 4:
+        return 24
+    if 4 <= degree <= 10 and stages >= 5:
+        return 16
+    if degree <= 8:
+        return 64 if stages == 2 else 32
+    if degree <= 16:
+        return {2: 64, 3: 32}.get(stages, 24)
+    if degree <= 24:
+        if stages == 5:
+            return 24 if degree <= 18 else 32
+        if stages == 6:
+            return 24 if degree <= 20 else 32
+        return {2: 96, 3: 48, 4: 32}[stages]
+    return {2: 96, 3: 64, 4: 48}.get(stages, 32)
+
+
 def test_poly_automatic_stage_sizes(ap, orc):
-    """Automatic stages: a ring of about 128 KiB up to degree 16 (24 KiB
-    stages at depth 4 up to degree 8, 16 KiB for degrees 4-8 at depths 5-6),
-    the largest stages that fit above (96 / 64 / 48 / 32 / 32 KiB at depths
-    2-6)."""
+    """Automatic stages: a ring of about 128 KiB up to degree 8 (24 KiB
+    stages at depth 4, 16 KiB for degrees 4-10 at depths 5-6), measured bands
+    of 16-96 KiB for degrees 9-24, and the largest stages that fit above
+    (96 / 64 / 48 / 32 / 32 KiB at depths 2-6)."""
     dev = device()
     n = 3 * 24576 + 5
     x = synth.uniform_pm1_torch(n, n, dev)
-    want_kib = {(2, False): 64, (3, False): 32, (4, False): 32, (5, False): 32, (6, False): 32,
-                (2, True): 96, (3, True): 64, (4, True): 48, (5, True): 32, (6, True): 32}
-    for degree in (0, 3, 4, 8, 9, 16, 17, 128):
+    for degree in (0, 3, 4, 8, 9, 10, 11, 16, 17, 18, 19, 20, 21, 23, 24, 25, 128):
         c = synth.coeffs_np(degree)
         want = orc.poly(to_np(x), c)
         for stages in (2, 3, 4, 5, 6):
             out = Guarded(n, 0, dev)
             ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
             assert ap.ap_check() == ap.AP_OK
-            kib = 24 if (stages == 4 and degree <= 8) else want_kib[(stages, degree > 16)]
-            if 4 <= degree <= 8 and stages >= 5:
-                kib = 16
+            kib = _auto_stage_kib(degree, stages)
             assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS) == kib * 256
             assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} automatic stages")
             assert out.intact()
