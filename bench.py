@@ -119,10 +119,24 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            self._wait_for_samples()
         except OSError:
             self.proc = None
         return self
+
+    def _wait_for_samples(self, need: int = 2, limit_s: float = 10.0):
+        """Return once nvidia-smi has written `need` samples (or has exited, or
+        `limit_s` passed). Its start-up can hold the driver for most of a
+        second; a timed region that overlapped it lost that time to idle."""
+        t_end = time.monotonic() + limit_s
+        while time.monotonic() < t_end and self.proc.poll() is None:
+            try:
+                with open(self.path) as fh:
+                    if sum(1 for line in fh if line.strip()) >= need:
+                        return
+            except OSError:
+                pass
+            time.sleep(0.05)
 
     def mark_start(self):
         self.t0 = datetime.datetime.now()
