@@ -585,7 +585,8 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // each consumer warp a barrier wait, a descriptor read and a release:
     // 96 KiB at depth 2, 64 KiB at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples
     // of 16 KiB (512 consumers x 8 floats) so that every thread takes whole
-    // pairs of groups. Degree 32: 0.99 / 0.99 / 1.0 / 0.89 of the copy at
+    // pairs of groups (degrees 25-28 keep 48 KiB at depth 3 and 25-26 keep
+    // 32 KiB at depth 4: 2-9 % faster there). Degree 32: 0.99 / 0.99 / 1.0 / 0.89 of the copy at
     // depths 2 / 3 / 4 / 6; degree 8: 1.0 / 1.02 / 1.02 / 1.02. Degrees 9-24
     // are still HBM-bound but carry enough fma work that neither family of
     // shapes holds: there the bands below are the per-band best of a sweep of every degree 9-24 at
@@ -624,8 +625,8 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
         }
         switch (stages) {
             case 2: return RingShape{96 * 1024, 1, 16};
-            case 3: return RingShape{64 * 1024, 1, 16};
-            case 4: return RingShape{48 * 1024, 1, 16};
+            case 3: return RingShape{degree <= 28 ? 48 * 1024 : 64 * 1024, 1, 16};
+            case 4: return RingShape{degree <= 26 ? 32 * 1024 : 48 * 1024, 1, 16};
             default: return RingShape{32 * 1024, 1, 16};
         }
     }

@@ -124,7 +124,11 @@ def _auto_stage_kib(degree: int, stages: int) -> int:
         if stages == 6:
             return 24 if degree <= 20 else 32
         return {2: 96, 3: 48, 4: 32}[stages]
-    return {2: 96, 3: 64, 4: 48}.get(stages, 32)
+    if stages == 3:
+        return 48 if degree <= 28 else 64
+    if stages == 4:
+        return 32 if degree <= 26 else 48
+    return 96 if stages == 2 else 32
 
 
 def test_poly_automatic_stage_sizes(ap, orc):
@@ -135,7 +139,7 @@ def test_poly_automatic_stage_sizes(ap, orc):
     dev = device()
     n = 3 * 24576 + 5
     x = synth.uniform_pm1_torch(n, n, dev)
-    for degree in (0, 3, 4, 8, 9, 10, 11, 16, 17, 18, 19, 20, 21, 23, 24, 25, 128):
+    for degree in (0, 3, 4, 8, 9, 10, 11, 16, 17, 18, 19, 20, 21, 23, 24, 25, 26, 27, 28, 29, 128):
         c = synth.coeffs_np(degree)
         want = orc.poly(to_np(x), c)
         for stages in (2, 3, 4, 5, 6):
