@@ -48,14 +48,14 @@ AP_DBG_CTAS_PER_SM = 6
 AP_DBG_ROLL_STAGES = 7
 AP_DBG_CONSUMER_WARPS = 8
 AP_DBG_EXCHANGE_STORE = 9
-AP_DBG_CACHE_HINTS = 10
 AP_DBG_DEVICE_CHECKS = 11
-AP_DBG_SCHEDULE = 12
 AP_DBG_EXCHANGE_GROUP = 13
 AP_DBG_STRICT_ALIGN = 14
 AP_DBG_EXCHANGE_LANES = 15
 AP_DBG_EXCHANGE_BATCH = 16
 AP_DBG_EXCHANGE_SEND_SLOTS = 17
+AP_DBG_RING_RUN = 18
+AP_DBG_CONSUMER_GROUPS = 19
 AP_DBG_LAST_PATH = 100
 AP_DBG_LAST_GRID = 101
 AP_DBG_LAST_STAGE_ELEMS = 102
@@ -63,6 +63,10 @@ AP_DBG_LAST_SMEM = 103
 AP_DBG_LAST_STAGES = 104
 AP_DBG_LAST_FLAGS = 105
 AP_DBG_LAST_SITE = 106
+AP_DBG_LAST_RUN = 107
+AP_DBG_LAST_WARPS = 108
+AP_DBG_LAST_GROUPS = 109
+AP_DBG_LAST_CHAINS = 110
 
 # Every symbol the headers under include/ declare.
 EXPORTED = (
@@ -95,7 +99,7 @@ AP_TUNE_POLY = 3
 
 class RingShape(ctypes.Structure):
     _fields_ = [("stage_bytes", ctypes.c_int64), ("ctas_per_sm", ctypes.c_int), ("consumer_warps", ctypes.c_int),
-                ("gbs", ctypes.c_double)]
+                ("stages_per_cta", ctypes.c_int), ("consumer_groups", ctypes.c_int), ("gbs", ctypes.c_double)]
 
 
 class APError(RuntimeError):
@@ -264,7 +268,8 @@ def ap_autotune(op: int, inp, out, n: int, stages: int, degree: int = 0, stream=
     _check(load().ap_autotune(op, _addr(inp), _addr(out), n, stages, degree, ctypes.byref(shape), _stream(stream)),
            "ap_autotune")
     return {"stage_bytes": shape.stage_bytes, "ctas_per_sm": shape.ctas_per_sm,
-            "consumer_warps": shape.consumer_warps, "gbs": shape.gbs}
+            "consumer_warps": shape.consumer_warps, "stages_per_cta": shape.stages_per_cta,
+            "consumer_groups": shape.consumer_groups, "gbs": shape.gbs}
 
 
 def ap_autotune_reset():

@@ -31,17 +31,17 @@ std::atomic<int64_t> g_ctas_per_sm{0};
 std::atomic<int64_t> g_roll_stages{0};
 std::atomic<int64_t> g_consumer_warps{0};
 std::atomic<int64_t> g_ex_tma_store{0};
-std::atomic<int64_t> g_cache_hints{0};
 std::atomic<int64_t> g_device_checks{0};
-std::atomic<int64_t> g_schedule{0};
 std::atomic<int64_t> g_ex_group{0};
 std::atomic<int64_t> g_strict_align{0};
 std::atomic<int64_t> g_ex_lanes{0};
 std::atomic<int64_t> g_ex_batch{0};
 std::atomic<int64_t> g_ex_send_slots{0};
+std::atomic<int64_t> g_ring_run{0};
+std::atomic<int64_t> g_consumer_groups{0};
 
 std::atomic<int64_t> g_last_path{0}, g_last_grid{0}, g_last_stage_elems{0}, g_last_smem{0}, g_last_stages{0},
-    g_last_flags{0}, g_last_site{0};
+    g_last_flags{0}, g_last_site{0}, g_last_run{0}, g_last_warps{0}, g_last_groups{0}, g_last_chains{0};
 
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;  // 2 s
 
@@ -158,14 +158,14 @@ Options options() {
     o.roll_stages = g_roll_stages.load();
     o.consumer_warps = g_consumer_warps.load();
     o.ex_tma_store = g_ex_tma_store.load();
-    o.cache_hints = g_cache_hints.load();
     o.device_checks = g_device_checks.load();
-    o.schedule = g_schedule.load();
     o.ex_group = g_ex_group.load();
     o.strict_align = g_strict_align.load();
     o.ex_lanes = g_ex_lanes.load();
     o.ex_batch = g_ex_batch.load();
     o.ex_send_slots = g_ex_send_slots.load();
+    o.ring_run = g_ring_run.load();
+    o.consumer_groups = g_consumer_groups.load();
     return o;
 }
 
@@ -176,6 +176,14 @@ void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem
     g_last_smem = smem;
     g_last_stages = stages;
     g_last_flags = flags;
+    g_last_run = g_last_warps = g_last_groups = g_last_chains = 0;
+}
+
+void record_ring_shape(int64_t run, int64_t warps, int64_t groups, int64_t chains) {
+    g_last_run = run;
+    g_last_warps = warps;
+    g_last_groups = groups;
+    g_last_chains = chains;
 }
 
 }  // namespace ap
@@ -396,6 +404,8 @@ ap_status ap_autotune(ap_tune_op op, const float* in, float* out, int64_t n, int
     chosen->stage_bytes = best.payload;
     chosen->ctas_per_sm = static_cast<int>(best.ctas_per_sm);
     chosen->consumer_warps = static_cast<int>(best.consumer_warps);
+    chosen->stages_per_cta = static_cast<int>(best.run);
+    chosen->consumer_groups = static_cast<int>(best.groups);
     chosen->gbs = gbs;
     return AP_OK;
 }
@@ -446,24 +456,16 @@ ap_status ap_debug_set(int key, int64_t value) {
             g_roll_stages = value;
             return AP_OK;
         case AP_DBG_CONSUMER_WARPS:
-            if (value != 0 && value != 8 && value != 15 && value != 16) return AP_ERR_ARG;
+            if (value != 0 && value != 8 && value != 12 && value != 16) return AP_ERR_ARG;
             g_consumer_warps = value;
             return AP_OK;
         case AP_DBG_EXCHANGE_STORE:
             if (value > 2) return AP_ERR_ARG;
             g_ex_tma_store = value;
             return AP_OK;
-        case AP_DBG_CACHE_HINTS:
-            if (value > 1) return AP_ERR_ARG;  // bit 1 (streaming stores) was measured and removed
-            g_cache_hints = value;
-            return AP_OK;
         case AP_DBG_DEVICE_CHECKS:
             if (value > 1) return AP_ERR_ARG;
             g_device_checks = value;
-            return AP_OK;
-        case AP_DBG_SCHEDULE:
-            if (value > 1) return AP_ERR_ARG;
-            g_schedule = value;
             return AP_OK;
         case AP_DBG_EXCHANGE_GROUP:
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return AP_ERR_ARG;
@@ -485,6 +487,14 @@ ap_status ap_debug_set(int key, int64_t value) {
             if (value > 16 || (value & (value - 1)) != 0) return AP_ERR_ARG;  // 0, 1 or a power of two up to 16
             g_ex_send_slots = value;
             return AP_OK;
+        case AP_DBG_RING_RUN:
+            if (value > (int64_t(1) << 20)) return AP_ERR_ARG;
+            g_ring_run = value;
+            return AP_OK;
+        case AP_DBG_CONSUMER_GROUPS:
+            if (value > 3) return AP_ERR_ARG;
+            g_consumer_groups = value;
+            return AP_OK;
         default: return AP_ERR_ARG;
     }
 }
@@ -501,14 +511,14 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_ROLL_STAGES: return o.roll_stages;
         case AP_DBG_CONSUMER_WARPS: return o.consumer_warps;
         case AP_DBG_EXCHANGE_STORE: return o.ex_tma_store;
-        case AP_DBG_CACHE_HINTS: return o.cache_hints;
         case AP_DBG_DEVICE_CHECKS: return o.device_checks;
-        case AP_DBG_SCHEDULE: return o.schedule;
         case AP_DBG_EXCHANGE_GROUP: return o.ex_group;
         case AP_DBG_STRICT_ALIGN: return o.strict_align;
         case AP_DBG_EXCHANGE_LANES: return o.ex_lanes;
         case AP_DBG_EXCHANGE_BATCH: return o.ex_batch;
         case AP_DBG_EXCHANGE_SEND_SLOTS: return o.ex_send_slots;
+        case AP_DBG_RING_RUN: return o.ring_run;
+        case AP_DBG_CONSUMER_GROUPS: return o.consumer_groups;
         case AP_DBG_LAST_PATH: return g_last_path.load();
         case AP_DBG_LAST_GRID: return g_last_grid.load();
         case AP_DBG_LAST_STAGE_ELEMS: return g_last_stage_elems.load();
@@ -516,6 +526,10 @@ int64_t ap_debug_get(int key) {
         case AP_DBG_LAST_STAGES: return g_last_stages.load();
         case AP_DBG_LAST_FLAGS: return g_last_flags.load();
         case AP_DBG_LAST_SITE: return g_last_site.load();
+        case AP_DBG_LAST_RUN: return g_last_run.load();
+        case AP_DBG_LAST_WARPS: return g_last_warps.load();
+        case AP_DBG_LAST_GROUPS: return g_last_groups.load();
+        case AP_DBG_LAST_CHAINS: return g_last_chains.load();
         default: return -1;
     }
 }
@@ -587,11 +601,26 @@ ap_status emulate_ring(const StreamGeom& g, const float* in_host, float* out_hos
             written[dst + b] = 1;
         }
     };
+    RegularStages reg;
+    make_regular(g, &reg);
     for (int64_t j = 0; j < g.n_stages && result == AP_OK; ++j) {
         std::memset(slot, 0xA5, g.slot_bytes);
         std::memset(written, 0, g.slot_bytes);
         StagePlan sp;
         plan_stage(g, j, &sp);
+        if (j >= 1 && j < reg.end) {
+            // the producer's shortcut for a regular stage must give the same
+            // copy and descriptor as the full plan
+            SlotDesc d, full_d;
+            const uint64_t src = regular_stage(g, reg, j, &d);
+            make_slot_desc(sp, &full_d);
+            const Span& s0 = sp.span[0];
+            if (sp.nspans != 1 || s0.bulk_src != src || s0.bulk_bytes != reg.bytes || s0.bulk_dst != 0 ||
+                s0.head_end != s0.x0 || s0.tail_begin != s0.x1 || std::memcmp(&d, &full_d, sizeof(d)) != 0) {
+                fail();
+                break;
+            }
+        }
         for (int k = 0; k < sp.nspans && result == AP_OK; ++k) {
             const Span& sn = sp.span[k];
             if (g.box_bytes != 0) {

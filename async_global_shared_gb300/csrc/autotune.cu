@@ -2,8 +2,9 @@
 // FAQ: how many stages to use is a trade of latency hiding against shared
 // memory, and the sweet spot is found by profiling. ap_autotune times the
 // ring over the caller's buffers for every stage size and CTAs-per-SM count
-// that fits (the ring depth is the caller's), keeps the fastest, and installs
-// it for later calls of that operation and depth on this device.
+// that fits, under both schedules (a persistent grid, or runs of consecutive
+// stages per CTA; the ring depth is the caller's), keeps the fastest, and
+// installs it for later calls of that operation and depth on this device.
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -64,18 +65,24 @@ ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, 
     }
     double best_ms = -1.0;
     ap_status result = AP_OK;
+    // Schedules: a persistent grid of cps = 1..4 CTAs per SM, or (cps 0)
+    // runs of `runs[r]` consecutive stages per CTA.
+    const int64_t runs[3] = {stages, 2 * static_cast<int64_t>(stages), 4 * static_cast<int64_t>(stages)};
     for (int wi = 0; wi < 2 && result == AP_OK; ++wi) {
         const int warps = warp_choices[wi];
         if (kind != OP_POLY && warps != 8) continue;  // data movement: 8 consumer warps
         for (int64_t kib : kPayloadKiB) {
-            for (int64_t cps = 1; cps <= 4; ++cps) {
+            for (int64_t sched = 1; sched <= 7; ++sched) {
+                const int64_t cps = sched <= 4 ? sched : 0;
+                const int64_t run = sched <= 4 ? 0 : runs[sched - 5];
                 // the ring of one CTA, and cps of them per SM, must fit in shared memory
                 const int64_t per_cta = static_cast<int64_t>(stages) * (kib * 1024 + 176) + 16 * stages + 4096;
                 if (per_cta > di.smem_optin || cps * (per_cta + 1024) > kSmemPerSM) continue;
-                if (kind == OP_POLY && cps > 1) continue;  // 16 warps x 75 registers: one CTA per SM
+                if (kind == OP_POLY && cps > 1) continue;  // 16 warps x 92 registers: one CTA per SM
                 Options o = base;
                 o.stage_bytes = kib * 1024;
-                o.ctas_per_sm = cps;
+                o.ctas_per_sm = cps > 0 ? cps : 1;
+                o.ring_run = run > 0 ? run : 1;  // 1: the persistent grid
                 o.consumer_warps = warps;
                 ap_status st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);  // warm-up
                 if (st == AP_ERR_SMEM) continue;
@@ -97,7 +104,7 @@ ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, 
                 const double ms = ms_rep[1];
                 if (best_ms < 0.0 || ms < best_ms) {
                     best_ms = ms;
-                    *best = RingShape{kib * 1024, cps, warps};
+                    *best = RingShape{kib * 1024, cps > 0 ? cps : 1, warps, run};
                 }
             }
             if (result != AP_OK) break;

@@ -42,7 +42,7 @@ enum WaitResult : int { WAIT_OK = 0, WAIT_TIMEOUT = 1, WAIT_ABORTED = 2 };
 
 // Wait for the phase with `parity` of the CTA-local barrier `bar`. Gives up
 // with WAIT_TIMEOUT after `timeout_ns`, or with WAIT_ABORTED as soon as the
-// CTA's abort flag is set (pass nullptr to ignore the flag, as drains do).
+// CTA's abort flag is set (nullptr: ignore the flag).
 template <bool kClusterScope>
 __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                           volatile int* abort_flag) {
@@ -56,6 +56,28 @@ __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, uint64_
         if (abort_flag != nullptr && *abort_flag) return WAIT_ABORTED;
         if (ptx::globaltimer_ns() - t0 > timeout_ns) return WAIT_TIMEOUT;
     }
+}
+
+// A drain: before a kernel leaves, it waits for the copies it issued, so that
+// none is still reading or writing a CTA's shared memory when the CTA exits.
+// After an abort (a wait elsewhere gave up) the barrier of such a copy may
+// never complete: its receiver no longer consumes, or fault injection
+// inflated the bytes it expects, although the bytes themselves still land.
+// The drain then stops at once and holds the thread for a grace period far
+// longer than an issued copy takes to finish, instead of waiting out the full
+// limit for every remaining copy. Returns false when the drain should stop.
+constexpr uint64_t kDrainGraceNs = 100000;
+
+template <bool kClusterScope>
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns, uint32_t* status,
+                                           uint32_t site, volatile int* abort_flag) {
+    const int w = wait_phase<kClusterScope>(bar, parity, timeout_ns, abort_flag);
+    if (w == WAIT_OK) return true;
+    if (w == WAIT_TIMEOUT) raise_timeout(status, site, abort_flag);
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < kDrainGraceNs) {
+    }
+    return false;
 }
 
 }  // namespace ap

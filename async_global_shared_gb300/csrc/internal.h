@@ -33,14 +33,14 @@ struct Options {
     int64_t roll_stages;
     int64_t consumer_warps;
     int64_t ex_tma_store;
-    int64_t cache_hints;
     int64_t device_checks;
-    int64_t schedule;
     int64_t ex_group;
     int64_t strict_align;
     int64_t ex_lanes;
     int64_t ex_batch;
     int64_t ex_send_slots;
+    int64_t ring_run;
+    int64_t consumer_groups;
 };
 
 Options options();
@@ -51,6 +51,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // What a launcher reports about the launch it made (AP_DBG_LAST_*).
 void record_launch(int64_t path, int64_t grid, int64_t stage_elems, int64_t smem, int64_t stages, int64_t flags);
+// The ring's schedule and consumer layout for the same launch (run 0:
+// persistent grid), recorded after record_launch.
+void record_ring_shape(int64_t run, int64_t warps, int64_t groups, int64_t chains);
 
 enum Path : int64_t {
     PATH_RING = 1,
@@ -75,11 +78,17 @@ struct OpArgs {
 int64_t stage_elems_for(int64_t payload_bytes, int64_t unit);
 
 // Default ring shape for an op and ring depth: stage payload bytes, CTAs
-// per SM the grid is sized for, consumer warps per CTA.
+// per SM the grid is sized for, consumer warps per CTA, and the schedule:
+// run = 0 is a persistent grid of SMs x ctas_per_sm CTAs, CTA b taking stages
+// b, b + grid, ...; run >= 2 gives every CTA `run` consecutive stages and
+// launches as many CTAs as that takes (the hardware starts them in order as
+// earlier ones finish; ctas_per_sm is then unused).
 struct RingShape {
     int64_t payload;
     int64_t ctas_per_sm;
     int64_t consumer_warps;
+    int64_t run = 0;
+    int64_t groups = 0;  // ap_poly's consumer groups (0: the launcher's rule)
 };
 RingShape auto_ring_shape(OpKind kind, int stages, int degree);
 

@@ -94,16 +94,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// Same, with an L2 cache-policy operand (see l2_evict_first_policy).
-__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                              uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // Global -> shared copy of one 2-D box described by a tensor map (the TMA
 // engine's descriptor form): box at {c0 = column, c1 = row}; rows past the
 // tensor's end arrive as zeros. completes `box bytes` of transactions on bar.
@@ -186,13 +176,6 @@ __device__ __forceinline__ void bulk_wait_read() {
 
 // Wait until all of this thread's bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// L2 policy: lines touched once, evict them first.
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
 
 // ---------------------------------------------------------------- per-thread cp.async
 

@@ -300,4 +300,68 @@ AP_HD uint32_t smem_offset_of_output(const StagePlan& p, int64_t e) {
     return p.span[1].region + p.span[1].lead + static_cast<uint32_t>(4 * (q - p.len1));
 }
 
+// Regular stages. Every stage j in [1, end) is a whole stage of se outputs
+// whose one input span neither wraps past n nor reaches the buffer's
+// unaligned tail (its start is past the unaligned head since j >= 1). Such a
+// stage's plan is stage 1's moved by j - 1 stages: one bulk copy of `bytes`
+// from src1 + 4 se (j - 1) to slot offset 0, and a descriptor whose first
+// input sits at slot offset off0 in mode `mode` (VEC or SHIFTED). The
+// producer takes this shortcut for them instead of planning each stage from
+// the geometry (about ten instructions instead of a few hundred, which
+// matters when the consumer warps leave the producer few issue slots).
+// Bulk (not tensor-map) mode only; end = 0 when no stage qualifies.
+struct RegularStages {
+    int64_t end;     // regular stages are [1, end)
+    uint64_t src1;   // bulk source of stage 1
+    uint32_t bytes;  // bulk bytes of a regular stage
+    uint32_t off0;   // slot offset of a regular stage's first input
+    uint32_t mode;   // its consumer mode
+    uint32_t pad_;
+};
+
+AP_HD void make_regular(const StreamGeom& g, RegularStages* r) {
+    r->end = 0;
+    r->src1 = 0;
+    r->bytes = 0;
+    r->off0 = 0;
+    r->mode = MODE_VEC;
+    r->pad_ = 0;
+    if (g.box_bytes != 0 || g.n_stages < 3) return;
+    // stage j reads [lo + off, lo + off + se) with lo = out_head + j se: it
+    // is regular while lo + off + se <= min(n, t_in)
+    const int64_t lim = (g.n < g.t_in ? g.n : g.t_in) - g.out_head - g.off - g.se;
+    if (lim < g.se) return;
+    int64_t end = lim / g.se + 1;
+    if (end > g.n_stages) end = g.n_stages;
+    StagePlan sp;
+    plan_stage(g, 1, &sp);
+    const Span& sn = sp.span[0];
+    if (sp.nspans != 1 || sp.hi - sp.lo != g.se || sn.head_end != sn.x0 || sn.tail_begin != sn.x1 ||
+        sn.bulk_bytes == 0 || sn.bulk_dst != 0 || sp.e_al != sp.lo || sp.e_end != sp.hi)
+        return;
+    SlotDesc d;
+    make_slot_desc(sp, &d);
+    if (d.mode == MODE_SCALAR) return;
+    r->end = end;
+    r->src1 = sn.bulk_src;
+    r->bytes = sn.bulk_bytes;
+    r->off0 = d.off0;
+    r->mode = d.mode;
+}
+
+// The bulk source and the descriptor of regular stage j (1 <= j < r.end).
+AP_HD uint64_t regular_stage(const StreamGeom& g, const RegularStages& r, int64_t j, SlotDesc* d) {
+    const int64_t lo = g.out_head + j * g.se;
+    d->lo = lo;
+    d->hi = lo + g.se;
+    d->e_al = lo;
+    d->e_end = lo + g.se;
+    d->len1 = g.se;
+    d->off0 = r.off0;
+    d->off1 = 0;
+    d->mode = r.mode;
+    d->pad_[0] = d->pad_[1] = d->pad_[2] = 0;
+    return r.src1 + 4 * static_cast<uint64_t>(g.se) * static_cast<uint64_t>(j - 1);
+}
+
 }  // namespace ap

@@ -76,6 +76,19 @@ struct OpPolyDev {
         for (int k = tid; k <= degree; k += nthreads) cs[k] = c[k];
         if (tid < 4) cs[tid - 4] = 0.0f;
     }
+    // Four Horner steps with the coefficients of one aligned 16-byte word,
+    // highest power (q.w) first.
+    template <int N>
+    __device__ __forceinline__ static void steps4(float (&p)[N], const float (&v)[N], const float4 q) {
+#pragma unroll
+        for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.w);
+#pragma unroll
+        for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.z);
+#pragma unroll
+        for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.y);
+#pragma unroll
+        for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.x);
+    }
     template <int N>
     __device__ __forceinline__ void apply(float (&v)[N], const float* cs) const {
         const float top = cs[degree];
@@ -96,23 +109,64 @@ struct OpPolyDev {
 #pragma unroll
             for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], ck);
         }
-        // Steps k, k-1, k-2, k-3 from one aligned 16-byte word, the next word
-        // loaded one iteration ahead (the last iteration reads the four zero
-        // floats staged before c[0]).
+        // Steps k down to 0 from whole aligned 16-byte words (k + 1 is a
+        // multiple of four), each word loaded ahead of its use; a load past
+        // c[0] reads the four zero floats staged below it. The loop's shape
+        // is chosen by chain count, each form measured at degrees 32 and 128
+        // against the others (GB300, 2^30 floats): with 16 chains one word a
+        // trip; with 24, and with 32 below degree 64, two words a trip; with
+        // 32 from degree 64, the odd words one at a time and then four a
+        // trip with one exit test (0.84 -> 0.856 of the register-only fma
+        // rate at ring depth 6). The same change to another chain count cost
+        // it 1-5 %.
         if (k >= 3) {
-            float4 q = *reinterpret_cast<const float4*>(cs + k - 3);
+            const float4* w = reinterpret_cast<const float4*>(cs + k - 3);
+            const float4* const w0 = reinterpret_cast<const float4*>(cs);
+            if constexpr (N >= 32) {
+                if (degree >= 64) {
+                    for (int r = ((k + 1) >> 2) & 3; r > 0; --r) {
+                        const float4 q = *w;
+                        --w;
+                        steps4(p, v, q);
+                    }
+                    if (w >= w0) {
+                        float4 q0 = w[0];
+                        do {
+                            const float4 q1 = w[-1];
+                            steps4(p, v, q0);
+                            const float4 q2 = w[-2];
+                            steps4(p, v, q1);
+                            const float4 q3 = w[-3];
+                            steps4(p, v, q2);
+                            q0 = w[-4];
+                            steps4(p, v, q3);
+                            w -= 4;
+                        } while (w >= w0);
+                    }
+#pragma unroll
+                    for (int t = 0; t < N; ++t) v[t] = p[t];
+                    return;
+                }
+            }
+            if constexpr (N >= 24) {
+                float4 qa = w[0];
+                while (true) {
+                    const float4 qb = w[-1];
+                    steps4(p, v, qa);
+                    if (w == w0) break;
+                    qa = w[-2];
+                    steps4(p, v, qb);
+                    w -= 2;
+                    if (w < w0) break;
+                }
+            } else {
+                float4 q = *w;
 #pragma unroll 2
-            for (; k >= 3; k -= 4) {
-                const float4 next = *reinterpret_cast<const float4*>(cs + k - 7);
-#pragma unroll
-                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.w);
-#pragma unroll
-                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.z);
-#pragma unroll
-                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.y);
-#pragma unroll
-                for (int t = 0; t < N; ++t) p[t] = fmaf(p[t], v[t], q.x);
-                q = next;
+                for (; k >= 3; k -= 4) {
+                    const float4 next = *reinterpret_cast<const float4*>(cs + k - 7);
+                    steps4(p, v, q);
+                    q = next;
+                }
             }
         }
 #pragma unroll
@@ -132,9 +186,9 @@ struct RingParams {
     uint64_t timeout_ns;
     uint32_t* status;
     uint32_t coef_off;  // byte offset of the op's staged data in dynamic shared memory
-    uint32_t hints;     // bit 0: loads marked L2 evict-first
-    uint32_t schedule;  // 0: CTA b takes stages b, b + grid, ...; 1: a contiguous run of stages
     uint32_t groups;    // consumer groups taking alternate stages: 1, or 2 (see ring_kernel)
+    int64_t run;        // 0: persistent grid, CTA b takes stages b, b + grid, ...; else `run` stages a CTA
+    RegularStages reg;  // stages the producer plans by the regular-stage shortcut
     Op op;
 };
 
@@ -384,17 +438,17 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
 
     const int64_t T = P.g.n_stages;
     const int64_t G = gridDim.x;
-    // This CTA's stages: j0, j0 + step, ... (count of them).
+    // This CTA's stages: j0, j0 + step, ... (count of them). Persistent grid:
+    // b, b + G, b + 2G, ...; otherwise the run of stages [b run, b run + run).
     int64_t j0, step, count;
-    if (P.schedule == 0) {
+    if (P.run == 0) {
         j0 = blockIdx.x;
         step = G;
         count = j0 < T ? (T - j0 + G - 1) / G : 0;
     } else {
-        const int64_t per = (T + G - 1) / G;
-        j0 = static_cast<int64_t>(blockIdx.x) * per;
+        j0 = static_cast<int64_t>(blockIdx.x) * P.run;
         step = 1;
-        count = j0 < T ? (T - j0 < per ? T - j0 : per) : 0;
+        count = j0 < T ? (T - j0 < P.run ? T - j0 : P.run) : 0;
     }
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -402,7 +456,6 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
     if (warp == 0) {
         if (lane != 0) return;
         // ------------------------------------------------ producer (one thread)
-        const uint64_t l2_policy = (P.hints & 1u) ? ptx::l2_evict_first_policy() : 0;
         if (P.g.box_bytes != 0) {
             // box destinations must be 128-byte aligned: refuse (status, no copy) otherwise
             if (smem_base & 127u) {
@@ -422,6 +475,31 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
                 if (w == WAIT_TIMEOUT) raise_timeout(P.status, SITE_RING_PRODUCER_EMPTY, abort_flag);
                 break;
             }
+            const uint32_t slot = smem_base + static_cast<uint32_t>(s) * slot_bytes;
+            if (j >= 1 && j < P.reg.end) {
+                // a regular stage: one bulk copy to the slot's start
+                SlotDesc d;
+                const uint64_t src = regular_stage(P.g, P.reg, j, &d);
+                if (kChecks) {  // the shortcut must agree with the full plan
+                    StagePlan sp;
+                    plan_stage(P.g, j, &sp);
+                    SlotDesc full_d;
+                    make_slot_desc(sp, &full_d);
+                    if (!producer_plan_ok(P.g, sp) || sp.nspans != 1 || sp.span[0].bulk_src != src ||
+                        sp.span[0].bulk_bytes != P.reg.bytes || sp.span[0].bulk_dst != 0 ||
+                        sp.span[0].head_end != sp.span[0].x0 || sp.span[0].tail_begin != sp.span[0].x1 ||
+                        full_d.lo != d.lo || full_d.hi != d.hi || full_d.e_al != d.e_al || full_d.e_end != d.e_end ||
+                        full_d.len1 != d.len1 || full_d.off0 != d.off0 || full_d.mode != d.mode) {
+                        check_fail(P.status, SITE_CHECK_PRODUCER, abort_flag);
+                        break;
+                    }
+                }
+                descs[s] = d;  // published to the consumers by the arrive below
+                ptx::mbar_arrive_expect_tx(full(s), P.reg.bytes + P.tx_extra);
+                ptx::bulk_g2s(slot, reinterpret_cast<const void*>(src), P.reg.bytes, full(s));
+                if (++s == S) s = 0, ph ^= 1u;
+                continue;
+            }
             StagePlan sp;
             plan_stage(P.g, j, &sp);
             if (kChecks && !producer_plan_ok(P.g, sp)) {
@@ -429,7 +507,6 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
                 break;
             }
             make_slot_desc(sp, &descs[s]);  // published to the consumers by the arrive below
-            const uint32_t slot = smem_base + static_cast<uint32_t>(s) * slot_bytes;
             bool edges = false;
             uint32_t tx = 0;
             for (int k = 0; k < sp.nspans; ++k) {
@@ -466,22 +543,16 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 1) ring_kernel(cons
                     }
                     continue;
                 }
-                if (P.hints & 1u) {
-                    ptx::bulk_g2s_hint(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes,
-                                       full(s), l2_policy);
-                } else {
-                    ptx::bulk_g2s(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes,
-                                  full(s));
-                }
+                ptx::bulk_g2s(slot + sn.bulk_dst, reinterpret_cast<const void*>(sn.bulk_src), sn.bulk_bytes, full(s));
             }
             if (++s == S) s = 0, ph ^= 1u;
         }
         // Never leave with copies in flight: wait (bounded) for the last
         // S tiles issued. Tiles already consumed return at once.
         for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k) {
-            if (wait_phase<false>(full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1), P.timeout_ns,
-                                  nullptr) != WAIT_OK)
-                raise_timeout(P.status, SITE_RING_DRAIN, abort_flag);
+            if (!drain_wait<false>(full(static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1), P.timeout_ns,
+                                   P.status, SITE_RING_DRAIN, abort_flag))
+                break;
         }
         return;
     }
@@ -544,7 +615,13 @@ ap_status launch_ring_checks(const DeviceInfo& di, int64_t warps, const RingPara
         }
         return launch_ring_op<Op, 16, kChecks>(di, P, grid, smem, stream);
     }
-    if (warps == 15) return launch_ring_op<Op, 15, kChecks>(di, P, grid, smem, stream);
+    if (warps == 12) {
+        if constexpr (std::is_same<Op, OpPolyDev>::value) {
+            if (P.groups == 2) return launch_ring_op<Op, 12, kChecks, 2>(di, P, grid, smem, stream);
+            if (P.groups == 3) return launch_ring_op<Op, 12, kChecks, 3>(di, P, grid, smem, stream);
+        }
+        return launch_ring_op<Op, 12, kChecks>(di, P, grid, smem, stream);
+    }
     return launch_ring_op<Op, 8, kChecks>(di, P, grid, smem, stream);
 }
 
@@ -575,75 +652,65 @@ int64_t stage_elems_for(int64_t payload_bytes, int64_t unit) {
 }
 
 RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
-    // Measured on GB300 (2^28-float scale and 2^30-float polynomial, medians of
-    // interleaved repetitions): data movement peaks with about 64-96 KiB of
-    // ring per SM in 16-24 KiB stages for depths 2-4; larger rings lose
-    // bandwidth. The polynomial runs 16 consumer warps unless stated. Up to
-    // degree 8 it is HBM-bound and, like the plain stream, prefers a ring of
-    // about 128 KiB (64 KiB stages at depth 2, 32 KiB at 3-6). Above degree 24
-    // the fma work wants the largest stages that fit, since every stage costs
-    // each consumer warp a barrier wait, a descriptor read and a release:
-    // 96 KiB at depth 2, 64 KiB at 3, 48 KiB at 4 and 32 KiB at 5-6, multiples
-    // of 16 KiB (512 consumers x 8 floats) so that every thread takes whole
-    // pairs of groups (degrees 25-28 keep 48 KiB at depth 3 and 25-26 keep
-    // 32 KiB at depth 4: 2-9 % faster there). Degree 32: 0.99 / 0.99 / 1.0 / 0.89 of the copy at
-    // depths 2 / 3 / 4 / 6; degree 8: 1.0 / 1.02 / 1.02 / 1.02. Degrees 9-24
-    // are still HBM-bound but carry enough fma work that neither family of
-    // shapes holds: there the bands below are the per-band best of a sweep of every degree 9-24 at
-    // depths 2-6 over 16-32 KiB stages and 8 or 16 warps (2^30 floats; the
-    // former 32-64 KiB defaults ran 0.90-0.97 of the copy in the cells that
-    // changed, these run 0.91-1.03; degrees 11 and 13 at depth 6 lose 1 %). The best stage
-    // size stays jagged between neighbouring degrees (ap_autotune finds it for
-    // one workload). Degrees 4-10 at depths 5-6 take 16 KiB stages with 8
-    // consumer warps (16 values a thread per stage instead of 8): 0.94-1.02 of
-    // the copy against 0.92-0.96; below degree 4 that shape is no better at
-    // depth 6.
+    // Measured on GB300 (2^28-float scale and row shift, 2^30-float
+    // polynomial at degrees 0-128, every ring depth 2-6; medians of
+    // interleaved repetitions). Two schedules: a persistent grid (run 0), and
+    // runs of consecutive stages per CTA (run r), as many CTAs as that takes,
+    // which the hardware starts in index order as earlier ones finish, so the
+    // grid reads and writes one narrow window of memory at any moment. Runs
+    // win wherever the kernel is bound by memory: 1.03-1.05 of the copy
+    // against 0.96-1.0 for the persistent grid. Where the fma work bounds it,
+    // a CTA must keep its SM busy across stages and the persistent grid wins
+    // (a run's first load is exposed with one 16-warp CTA per SM).
     if (kind == OP_POLY) {
-        if (degree <= 8 && stages == 4) return RingShape{24 * 1024, 1, 16};  // 0.98-1.01 against 0.94-0.96
-        if (degree >= 4 && degree <= 10 && stages >= 5) return RingShape{16 * 1024, 1, 8};
-        if (degree <= 8) return RingShape{stages == 2 ? 64 * 1024 : 32 * 1024, 1, 16};
-        if (degree <= 16) {
-            switch (stages) {
-                case 2: return RingShape{64 * 1024, 1, 16};
-                case 3: return RingShape{32 * 1024, 1, 16};
-                case 4: return RingShape{24 * 1024, 1, 16};
-                default: return RingShape{24 * 1024, 1, 8};
-            }
-        }
-        if (degree <= 24) {
-            switch (stages) {
-                case 2: return RingShape{96 * 1024, 1, 16};
-                case 3: return RingShape{48 * 1024, 1, 16};
-                case 4: return RingShape{32 * 1024, 1, 16};
-                case 5:
-                    if (degree <= 18) return RingShape{24 * 1024, 1, 8};
-                    return RingShape{32 * 1024, 1, degree <= 22 ? 8 : 16};
-                default:
-                    if (degree <= 20) return RingShape{24 * 1024, 1, 16};
-                    return RingShape{32 * 1024, 1, degree <= 22 ? 8 : 16};
-            }
-        }
+        const int64_t r = 2 * static_cast<int64_t>(stages);  // runs: every slot filled twice
         switch (stages) {
-            case 2: return RingShape{96 * 1024, 1, 16};
-            case 3: return RingShape{degree <= 28 ? 48 * 1024 : 64 * 1024, 1, 16};
-            case 4: return RingShape{degree <= 26 ? 32 * 1024 : 48 * 1024, 1, 16};
-            default: return RingShape{32 * 1024, 1, 16};
+            case 2:
+                // degrees 0-24: 1.054 of the copy falling to 0.94 at 24 (persistent 0.93-0.97)
+                if (degree <= 24) return RingShape{64 * 1024, 1, 16, 4};
+                return RingShape{96 * 1024, 1, 16};
+            case 3:
+                // degrees 0-10: 1.06 falling to 1.0; above, persistent stages
+                // of 32-64 KiB (0.92-1.0 of the copy up to degree 32); from
+                // degree 80 one 24-chain round a stage (48 KiB: 0.852 of the
+                // register-only fma rate at degree 128, 0.839 with 64 KiB)
+                if (degree <= 10) return RingShape{32 * 1024, 1, 16, r};
+                if (degree <= 16) return RingShape{32 * 1024, 1, 16};
+                if (degree <= 28) return RingShape{48 * 1024, 1, 16};
+                if (degree < 80) return RingShape{64 * 1024, 1, 16};
+                return RingShape{48 * 1024, 1, 16};
+            case 4:
+                // degrees 0-22: 1.055 falling to 0.98 (persistent 0.95-1.0)
+                if (degree <= 22) return RingShape{32 * 1024, 1, 16, r};
+                return RingShape{degree <= 26 ? 32 * 1024 : 48 * 1024, 1, 16};
+            case 5:
+                // degrees 0-18: 1.053 falling to 1.02
+                if (degree <= 18) return RingShape{32 * 1024, 1, 16, r};
+                if (degree <= 22) return RingShape{32 * 1024, 1, 8};
+                return RingShape{32 * 1024, 1, 16};
+            default:
+                // degrees 0-10: 24 KiB runs (1.05); 11-26: 32 KiB runs (1.044
+                // falling to 0.99); from 27 the persistent grid with 12
+                // consumer warps in three groups, each taking every third
+                // stage in two rounds of 32 chains (degree 32: 0.99-1.03 of
+                // the copy; degree 128: 0.847-0.856 of the register-only fma
+                // rate, against 0.836 with 16 warps in two groups)
+                if (degree <= 10) return RingShape{24 * 1024, 1, 16, r};
+                if (degree <= 26) return RingShape{32 * 1024, 1, 16, r};
+                return RingShape{32 * 1024, 1, 12, 0, 3};
         }
     }
-    switch (stages) {
-        case 2: return RingShape{16 * 1024, 2, 8};
-        case 3: return RingShape{24 * 1024, 1, 8};
-        case 4: return RingShape{16 * 1024, 1, 8};
-        case 5: return RingShape{36 * 1024, 1, 8};
-        default: return RingShape{32 * 1024, 1, 8};
-    }
+    // Scale and row shift: runs of 2 S consecutive 16 KiB stages per CTA (each
+    // slot of the ring filled twice): 1.03-1.05 of the copy at every depth,
+    // where the persistent grid reached 0.97-1.0 (2^28 floats).
+    return RingShape{16 * 1024, 1, 8, 2 * static_cast<int64_t>(stages)};
 }
 
 namespace {
 
 template <class Op>
 void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeom& g, int stages, uint32_t tx_extra,
-                 uint64_t timeout, uint32_t* status, int64_t coef_off, uint32_t hints, const CUtensorMap& tmap,
+                 uint64_t timeout, uint32_t* status, int64_t coef_off, const CUtensorMap& tmap,
                  const CUtensorMap& tmap_lines) {
     P.tmap = tmap;
     P.tmap_lines = tmap_lines;
@@ -655,9 +722,9 @@ void fill_params(RingParams<Op>& P, const float* in, float* out, const StreamGeo
     P.timeout_ns = timeout;
     P.status = status;
     P.coef_off = static_cast<uint32_t>(coef_off);
-    P.hints = hints;
-    P.schedule = 0;
     P.groups = 1;
+    P.run = 0;
+    make_regular(g, &P.reg);
 }
 
 }  // namespace
@@ -714,8 +781,20 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     const int64_t coef_bytes = op.kind == OP_POLY ? 16 + (4 * (op.degree + 1) + 15) / 16 * 16 : 0;
     const int64_t smem = coef_off + coef_bytes;
     if (smem > di.smem_optin) return AP_ERR_SMEM;
-    int64_t grid = std::min<int64_t>(g.n_stages, static_cast<int64_t>(di.sms) * cps);
-    if (o.grid > 0) grid = std::min<int64_t>(grid, o.grid);
+    // Schedule: a persistent grid, or runs of consecutive stages (a grid cap
+    // asks for the persistent grid). Runs are lengthened where the grid would
+    // pass 2^30 CTAs.
+    int64_t run = o.ring_run == 1 ? 0 : (o.ring_run > 1 ? o.ring_run : shape.run);
+    if (o.grid > 0) run = 0;
+    int64_t grid;
+    if (run > 0) {
+        const int64_t cap = int64_t(1) << 30;
+        if ((g.n_stages + run - 1) / run > cap) run = (g.n_stages + cap - 1) / cap;
+        grid = (g.n_stages + run - 1) / run;
+    } else {
+        grid = std::min<int64_t>(g.n_stages, static_cast<int64_t>(di.sms) * cps);
+        if (o.grid > 0) grid = std::min<int64_t>(grid, o.grid);
+    }
     if (grid < 1) grid = 1;
 
     const uint64_t ia = g.in_addr, oa = g.out_addr;
@@ -724,37 +803,45 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
     if (((ia + 4 * static_cast<uint64_t>(off) - oa) & 15) != 0 || off != 0) flags |= 2;
     if (use_tensor) flags |= g.line_h > 0 ? 4 | 8 : 4;
     record_launch(PATH_RING, grid, se, smem, stages, flags);
+    record_ring_shape(run, warps, 1, 0);
 
     const uint64_t timeout = static_cast<uint64_t>(o.timeout_ns);
     const uint32_t tx_extra = static_cast<uint32_t>(o.tx_extra);
-    const uint32_t hints = static_cast<uint32_t>(o.cache_hints);
     switch (op.kind) {
         case OP_COPY: {
             RingParams<OpCopyDev> P;
-            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
-            P.schedule = static_cast<uint32_t>(o.schedule);
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, tmap, tmap_lines);
+            P.run = run;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_SCALE: {
             RingParams<OpScaleDev> P;
-            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
-            P.schedule = static_cast<uint32_t>(o.schedule);
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, tmap, tmap_lines);
+            P.run = run;
             P.op.alpha = op.alpha;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }
         case OP_POLY: {
             RingParams<OpPolyDev> P;
-            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, hints, tmap, tmap_lines);
-            P.schedule = static_cast<uint32_t>(o.schedule);
+            fill_params(P, in, out, g, stages, tx_extra, timeout, di.status, coef_off, tmap, tmap_lines);
+            P.run = run;
             P.op.degree = op.degree;
-            // 24-chain rounds: from degree 64 wherever stages are whole
-            // rounds; from degree 32 only where a stage is exactly one round
-            // (48 KiB: degrees 32-48 gain 3-4 %, while two rounds of 96 KiB
-            // lose 4-11 % there).
+            // 24-chain rounds (16 consumer warps): from degree 64 wherever a
+            // group's share of a stage is whole rounds; below it the 16-chain
+            // loop is faster.
             P.groups = warps == 16 && stages % 2 == 0 && stages >= 4 ? 2 : 1;
+            if (o.consumer_warps == 0 && shape.groups > 0) P.groups = static_cast<uint32_t>(shape.groups);
+            if (o.consumer_groups > 0) {
+                // an explicit count must divide the warps (16: 1 or 2; 12: 1, 2 or 3) and the ring depth
+                const int64_t gcount = o.consumer_groups;
+                if (warps % gcount != 0 || stages % gcount != 0 || (warps == 16 && gcount == 3) || warps == 8)
+                    return AP_ERR_ARG;
+                P.groups = static_cast<uint32_t>(gcount);
+            }
             const int64_t round_groups = 6 * 32 * 16 / P.groups;
             const bool whole_rounds = warps == 16 && (se / 4) % round_groups == 0;
-            P.op.six_groups = whole_rounds && (op.degree >= 64 || (op.degree >= 32 && se / 4 == round_groups)) ? 1 : 0;
+            P.op.six_groups = whole_rounds && op.degree >= 64 ? 1 : 0;
+            record_ring_shape(run, warps, P.groups, warps == 16 ? (P.op.six_groups ? 24 : 16) : 32);
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);
         }

@@ -523,7 +523,10 @@ def bench_scale(args, d: Dist) -> dict:
 def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     """Every kernel of the path at its workload's full size, 20 timed launches
     after 3 warm-up (CUDA events), as GB/s (read + write bytes) and the
-    fraction of the measured copy. Timed separately from the headline."""
+    fraction of the measured copy. Timed separately from the headline: the
+    synchronous and the pages' asynchronous scale, the ring's scale and row
+    shift at every ring depth, the cluster calls, the masked copy, all 16
+    (degree, depth) cells of the polynomial sweep and the two FP32 roofs."""
     import torch
 
     out = {}
@@ -532,34 +535,44 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
         ms = time_steps(fn, 20, 3, stream) / 20
         gb = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"GB/s": round(gb, 1), "frac": round(gb / peak, 4), "ms": round(ms, 4), **extra}
+        return ms
 
     n = x.numel()  # 2^28 floats
     put("scale_sync (baseline), 2^20 x 256", 8 * n, lambda: ap.ap_scale_sync(x, y, n // 256, 256, 2.0, stream))
     put("scale, the pages' 2 x 1 KiB per-thread cp.async pipeline, 2^20 x 256", 8 * n,
         lambda: ap.ap_debug_scale_pages_async(x, y, n // 256, 256, 2.0, stream))
-    for S in (3, 4):
+    for S in (2, 3, 4, 5, 6):
         put(f"scale ring S={S}, 2^20 x 256", 8 * n, lambda: ap.ap_scale(x, y, n // 256, 256, 2.0, S, stream))
-    put("row roll 2^26 x 4, shift 1", 8 * n, lambda: ap.ap_row_roll(x, y, n // 4, 4, 1, stream))
+    for S in (2, 3, 4, 5, 6):
+        ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
+        put(f"row roll 2^26 x 4, shift 1, S={S}", 8 * n, lambda: ap.ap_row_roll(x, y, n // 4, 4, 1, stream))
+    ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
     put("row roll 2^26 x 4, A + 4 bytes", 8 * (n - 4), lambda: ap.ap_row_roll(x[1:n - 3], y[:n - 4], (n - 4) // 4, 4, 1,
                                                                                    stream))
     for cs in (2, 4, 8):
         put(f"cluster exchange cs={cs}, 32 KiB chunks", 8 * n,
             lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768, stream))
+    put("cluster exchange_ex cs=16, 32 KiB chunks", 8 * n,
+        lambda: ap.ap_cluster_exchange_ex(x, y, n, 16, 32768, 1, stream))
     for cs in (4, 8, 16):
         put(f"cluster all-to-all cs={cs}, 32 KiB chunks", 8 * n,
             lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768, stream))
-    codes = torch.full((n // 4,), 16, dtype=torch.int8, device=dev)
-    # per 16-byte chunk: 16 read + 16 written + 1 code byte
-    put("masked copy, all chunks copied", 33 * (n // 4), lambda: ap.ap_masked_copy(x, y, n // 4, codes, 4, stream))
-    del codes
+    for name, pattern in (("all chunks copied", [16]),
+                          ("1/8 off, 1/8 half, 1/8 zeroed, 5/8 copied", [-1, 8, -2, 16, 16, 16, 16, 16])):
+        codes = torch.tensor(pattern, dtype=torch.int8).repeat(n // 4 // len(pattern)).to(dev)
+        # per 16-byte chunk: the bytes it reads, the 16 it writes unless predicated off, 1 code byte
+        rd = sum(max(c, 0) for c in pattern) / len(pattern)
+        wr = sum(16 for c in pattern if c != -1) / len(pattern)
+        put(f"masked copy, {name}", (n // 4) * (rd + wr + 1), lambda: ap.ap_masked_copy(x, y, n // 4, codes, 4, stream))
+        del codes
     xp = synth.uniform_pm1_torch(synth.SEED_POLY, 1 << 30, dev)
     yp = torch.empty_like(xp)
-    for K in (8, 32, 128):
+    for K in (0, 8, 32, 128):
         c = synth.coeffs_np(K).tolist()
-        put(f"poly K={K}, 2^30, S=2", 8 * (1 << 30), lambda: ap.ap_poly(xp, yp, 1 << 30, c, K, 2, stream),
-            fp32_tflops=None)
-        ms = out[f"poly K={K}, 2^30, S=2"]["ms"]
-        out[f"poly K={K}, 2^30, S=2"]["fp32_tflops"] = round(2.0 * K * (1 << 30) / (ms * 1e-3) / 1e12, 2)
+        for S in (2, 3, 4, 6):
+            key = f"poly K={K}, 2^30, S={S}"
+            ms = put(key, 8 * (1 << 30), lambda: ap.ap_poly(xp, yp, 1 << 30, c, K, S, stream))
+            out[key]["fp32_tflops"] = round(2.0 * K * (1 << 30) / (ms * 1e-3) / 1e12, 2)
     del xp, yp
     # The FP32 roofs under the same clocks: register-only fma chains, and the
     # operand pattern of the Horner loop (a coefficient read from shared memory
@@ -575,9 +588,10 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
         roofs[key] = 2.0 * fma / (ms * 1e-3) / 1e12
         out[key] = {"fp32_tflops": round(roofs[key], 2), "ms": round(ms, 4)}
     del probe
-    k128 = out["poly K=128, 2^30, S=2"]
-    k128["frac_of_register_probe"] = round(k128["fp32_tflops"] / roofs["fp32 fma probe, registers only"], 4)
-    k128["frac_of_horner_probe"] = round(k128["fp32_tflops"] / roofs["fp32 fma probe, Horner operands"], 4)
+    for S in (2, 3, 4, 6):
+        k128 = out[f"poly K=128, 2^30, S={S}"]
+        k128["frac_of_register_probe"] = round(k128["fp32_tflops"] / roofs["fp32 fma probe, registers only"], 4)
+        k128["frac_of_horner_probe"] = round(k128["fp32_tflops"] / roofs["fp32 fma probe, Horner operands"], 4)
     st = ap.ap_check()
     if st != 0:
         raise RuntimeError(f"device status {ap.ap_status_string(st)}")
@@ -680,89 +694,27 @@ def sweep(which: str, args):
         window["t1"] = datetime.datetime.now()
         return ms
 
-    if "scale" in groups or "tune" in groups or "hints" in groups or "schedule" in groups or "tensortune" in groups:
+    if "scale" in groups:
         n_t, t = SCALE_TILES, SCALE_TILE
         n = n_t * t
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, n, dev)
         y = torch.empty_like(x)
-        if "scale" in groups:
-            ms = run(lambda: ap.ap_scale_sync(x, y, n_t, t, 2.0))
-            yield line("scale 2^28 f32", "scale_sync", 8 * n, ms)
-            ms = run(lambda: ap.ap_debug_scale_pages_async(x, y, n_t, t, 2.0))
-            yield line("scale 2^28 f32", "the pages' async pipeline (2 x 1 KiB, per-thread cp.async)", 8 * n, ms)
-            for S in (2, 3, 4, 5, 6):
-                ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
-                yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
-                           stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
-                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
-            ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)  # the tensor-map producer
-            for S in (2, 3, 4, 5, 6):
-                ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
-                yield line("scale 2^28 f32", f"ring tensor-map producer S={S}", 8 * n, ms,
-                           stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
-                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
-            ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 0)
-        if "schedule" in groups:
-            cands = [(2, 0, 0, 0), (2, 1, 0, 0), (3, 0, 0, 0), (3, 1, 0, 0), (4, 0, 0, 0), (4, 1, 0, 0),
-                     (2, 1, 32, 1), (2, 1, 64, 1), (3, 1, 48, 1), (2, 1, 16, 1)]
-            reps = {c: [] for c in cands}
-            for _ in range(5):
-                for S, sched, kib, cps in cands:
-                    ap.ap_debug_set(ap.AP_DBG_SCHEDULE, sched)
-                    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                    ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                    reps[(S, sched, kib, cps)].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S)))
-            for key in (ap.AP_DBG_SCHEDULE, ap.AP_DBG_STAGE_BYTES, ap.AP_DBG_CTAS_PER_SM):
-                ap.ap_debug_set(key, 0)
-            for (S, sched, kib, cps), v in reps.items():
-                v = sorted(v)
-                yield line("scale 2^28 f32", f"ring S={S} schedule={sched} stage={kib or 'auto'}KiB ctas/SM={cps or 'auto'}",
-                           8 * n, v[2], min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
-        if "hints" in groups:
-            reps = {h: [] for h in (0, 1)}
-            for _ in range(5):
-                for h in reps:
-                    ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, h)
-                    reps[h].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, 2)))
-            ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, 0)
-            for h, v in reps.items():
-                v = sorted(v)
-                yield line("scale 2^28 f32", f"ring S=2 cache_hints={h} (median of 5)", 8 * n, v[2],
-                           min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
-        if "tensortune" in groups:
-            # the tensor-map producer: ring depth x stage size x CTAs per SM
-            cands = [(S, kib, cps) for S in (2, 3, 4, 6) for kib in (8, 16, 32) for cps in (1, 2, 3, 4)
-                     if S * (kib + 3) * cps <= 220]
-            reps = {c: [] for c in cands}
-            ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
-            for _ in range(3):
-                for S, kib, cps in cands:
-                    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                    ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                    reps[(S, kib, cps)].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S)))
-            for key in (ap.AP_DBG_FORCE_PATH, ap.AP_DBG_STAGE_BYTES, ap.AP_DBG_CTAS_PER_SM):
-                ap.ap_debug_set(key, 0)
-            for (S, kib, cps), v in reps.items():
-                v = sorted(v)
-                yield line("scale 2^28 f32", f"ring tensor-map producer S={S} stage={kib}KiB ctas/SM={cps} (median of 3)",
-                           8 * n, v[1], min_ms=round(v[0], 5), max_ms=round(v[-1], 5))
-        if "tune" in groups:
-            cands = [(2, 16, 2), (2, 12, 3), (3, 24, 1), (3, 8, 3), (4, 16, 1), (4, 8, 2),
-                     (5, 12, 1), (5, 16, 1), (5, 8, 2), (5, 36, 1), (5, 24, 1), (5, 6, 3), (5, 4, 4),
-                     (6, 8, 2), (6, 12, 1), (6, 16, 1), (6, 32, 1), (6, 4, 3), (6, 6, 2), (6, 24, 1)]
-            reps = {c: [] for c in cands}
-            for _ in range(5):  # interleaved repetitions: drift hits every candidate alike
-                for S, kib, cps in cands:
-                    ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                    ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                    reps[(S, kib, cps)].append(run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S)))
-            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
-            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
-            for (S, kib, cps), v in reps.items():
-                v = sorted(v)
-                yield line("scale 2^28 f32", f"ring S={S} stage={kib}KiB ctas/SM={cps} (median of 5)", 8 * n,
-                           v[len(v) // 2], min_ms=round(v[0], 5), max_ms=round(v[-1], 5),
-                           ring_kib_per_sm=S * kib * cps)
+        ms = run(lambda: ap.ap_scale_sync(x, y, n_t, t, 2.0))
+        yield line("scale 2^28 f32", "scale_sync", 8 * n, ms)
+        ms = run(lambda: ap.ap_debug_scale_pages_async(x, y, n_t, t, 2.0))
+        yield line("scale 2^28 f32", "the pages' async pipeline (2 x 1 KiB, per-thread cp.async)", 8 * n, ms)
+        for S in (2, 3, 4, 5, 6):
+            ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
+            yield line("scale 2^28 f32", f"ring S={S}", 8 * n, ms,
+                       stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
+                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
+        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)  # the tensor-map producer
+        for S in (2, 3, 4, 5, 6):
+            ms = run(lambda: ap.ap_scale(x, y, n_t, t, 2.0, S))
+            yield line("scale 2^28 f32", f"ring tensor-map producer S={S}", 8 * n, ms,
+                       stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS),
+                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS))
+        ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 0)
         del x, y
     if "poly" in groups:
         n = 1 << 30
@@ -776,59 +728,18 @@ def sweep(which: str, args):
                 yield line("poly 2^30 f32", f"ring S={S} K={K} (defaults)", 8 * n, ms,
                            fp32_tflops=round(tflops, 2), fma_per_elem=K,
                            stage_elems=ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
-        if "polywarps" in groups:
-            for K in (8, 32, 128):
-                c = synth.coeffs_np(K).tolist()
-                for warps in (8, 15, 16):
-                    ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
-                    for S, kib in ((2, 96), (3, 64), (4, 48), (6, 32)):
-                        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                        ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
-                        tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
-                        yield line("poly 2^30 f32", f"ring S={S} K={K} warps={warps} stage={kib}KiB", 8 * n, ms,
-                                   fp32_tflops=round(tflops, 2), fma_per_elem=K)
-            ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 0)
-            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
-        if "polyocc" in groups:
-            # degree 128 (fma-bound): consumer warps x CTAs per SM x stage size
-            c = synth.coeffs_np(128).tolist()
-            for warps, cps, S, kib in ((16, 1, 3, 64), (16, 1, 2, 96), (8, 1, 3, 64), (8, 2, 3, 32), (8, 2, 2, 48),
-                                       (8, 3, 2, 32), (8, 3, 3, 24), (15, 1, 3, 64), (8, 2, 3, 24), (16, 1, 6, 32)):
-                ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
-                ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                try:
-                    ms = run(lambda: ap.ap_poly(x, y, n, c, 128, S))
-                except ap.APError:
-                    continue
-                yield line("poly 2^30 f32", f"ring S={S} K=128 warps={warps} ctas/SM={cps} stage={kib}KiB", 8 * n, ms,
-                           fp32_tflops=round(2.0 * 128 * n / (ms * 1e-3) / 1e12, 2),
-                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
-            for key in (ap.AP_DBG_CONSUMER_WARPS, ap.AP_DBG_CTAS_PER_SM, ap.AP_DBG_STAGE_BYTES):
-                ap.ap_debug_set(key, 0)
-        if "polytune" in groups:
-            for K in (32, 128):
-                c = synth.coeffs_np(K).tolist()
-                for S in (2, 4, 6):
-                    for kib in (16, 24, 32, 48):
-                        if S * kib > 200:
-                            continue
-                        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, kib * 1024)
-                        ms = run(lambda: ap.ap_poly(x, y, n, c, K, S))
-                        tflops = 2.0 * K * n / (ms * 1e-3) / 1e12
-                        yield line("poly 2^30 f32", f"ring S={S} K={K} stage={kib}KiB", 8 * n, ms,
-                                   fp32_tflops=round(tflops, 2), fma_per_elem=K)
-                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
-        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, 0)
-        # the FP32 roof measured under the same conditions: register-only fma chains
+        # the FP32 roofs measured under the same conditions: register-only fma
+        # chains, and the Horner loop's operand pattern without memory
         probe = torch.empty(sms * 1024, dtype=torch.float32, device=dev)
-        iters = 1 << 16
-        ms = run(lambda: ap.ap_debug_fma_probe(probe, probe.numel(), iters))
-        tfma = sms * 1024 * 32 * iters / (ms * 1e-3) / 1e12
-        d = line("fp32 fma probe (registers only)", "fma_probe_kernel", 0, ms, fp32_tflops=round(2 * tfma, 2))
-        d.pop("GB/s")
-        d.pop("frac_of_measured_hbm")
-        yield d
+        for kern, fn, iters, fma in (
+                ("fma_probe_kernel (registers only)", ap.ap_debug_fma_probe, 1 << 16, sms * 1024 * 32),
+                ("fma_probe_horner_kernel (Horner operands)", ap.ap_debug_fma_probe_horner, 1 << 10,
+                 sms * 512 * 24 * 128)):
+            ms = run(lambda: fn(probe, probe.numel(), iters))
+            d = line("fp32 fma probe", kern, 0, ms, fp32_tflops=round(2.0 * fma * iters / (ms * 1e-3) / 1e12, 2))
+            d.pop("GB/s")
+            d.pop("frac_of_measured_hbm")
+            yield d
         del x, y, probe
     if "roll" in groups:
         rows, cols = 1 << 26, 4
@@ -836,14 +747,11 @@ def sweep(which: str, args):
         abuf = torch.empty(n + 4, dtype=torch.float32, device=dev)
         bbuf = torch.empty(n + 4, dtype=torch.float32, device=dev)
         synth.uniform_pm1_torch(synth.SEED_ROLL, n + 4, dev, out=abuf)
-        for S in (0, 2, 3, 6) if "rolltune" in groups else (0,):
-            ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
-            for name, sa, sb in (("aligned", 0, 0), ("A+4B", 1, 0), ("B+4B", 0, 1), ("A+4B,B+4B", 1, 1)):
-                A, B = abuf[sa:sa + n], bbuf[sb:sb + n]
-                ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
-                yield line("roll 2^26x4 f32", f"ring {name} S={S or 'default'}", 8 * n, ms,
-                           flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
-        ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, 0)
+        for name, sa, sb in (("aligned", 0, 0), ("A+4B", 1, 0), ("B+4B", 0, 1), ("A+4B,B+4B", 1, 1)):
+            A, B = abuf[sa:sa + n], bbuf[sb:sb + n]
+            ms = run(lambda: ap.ap_row_roll(A, B, rows, cols, 1))
+            yield line("roll 2^26x4 f32", f"ring {name}", 8 * n, ms,
+                       flags=ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS), stages=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
         # the tensor-map producer (aligned variant): each stage one 2-D box of
         # 1 KiB lines of the input, the stage that wraps as 1-D boxes
         ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
@@ -862,35 +770,6 @@ def sweep(which: str, args):
         n = 1 << 28
         x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
         y = torch.empty_like(x)
-        for store, piece_kib, cps in ((2, 16, 1), (2, 16, 2), (2, 16, 3), (2, 12, 2), (2, 32, 2), (1, 16, 2)):
-            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
-            ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
-            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-            for cs in (1, 2, 4, 8):
-                ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
-                yield line("exchange 2^28 f32, 32 KiB chunks",
-                           f"cluster cs={cs} piece={piece_kib}KiB ctas/SM={cps} store={'tma' if store == 1 else 'warps'}",
-                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
-                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
-        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
-        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
-        # each receiver form at the default pieces and slots: bulk (TMA) stores,
-        # or 1/2/4/8 warps storing each piece together
-        for store, group in ((1, 0), (2, 1), (2, 2), (2, 4), (2, 8)):
-            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
-            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
-            form = "tma" if store == 1 else f"warps x{group}"
-            for cs in (1, 2, 4, 8):
-                ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
-                yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster cs={cs} store={form} (default pieces)",
-                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
-                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
-            ms = run(lambda: ap.ap_cluster_exchange_ex(x, y, n, 16, 32768, 1))
-            yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster_ex cs=16 store={form}", 8 * n, ms,
-                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID))
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, 0)
         # small chunks (the pages' example moves 256 bytes): batched against plain pieces
         for chunk in (256, 1024, 4096):
             for batch in (0, 1):
@@ -908,29 +787,6 @@ def sweep(which: str, args):
                                    slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
                                    item_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_BATCH, 0)
-        # loader and pusher lanes with smaller pieces (ring depths that 2 and 4 divide)
-        for piece_kib, cps in ((4, 2), (2, 2), (8, 1)):
-            for lanes in (1, 2, 4):
-                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
-                ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
-                for cs in (2, 8):
-                    ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
-                    yield line("exchange 2^28 f32, 32 KiB chunks",
-                               f"cluster cs={cs} piece={piece_kib}KiB ctas/SM={cps} lanes={lanes}", 8 * n, ms,
-                               slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
-        for key in (ap.AP_DBG_STAGE_BYTES, ap.AP_DBG_CTAS_PER_SM, ap.AP_DBG_EXCHANGE_LANES):
-            ap.ap_debug_set(key, 0)
-        for cps in (3, 4):
-            ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-            for piece_kib in (4, 8):
-                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
-                ms = run(lambda: ap.ap_cluster_exchange_ex(x, y, n, 16, 32768, 1))
-                yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster_ex cs=16 ctas/SM={cps} piece={piece_kib}KiB",
-                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
-                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
-        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
-        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         for cs, shift in ((3, 1), (6, 2), (16, 1), (16, 5)):
             ms = run(lambda: ap.ap_cluster_exchange_ex(x, y, n, cs, 32768, shift))
             yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster_ex cs={cs} shift={shift}", 8 * n, ms,
@@ -939,48 +795,16 @@ def sweep(which: str, args):
             ms = run(lambda: ap.ap_cluster_exchange(x, y, n, cs, 32768))
             yield line("exchange 2^28 f32, 32 KiB chunks", f"cluster cs={cs} (defaults)", 8 * n, ms,
                        grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES))
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
-        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
         del x, y
     if "alltoall" in groups:
         n = 1 << 28
         x = synth.uniform_pm1_torch(synth.SEED_EXCHANGE, n, dev)
         y = torch.empty_like(x)
-        for store, group in ((1, 0), (2, 1), (2, 2), (2, 4), (2, 8)):
-            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, store)
-            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, group)
-            form = "tma" if store == 1 else f"warps x{group}"
-            for cs in (1, 2, 4, 8, 16):
-                ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
-                yield line("all-to-all 2^28 f32, 32 KiB chunks", f"cluster a2a cs={cs} store={form} (default pieces)",
-                           8 * n, ms, grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID),
-                           slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
-                           piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, 0)
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, 0)
         for cs in (1, 2, 4, 8, 16):
-            for piece_kib, cps in ((0, 0), (2, 2), (4, 2), (8, 2), (16, 2), (4, 1), (8, 1), (16, 1)):
-                ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, piece_kib * 1024)
-                ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
-                try:
-                    ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
-                except ap.APError:
-                    continue
-                yield line("all-to-all 2^28 f32, 32 KiB chunks",
-                           f"cluster a2a cs={cs} piece<={piece_kib or 'auto '}KiB ctas/SM={cps or 'auto'}", 8 * n, ms,
-                           grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
-                           piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
-        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 0)
-        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 0)
-        # loader and pusher lanes, at the default receiver and pieces
-        for lanes in (1, 2, 4):
-            ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, lanes)
-            for cs in (1, 2, 4, 8, 16):
-                ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
-                yield line("all-to-all 2^28 f32, 32 KiB chunks", f"cluster a2a cs={cs} lanes={lanes} (default pieces)",
-                           8 * n, ms, slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
-                           piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
-        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, 0)
+            ms = run(lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768))
+            yield line("all-to-all 2^28 f32, 32 KiB chunks", f"cluster a2a cs={cs} (defaults)", 8 * n, ms,
+                       grid=ap.ap_debug_get(ap.AP_DBG_LAST_GRID), slots=ap.ap_debug_get(ap.AP_DBG_LAST_STAGES),
+                       piece_bytes=4 * ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS))
         del x, y
     if "autotune" in groups:
         n = 1 << 28
@@ -1168,8 +992,9 @@ def sweep(which: str, args):
 
 # ----------------------------------------------------------------------------- profiling cases
 
-PROFILE_CASES = ("scale", "sync", "poly32", "poly32_s4", "poly128", "roll", "roll_mis", "roll_tensor", "exchange4", "exchange16",
-                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked")
+PROFILE_CASES = ("scale", "scale_s6", "sync", "poly0", "poly8", "poly32", "poly32_s4", "poly32_s6", "poly128",
+                 "poly128_s6", "roll", "roll_mis", "roll_tensor", "exchange2", "exchange4", "exchange8", "exchange16",
+                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "copy_2gib")
 
 
 def profile_case(name: str, args):
@@ -1191,6 +1016,13 @@ def profile_case(name: str, args):
         "poly32": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 3),
         "poly128": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(128).tolist(), 128, 2),
         "poly32_s4": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 4),
+        "poly32_s6": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(32).tolist(), 32, 6),
+        "poly128_s6": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(128).tolist(), 128, 6),
+        "poly0": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(0).tolist(), 0, 2),
+        "poly8": lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(8).tolist(), 8, 2),
+        "exchange2": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 2, 32768),
+        "exchange8": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 8, 32768),
+        "scale_s6": lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, 6),
         "roll": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "roll_mis": lambda: ap.ap_row_roll(x[1:n + 1], y[:n], n // 4, 4, 1),
         "exchange4": lambda: ap.ap_cluster_exchange(x[:n], y[:n], n, 4, 32768),
@@ -1202,6 +1034,12 @@ def profile_case(name: str, args):
         "roll_tensor": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "masked": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
     }
+    if name == "copy_2gib":
+        # the measured copy the roofline divides by: torch's copy of 2^30
+        # bf16 elements (2 GiB read + 2 GiB written), at its full size
+        a = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev).fill_(1.0)
+        b = torch.empty_like(a)
+        calls["copy_2gib"] = lambda: b.copy_(a)
     if name == "roll_tensor":
         ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     fn = calls[name]

@@ -242,13 +242,15 @@ ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const in
                          cudaStream_t stream);
 
 /*
- * ap_autotune: choose the ring's stage size, CTAs per SM and consumer warps by
+ * ap_autotune: choose the ring's stage size, schedule and consumer warps by
  * timing them on this device. Source: "CUDA Async Copy and Pipeline Guide",
  * FAQ: more stages hide more latency but use more shared memory, and the
  * sweet spot is found by profiling. For the given ring depth the call runs
- * the operation over in/out for every stage size from 8 to 96 KiB and every
- * CTAs-per-SM count (1-4) whose shared memory fits, three timed launches
- * each (CUDA events on `stream`, median), keeps the fastest and installs it:
+ * the operation over in/out for every stage size from 8 to 96 KiB, under
+ * both schedules: a persistent grid of 1-4 CTAs per SM (whose shared memory
+ * fits), and CTAs that each take a run of depth, 2 x depth or 4 x depth
+ * consecutive stages. Three timed launches each (CUDA events on `stream`,
+ * median); it keeps the fastest and installs it:
  * later calls of that operation with that depth on this device use it
  * instead of the built-in defaults (explicit ap_debug_set settings still
  * win). Blocks until the timing is done.
@@ -266,8 +268,10 @@ typedef enum ap_tune_op { AP_TUNE_SCALE = 1, AP_TUNE_ROW_ROLL = 2, AP_TUNE_POLY 
 
 typedef struct ap_ring_shape {
     int64_t stage_bytes; /* payload of one ring stage */
-    int ctas_per_sm;     /* resident CTAs per SM the grid is sized for */
+    int ctas_per_sm;     /* persistent grid: resident CTAs per SM the grid is sized for */
     int consumer_warps;  /* consumer warps per CTA */
+    int stages_per_cta;  /* 0: persistent grid; r: every CTA takes r consecutive stages */
+    int consumer_groups; /* ap_poly: consumer groups taking stages in turn (1 or 2) */
     double gbs;          /* measured rate of the chosen shape, GB/s */
 } ap_ring_shape;
 

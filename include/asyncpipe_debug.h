@@ -38,13 +38,10 @@ typedef enum ap_debug_key {
     AP_DBG_GRID = 5,            /* cap on the number of CTAs of ring kernels (0 = automatic) */
     AP_DBG_CTAS_PER_SM = 6,     /* resident ring CTAs per SM the grid is sized for (0 = 1) */
     AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 3) */
-    AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8, 15 or 16 (0 = automatic) */
+    AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8, 12 or 16 (0 = automatic) */
     AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
                                    piece to a shared->global bulk copy, 2 receiver warps with 16-byte
                                    stores (AP_DBG_EXCHANGE_GROUP warps per piece) */
-    AP_DBG_CACHE_HINTS = 10,    /* ring cache hints: 1 = bulk loads carry an L2 evict-first policy,
-                                   0 = none; any other value is AP_ERR_ARG (streaming consumer
-                                   stores, once bit 1, gained nothing and were removed) */
     AP_DBG_DEVICE_CHECKS = 11,  /* 1: ring kernels verify, before every stage, that each copy and each
                                    shared/global range they touch lies inside the caller's buffers and
                                    the stage slot; a violation makes ap_check report AP_ERR_SHAPE (site
@@ -56,8 +53,6 @@ typedef enum ap_debug_key {
     AP_DBG_LAST_STAGE_ELEMS = 102, /* elements per ring stage (chunk elements for exchange) */
     AP_DBG_LAST_SMEM = 103,     /* dynamic shared memory per CTA, bytes */
     AP_DBG_LAST_STAGES = 104,   /* ring depth */
-    AP_DBG_SCHEDULE = 12,       /* ring stage order: 0 CTA b takes stages b, b + grid, ... (all CTAs
-                                   stream one window of memory); 1 each CTA takes a contiguous run */
     AP_DBG_EXCHANGE_GROUP = 13, /* cluster exchange, warp-store receiver: warps that store one piece
                                    together, 1, 2, 4 or 8 (the eight receiver warps take pieces in
                                    turn, 8 / value at once); 0 = automatic */
@@ -78,7 +73,20 @@ typedef enum ap_debug_key {
                                    all-to-all; where none fits, one ring depth); 1 never split;
                                    0 automatic (the all-to-all splits where its ring depth is a power
                                    of two, with that many send buffers) */
+    AP_DBG_RING_RUN = 18,       /* ring schedule: 0 automatic; 1 a persistent grid (SMs x CTAs per SM
+                                   CTAs, CTA b taking stages b, b + grid, ...); r = 2 .. 2^20 every
+                                   CTA takes r consecutive stages and as many CTAs launch as that
+                                   takes. AP_DBG_GRID, when set, implies the persistent grid */
+    AP_DBG_CONSUMER_GROUPS = 19, /* ap_poly: consumer groups that take stages in turn (group g the
+                                   stages g, g + groups, ...): 0 automatic, or 1, 2, 3 where the count
+                                   divides the consumer warps (16: 1 or 2; 12: 1, 2 or 3) and the
+                                   ring depth; other counts make ap_poly return AP_ERR_ARG */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
+    AP_DBG_LAST_RUN = 107,      /* ring: consecutive stages per CTA, 0 for the persistent grid */
+    AP_DBG_LAST_WARPS = 108,    /* ring: consumer warps per CTA */
+    AP_DBG_LAST_GROUPS = 109,   /* ring: consumer groups taking stages in turn */
+    AP_DBG_LAST_CHAINS = 110,   /* ap_poly: Horner chains a consumer thread runs per round in whole
+                                   aligned stages (16, 24 or 32); 0 for other calls */
     AP_DBG_LAST_FLAGS = 105     /* bit 0: some stage used cp.async edge copies (misaligned head
                                    or unaligned tail); bit 1: some stage used the scalar
                                    shared-memory path (input/output alignments differ or wrap);

@@ -39,14 +39,14 @@ def reset_debug(ap):
         ap.AP_DBG_ROLL_STAGES,
         ap.AP_DBG_CONSUMER_WARPS,
         ap.AP_DBG_EXCHANGE_STORE,
-        ap.AP_DBG_CACHE_HINTS,
         ap.AP_DBG_DEVICE_CHECKS,
-        ap.AP_DBG_SCHEDULE,
         ap.AP_DBG_EXCHANGE_GROUP,
         ap.AP_DBG_EXCHANGE_SEND_SLOTS,
         ap.AP_DBG_STRICT_ALIGN,
         ap.AP_DBG_EXCHANGE_LANES,
         ap.AP_DBG_EXCHANGE_BATCH,
+        ap.AP_DBG_RING_RUN,
+        ap.AP_DBG_CONSUMER_GROUPS,
     ):
         ap.ap_debug_set(key, 0)
 

@@ -191,10 +191,9 @@ def test_debug_settings_roundtrip(ap):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, bad) == ap.AP_ERR_ARG
     for good in (1, 2, 4, 8, 16, 0):
         assert lib.ap_debug_set(ap.AP_DBG_EXCHANGE_SEND_SLOTS, good) == ap.AP_OK
-    for bad in (2, 3):  # streaming stores were removed: only the evict-first load hint remains
-        assert lib.ap_debug_set(ap.AP_DBG_CACHE_HINTS, bad) == ap.AP_ERR_ARG
-    for good in (1, 0):
-        assert lib.ap_debug_set(ap.AP_DBG_CACHE_HINTS, good) == ap.AP_OK
+    for removed in (10, 12):  # the cache-hint and stage-order keys gained nothing and were removed
+        assert lib.ap_debug_set(removed, 0) == ap.AP_ERR_ARG
+        assert lib.ap_debug_get(removed) == -1
 
 
 @pytest.mark.skipif(

@@ -28,11 +28,14 @@ def test_autotune_scale_installs_choice(ap, orc):
     scratch = torch.empty_like(x)
     shape = ap.ap_autotune(ap.AP_TUNE_SCALE, x, scratch, n, 2)
     assert shape["gbs"] > 0 and shape["stage_bytes"] >= 8192 and 1 <= shape["ctas_per_sm"] <= 4
+    assert shape["stages_per_cta"] in (0, 2, 4, 8)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     y = torch.empty_like(x)
     ap.ap_scale(x, y, n // 256, 256, 2.0, 2)
     assert ap.ap_check() == ap.AP_OK
-    assert ap.ap_debug_get(ap.AP_DBG_LAST_GRID) == sms * shape["ctas_per_sm"]
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_RUN) == shape["stages_per_cta"]
+    if shape["stages_per_cta"] == 0:
+        assert ap.ap_debug_get(ap.AP_DBG_LAST_GRID) == sms * shape["ctas_per_sm"]
     assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS) == shape["stage_bytes"] // 4
     assert_bits(to_np(y), orc.scale(to_np(x), 2.0), "scale with the tuned shape")
     ap.ap_autotune_reset()

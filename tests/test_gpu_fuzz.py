@@ -30,8 +30,8 @@ def _knobs(ap, rng):
     ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, int(rng.choice([0, 16, 48, 256, 4096, 24576, 65536])))
     ap.ap_debug_set(ap.AP_DBG_GRID, int(rng.choice([0, 0, 1, 2, 5, 37])))
     ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2, 3])))
-    ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, int(rng.choice([0, 8, 15, 16])))
-    ap.ap_debug_set(ap.AP_DBG_SCHEDULE, int(rng.choice([0, 1])))
+    ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, int(rng.choice([0, 8, 12, 16])))
+    ap.ap_debug_set(ap.AP_DBG_RING_RUN, int(rng.choice([0, 0, 1, 2, 3, 7, 12])))
 
 
 @pytest.mark.parametrize("seed", RING_SEEDS)

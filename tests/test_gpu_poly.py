@@ -26,7 +26,7 @@ def test_poly_small(ap, orc, degree, stages):
     x = synth.uniform_pm1_torch(n + degree, n, dev)
     c = synth.coeffs_np(degree)
     want = orc.poly(to_np(x), c)
-    for stage_bytes, grid, warps in ((256, 2, 8), (0, 0, 0), (1024, 3, 16), (0, 0, 16), (2048, 2, 15), (0, 0, 15)):
+    for stage_bytes, grid, warps in ((256, 2, 8), (0, 0, 0), (1024, 3, 16), (0, 0, 16), (2048, 2, 12), (0, 0, 12)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_GRID, grid)
         ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
@@ -42,14 +42,14 @@ def test_poly_degree_boundaries(ap, orc, degree):
     """Degrees on both sides of the coefficient loop's four-step words (a
     scalar lead-in until k + 1 is a multiple of four, then four steps per
     16-byte word with the next word loaded ahead), in rounds of 8 to 32
-    chains a thread: element by element against the oracle, under 8, 15 and
+    chains a thread: element by element against the oracle, under 8, 12 and
     16 consumer warps and stages that do and do not take six groups a round."""
     dev = device()
     n = 3 * 96 * 1024 // 4 + 4099
     x = synth.uniform_pm1_torch(n + degree + 11, n, dev)
     c = synth.coeffs_np(degree)
     want = orc.poly(to_np(x), c)
-    for stage_bytes, warps in ((0, 0), (48 * 1024, 16), (64 * 1024, 16), (32 * 1024, 8), (16 * 1024, 15)):
+    for stage_bytes, warps in ((0, 0), (48 * 1024, 16), (64 * 1024, 16), (32 * 1024, 8), (16 * 1024, 12)):
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
         ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
         out = Guarded(n, 0, dev)
@@ -57,6 +57,45 @@ def test_poly_degree_boundaries(ap, orc, degree):
         assert ap.ap_check() == ap.AP_OK
         assert_bits(to_np(out.view), want, f"poly K={degree} stage={stage_bytes} warps={warps}")
         assert out.intact()
+
+
+@pytest.mark.parametrize("warps,groups,stages", [(12, 2, 2), (12, 2, 4), (12, 2, 6), (12, 3, 3), (12, 3, 6),
+                                                  (16, 2, 2), (16, 1, 4), (12, 1, 5)])
+@pytest.mark.parametrize("degree", [0, 8, 33, 128])
+def test_poly_consumer_groups(ap, orc, degree, warps, groups, stages):
+    """Explicit consumer groups (group g takes stages g, g + groups, ...; the
+    count divides the warps and the ring depth), persistent and in runs of
+    consecutive stages, with ragged ends; element by element."""
+    dev = device()
+    c = synth.coeffs_np(degree)
+    ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+    ap.ap_debug_set(ap.AP_DBG_CONSUMER_GROUPS, groups)
+    for stage_bytes, run in ((16 * 1024, 1), (8 * 1024, 0), (12 * 1024, 2 * stages), (4096, 7)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        ap.ap_debug_set(ap.AP_DBG_RING_RUN, run)
+        n = 37 * stage_bytes // 4 + 1237
+        x = synth.uniform_pm1_torch(n + degree + 5, n, dev)
+        want = orc.poly(to_np(x), c)
+        out = Guarded(n, 1, dev)
+        ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"poly K={degree} warps={warps} groups={groups} S={stages} run={run}")
+        assert out.intact()
+
+
+def test_poly_consumer_groups_rejected(ap):
+    """A group count that does not divide the warps or the ring depth."""
+    import torch
+
+    dev = device()
+    x = torch.zeros(4096, device=dev)
+    y = torch.empty_like(x)
+    for warps, groups, stages in ((16, 3, 3), (12, 2, 3), (12, 3, 4), (8, 2, 4)):
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
+        ap.ap_debug_set(ap.AP_DBG_CONSUMER_GROUPS, groups)
+        with pytest.raises(ap.APError) as e:
+            ap.ap_poly(x, y, 4096, [1.0, 2.0], 1, stages)
+        assert e.value.status == ap.AP_ERR_ARG
 
 
 @pytest.mark.parametrize("stages", [4, 6])
@@ -108,47 +147,51 @@ def test_poly_six_group_rounds(ap, orc, degree):
             assert out.intact()
 
 
-def _auto_stage_kib(degree: int, stages: int) -> int:
-    """The documented automatic stage sizes of ap_poly, band by band."""
-    if degree <= 8 and stages == 4:
-        return 24
-    if 4 <= degree <= 10 and stages >= 5:
-        return 16
-    if degree <= 8:
-        return 64 if stages == 2 else 32
-    if degree <= 16:
-        return {2: 64, 3: 32}.get(stages, 24)
-    if degree <= 24:
-        if stages == 5:
-            return 24 if degree <= 18 else 32
-        if stages == 6:
-            return 24 if degree <= 20 else 32
-        return {2: 96, 3: 48, 4: 32}[stages]
+def _auto_shape(degree: int, stages: int) -> tuple:
+    """The documented automatic shapes of ap_poly, band by band: (stage KiB,
+    stages per CTA (0: persistent grid), consumer warps)."""
+    if stages == 2:
+        return (64, 4, 16) if degree <= 24 else (96, 0, 16)
     if stages == 3:
-        return 48 if degree <= 28 else 64
+        if degree <= 10:
+            return (32, 6, 16)
+        if degree <= 16:
+            return (32, 0, 16)
+        if degree <= 28:
+            return (48, 0, 16)
+        return (64, 0, 16) if degree < 80 else (48, 0, 16)
     if stages == 4:
-        return 32 if degree <= 26 else 48
-    return 96 if stages == 2 else 32
+        if degree <= 22:
+            return (32, 8, 16)
+        return (32, 0, 16) if degree <= 26 else (48, 0, 16)
+    if stages == 5:
+        if degree <= 18:
+            return (32, 10, 16)
+        return (32, 0, 8) if degree <= 22 else (32, 0, 16)
+    if degree <= 10:
+        return (24, 12, 16)
+    return (32, 12, 16) if degree <= 26 else (32, 0, 12)
 
 
 def test_poly_automatic_stage_sizes(ap, orc):
-    """Automatic stages: a ring of about 128 KiB up to degree 8 (24 KiB
-    stages at depth 4, 16 KiB for degrees 4-10 at depths 5-6), measured bands
-    of 16-96 KiB for degrees 9-24, and the largest stages that fit above
-    (96 / 64 / 48 / 32 / 32 KiB at depths 2-6)."""
+    """Automatic shapes across the degree bands at every depth: runs of
+    stages where memory bounds the kernel, the persistent grid where the fma
+    work does (stage size, schedule and consumer warps as documented)."""
     dev = device()
     n = 3 * 24576 + 5
     x = synth.uniform_pm1_torch(n, n, dev)
-    for degree in (0, 3, 4, 8, 9, 10, 11, 16, 17, 18, 19, 20, 21, 23, 24, 25, 26, 27, 28, 29, 128):
+    for degree in (0, 3, 4, 8, 9, 10, 11, 16, 17, 18, 19, 20, 21, 22, 23, 24, 25, 26, 27, 28, 29, 79, 80, 128):
         c = synth.coeffs_np(degree)
         want = orc.poly(to_np(x), c)
         for stages in (2, 3, 4, 5, 6):
             out = Guarded(n, 0, dev)
             ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
             assert ap.ap_check() == ap.AP_OK
-            kib = _auto_stage_kib(degree, stages)
-            assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS) == kib * 256
-            assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} automatic stages")
+            kib, run, warps = _auto_shape(degree, stages)
+            got = (ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS), ap.ap_debug_get(ap.AP_DBG_LAST_RUN),
+                   ap.ap_debug_get(ap.AP_DBG_LAST_WARPS))
+            assert got == (kib * 256, run, warps), f"K={degree} S={stages}: {got}"
+            assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} automatic shape")
             assert out.intact()
 
 
@@ -246,3 +289,33 @@ def test_fma_probes_cover_their_threads(ap):
         for elems, iters in ((100, 8), (512, 0)):
             with pytest.raises(ap.APError):
                 fn(out, elems, iters)
+
+
+# (degree, depth) -> (run, consumer warps, groups, chains) of the automatic shape
+AUTO_SHAPES = {
+    (0, 2): (4, 16, 1, 16), (8, 2): (4, 16, 1, 16), (32, 2): (0, 16, 1, 16), (128, 2): (0, 16, 1, 24),
+    (0, 3): (6, 16, 1, 16), (8, 3): (6, 16, 1, 16), (32, 3): (0, 16, 1, 16), (128, 3): (0, 16, 1, 24),
+    (0, 4): (8, 16, 2, 16), (8, 4): (8, 16, 2, 16), (32, 4): (0, 16, 2, 16), (128, 4): (0, 16, 2, 24),
+    (0, 6): (12, 16, 2, 16), (8, 6): (12, 16, 2, 16), (32, 6): (0, 12, 3, 32), (128, 6): (0, 12, 3, 32),
+}
+
+
+@pytest.mark.parametrize("degree,stages", sorted(AUTO_SHAPES))
+def test_poly_automatic_shapes(ap, orc, degree, stages):
+    """The automatic shape of each cell of the degree x depth sweep (runs of
+    stages where memory bounds the kernel, the persistent grid where the fma
+    work does, 24 chains a round from degree 64 with 16 warps, 12 warps in
+    three groups at depth 6 from degree 27) is the one that runs, and its
+    output matches the oracle element by element."""
+    dev = device()
+    n = (1 << 20) + 4099
+    x = synth.uniform_pm1_torch(n + degree + stages, n, dev)
+    c = synth.coeffs_np(degree)
+    out = Guarded(n, 0, dev)
+    ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
+    assert ap.ap_check() == ap.AP_OK
+    got = tuple(ap.ap_debug_get(k) for k in (ap.AP_DBG_LAST_RUN, ap.AP_DBG_LAST_WARPS, ap.AP_DBG_LAST_GROUPS,
+                                             ap.AP_DBG_LAST_CHAINS))
+    assert got == AUTO_SHAPES[(degree, stages)], f"K={degree} S={stages}: {got}"
+    assert_bits(to_np(out.view), orc.poly(to_np(x), c), f"automatic shape K={degree} S={stages}")
+    assert out.intact()

@@ -41,6 +41,31 @@ def test_scale_small_many_stages(ap, orc, stages, n_tiles, tile):
         assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 1
 
 
+@pytest.mark.parametrize("stages", [2, 3, 5, 6])
+@pytest.mark.parametrize("n", [5, 4099, 65536 + 3, 1000003])
+@pytest.mark.parametrize("run", [1, 2, 3, 7, 12])
+def test_scale_stage_runs(ap, orc, stages, n, run):
+    """Both schedules: a persistent grid (run 1) and CTAs that each take a run
+    of consecutive stages, including a short last run and runs shorter than,
+    equal to and longer than the ring, over misaligned buffers too."""
+    dev = device()
+    x = synth.uniform_pm1_torch(n + 5, n + 1, dev)
+    ap.ap_debug_set(ap.AP_DBG_RING_RUN, run)
+    for stage_bytes, in_shift, out_shift in ((256, 0, 0), (4096, 1, 0), (0, 0, 3)):
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, stage_bytes)
+        src = Guarded(n, in_shift, dev, fill=x[:n])
+        want = orc.scale(to_np(src.view), 2.0)
+        out = Guarded(n, out_shift, dev)
+        ap.ap_scale(src.view, out.view, n, 1, 2.0, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"run={run} S={stages} n={n} stage={stage_bytes}")
+        assert out.intact(), "wrote outside the output"
+        stage_elems = ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS)
+        n_stages = max(1, -(-(n - (-out_shift % 4)) // stage_elems))
+        if run > 1:
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_GRID) >= -(-(n_stages - 1) // run)
+
+
 @pytest.mark.parametrize("in_shift,out_shift", [(0, 1), (1, 0), (1, 1), (2, 3), (3, 2), (3, 3)])
 def test_scale_misaligned(ap, orc, in_shift, out_shift):
     dev = device()
@@ -180,23 +205,6 @@ def test_device_generator_matches_host(ap):
     idx = np.random.default_rng(0).integers(0, n, 4096)
     got = to_np(t[torch.from_numpy(idx).to(dev)])
     assert_bits(got, synth.uniform_pm1_np(synth.SEED_POLY, n)[idx], "device generator")
-
-
-@pytest.mark.parametrize("hints", [1])
-def test_scale_cache_hints(ap, orc, hints):
-    """L2 evict-first loads change no result."""
-    import torch
-
-    dev = device()
-    n_tiles, tile = 4099, 256
-    x = synth.uniform_pm1_torch(hints, n_tiles * tile, dev)
-    ap.ap_debug_set(ap.AP_DBG_CACHE_HINTS, hints)
-    for stages in (2, 5):
-        out = Guarded(n_tiles * tile, 1, dev)
-        ap.ap_scale(x, out.view, n_tiles, tile, 2.0, stages)
-        assert ap.ap_check() == ap.AP_OK
-        assert_bits(to_np(out.view), orc.scale(to_np(x), 2.0), f"hints={hints} S={stages}")
-        assert out.intact()
 
 
 @pytest.mark.parametrize("n_tiles,tile", [(1, 1), (5, 3), (37, 256), (1000, 1024), (1 << 20, 256)])
