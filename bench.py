@@ -543,6 +543,10 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
         lambda: ap.ap_debug_scale_pages_async(x, y, n // 256, 256, 2.0, stream))
     for S in (2, 3, 4, 5, 6):
         put(f"scale ring S={S}, 2^20 x 256", 8 * n, lambda: ap.ap_scale(x, y, n // 256, 256, 2.0, S, stream))
+    # context, not this library's kernel: torch's vectorized elementwise
+    # multiply over the same 2^28 floats, a plain load/store streaming kernel
+    put("context: torch.mul(x, 2) (torch's vectorized elementwise kernel), 2^28", 8 * n,
+        lambda: torch.mul(x, 2.0, out=y))
     for S in (2, 3, 4, 5, 6):
         ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, S)
         put(f"row roll 2^26 x 4, shift 1, S={S}", 8 * n, lambda: ap.ap_row_roll(x, y, n // 4, 4, 1, stream))
@@ -994,7 +998,7 @@ def sweep(which: str, args):
 
 PROFILE_CASES = ("scale", "scale_s6", "sync", "poly0", "poly8", "poly32", "poly32_s4", "poly32_s6", "poly128",
                  "poly128_s6", "roll", "roll_mis", "roll_tensor", "exchange2", "exchange4", "exchange8", "exchange16",
-                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "copy_2gib")
+                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "masked_mixed", "masked_all", "torch_mul_2p28")
 
 
 def profile_case(name: str, args):
@@ -1010,6 +1014,7 @@ def profile_case(name: str, args):
     x = synth.uniform_pm1_torch(synth.SEED_SCALE, n + 4, dev)
     y = torch.empty_like(x)
     codes = torch.tensor([-1, 8, -2, 16, 16, 16, 16, 16], dtype=torch.int8).repeat(n // 32).to(dev)
+    codes16 = torch.full((n // 4,), 16, dtype=torch.int8, device=dev)
     calls = {
         "scale": lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, 2),
         "sync": lambda: ap.ap_scale_sync(x[:n], y[:n], n // 256, 256, 2.0),
@@ -1033,13 +1038,15 @@ def profile_case(name: str, args):
         "a2a16": lambda: ap.ap_cluster_all_to_all(x[:n], y[:n], n, 16, 32768),
         "roll_tensor": lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1),
         "masked": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
+        "masked_mixed": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
+        "masked_all": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes16, 4),
     }
-    if name == "copy_2gib":
-        # the measured copy the roofline divides by: torch's copy of 2^30
-        # bf16 elements (2 GiB read + 2 GiB written), at its full size
-        a = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev).fill_(1.0)
+    if name == "torch_mul_2p28":
+        # a plain vectorized load/store kernel (torch's elementwise multiply,
+        # not this library's) over the headline's 2^28 floats, at full size
+        a = synth.uniform_pm1_torch(synth.SEED_SCALE, 1 << 28, dev)
         b = torch.empty_like(a)
-        calls["copy_2gib"] = lambda: b.copy_(a)
+        calls["torch_mul_2p28"] = lambda: torch.mul(a, 2.0, out=b)
     if name == "roll_tensor":
         ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     fn = calls[name]

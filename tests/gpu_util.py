@@ -104,3 +104,33 @@ def tensor_flags(ap, n: int, off: int) -> int:
     line_h = se // 256
     line_rows = (n - off % 256) // 256
     return 12 if 0 < line_h <= 256 and line_rows >= line_h else 4
+
+
+def oracle_poly_threads(orc, x: np.ndarray, c: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """The oracle's Horner loop (orc_poly) over contiguous ranges of x, one
+    range per host core (ctypes releases the GIL during each call). Each
+    element is computed exactly as the single-threaded oracle computes it; the
+    split only shares the work out for full-size checks."""
+    import ctypes
+    import os
+    import threading
+
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    c = np.ascontiguousarray(c, dtype=np.float32).ravel()
+    y = np.empty_like(x)
+    n = x.size
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
+    fp = ctypes.POINTER(ctypes.c_float)
+    rcs = [0] * threads
+
+    def work(t, lo, hi):
+        rcs[t] = orc._lib.orc_poly(x[lo:hi].ctypes.data_as(fp), y[lo:hi].ctypes.data_as(fp), hi - lo,
+                                   c.ctypes.data_as(fp), c.size - 1)
+
+    ths = [threading.Thread(target=work, args=(t, t * n // threads, (t + 1) * n // threads)) for t in range(threads)]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    assert all(rc == 0 for rc in rcs), "orc_poly rejected the degree"
+    return y

@@ -31,3 +31,20 @@ def test_round_f32_against_numpy():
     assert oracle_pins.round_f32(one + 3 * half_ulp) == float(np.float32(1 + 2**-22))
     # subnormal spacing
     assert oracle_pins.round_f32(Fraction(3, 2**150)) == float(np.float32(2**-148))
+
+
+def test_threaded_oracle_poly_is_the_oracle(orc):
+    """The full-size parity test's threaded split of the oracle's Horner loop
+    gives the single-threaded oracle's bits (ranges of every remainder)."""
+    import numpy as np
+
+    import synth
+    from gpu_util import oracle_poly_threads
+
+    x = synth.uniform_pm1_np(synth.SEED_POLY, 100003)
+    for degree in (0, 1, 8, 33):
+        c = synth.coeffs_np(degree)
+        want = orc.poly(x, c)
+        for threads in (1, 3, 7, 16):
+            got = oracle_poly_threads(orc, x, c, threads)
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (degree, threads)

@@ -43,3 +43,4 @@ def test_torch_generator_matches_numpy_cpu():
     for seed, n, chunk in ((synth.SEED_POLY, 5000, 1 << 26), (123, 70001, 4096)):
         t = synth.uniform_pm1_torch(seed, n, "cpu", chunk=chunk).numpy()
         assert np.array_equal(t.view(np.uint32), synth.uniform_pm1_np(seed, n).view(np.uint32))
+
