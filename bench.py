@@ -386,9 +386,9 @@ def bench_scale(args, d: Dist) -> dict:
         t_s0 = datetime.datetime.now()
         ms_sustained = time_steps(ring, sustain_steps, 0, stream, d)
         t_s1 = datetime.datetime.now()
-        rows = clk._rows() if clk.proc is not None else []
-    clocks = clk.summary()
+    rows = clk._rows()  # complete once the sampler has exited
     clocks_sustained = clk.window(t_s0, t_s1, rows) if rows else None
+    clocks = clk.summary()
     ms_sustained = d.max(ms_sustained)
     status = ap.ap_check()
     if status != 0:
