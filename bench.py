@@ -1028,6 +1028,18 @@ def profile_case(name: str, args):
     import synth
 
     dev = torch.device("cuda", 0)
+    if name == "torch_mul_2p28":
+        # a plain vectorized load/store kernel (torch's elementwise multiply,
+        # not this library's) over the headline's 2^28 floats, at full size;
+        # the inputs come from fill kernels, so the multiply is the first
+        # float elementwise kernel of the process
+        a = torch.empty(1 << 28, dtype=torch.float32, device=dev).fill_(1.5)
+        b = torch.empty_like(a)
+        for _ in range(args.warmup + args.steps):
+            torch.mul(a, 2.0, out=b)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": name, "launches": args.warmup + args.steps, "status": 0}), flush=True)
+        return
     n = 1 << 26  # 256 MiB in + 256 MiB out
     x = synth.uniform_pm1_torch(synth.SEED_SCALE, n + 4, dev)
     y = torch.empty_like(x)
@@ -1059,12 +1071,6 @@ def profile_case(name: str, args):
         "masked_mixed": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
         "masked_all": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes16, 4),
     }
-    if name == "torch_mul_2p28":
-        # a plain vectorized load/store kernel (torch's elementwise multiply,
-        # not this library's) over the headline's 2^28 floats, at full size
-        a = synth.uniform_pm1_torch(synth.SEED_SCALE, 1 << 28, dev)
-        b = torch.empty_like(a)
-        calls["torch_mul_2p28"] = lambda: torch.mul(a, 2.0, out=b)
     if name == "roll_tensor":
         ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     fn = calls[name]
