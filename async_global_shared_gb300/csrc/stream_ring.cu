@@ -114,11 +114,11 @@ struct OpPolyDev {
         // c[0] reads the four zero floats staged below it. The loop's shape
         // is chosen by chain count, each form measured at degrees 32 and 128
         // against the others (GB300, 2^30 floats): with 16 chains one word a
-        // trip; with 24, and with 32 below degree 64, two words a trip; with
-        // 32 from degree 64, the odd words one at a time and then four a
-        // trip with one exit test (0.84 -> 0.856 of the register-only fma
-        // rate at ring depth 6). The same change to another chain count cost
-        // it 1-5 %.
+        // trip; with 24, and with 32 below degree 64, an odd word alone and
+        // then two words a trip with one exit test; with 32 from degree 64,
+        // the odd words one at a time and then four a trip (0.84 -> 0.856 of
+        // the register-only fma rate at ring depth 6). The same change to
+        // another chain count cost it 1-5 %.
         if (k >= 3) {
             const float4* w = reinterpret_cast<const float4*>(cs + k - 3);
             const float4* const w0 = reinterpret_cast<const float4*>(cs);
@@ -149,15 +149,20 @@ struct OpPolyDev {
                 }
             }
             if constexpr (N >= 24) {
-                float4 qa = w[0];
-                while (true) {
-                    const float4 qb = w[-1];
-                    steps4(p, v, qa);
-                    if (w == w0) break;
-                    qa = w[-2];
-                    steps4(p, v, qb);
-                    w -= 2;
-                    if (w < w0) break;
+                if (((k + 1) >> 2) & 1) {
+                    const float4 q = *w;
+                    --w;
+                    steps4(p, v, q);
+                }
+                if (w >= w0) {
+                    float4 q0 = w[0];
+                    do {
+                        const float4 q1 = w[-1];
+                        steps4(p, v, q0);
+                        q0 = w[-2];
+                        steps4(p, v, q1);
+                        w -= 2;
+                    } while (w >= w0);
                 }
             } else {
                 float4 q = *w;
@@ -832,10 +837,10 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
             P.groups = warps == 16 && stages % 2 == 0 && stages >= 4 ? 2 : 1;
             if (o.consumer_warps == 0 && shape.groups > 0) P.groups = static_cast<uint32_t>(shape.groups);
             if (o.consumer_groups > 0) {
-                // an explicit count must divide the warps (16: 1 or 2; 12: 1, 2 or 3) and the ring depth
+                // an explicit count must divide the warps (16: 1 or 2; 12: 1, 2 or 3; 8: 1) and the ring
+                // depth (8 warps in two groups measured 0.78-0.80 of the fma rate at degree 128)
                 const int64_t gcount = o.consumer_groups;
-                if (warps % gcount != 0 || stages % gcount != 0 || (warps == 16 && gcount == 3) || warps == 8)
-                    return AP_ERR_ARG;
+                if (warps % gcount != 0 || stages % gcount != 0 || (warps == 8 && gcount > 1)) return AP_ERR_ARG;
                 P.groups = static_cast<uint32_t>(gcount);
             }
             const int64_t round_groups = 6 * 32 * 16 / P.groups;

@@ -79,7 +79,7 @@ typedef enum ap_debug_key {
                                    takes. AP_DBG_GRID, when set, implies the persistent grid */
     AP_DBG_CONSUMER_GROUPS = 19, /* ap_poly: consumer groups that take stages in turn (group g the
                                    stages g, g + groups, ...): 0 automatic, or 1, 2, 3 where the count
-                                   divides the consumer warps (16: 1 or 2; 12: 1, 2 or 3) and the
+                                   divides the consumer warps (16: 1 or 2; 12: 1, 2 or 3; 8: 1) and the
                                    ring depth; other counts make ap_poly return AP_ERR_ARG */
     AP_DBG_LAST_SITE = 106,     /* where the error ap_check last reported was raised (kernel site code) */
     AP_DBG_LAST_RUN = 107,      /* ring: consecutive stages per CTA, 0 for the persistent grid */

@@ -90,7 +90,7 @@ def test_poly_consumer_groups_rejected(ap):
     dev = device()
     x = torch.zeros(4096, device=dev)
     y = torch.empty_like(x)
-    for warps, groups, stages in ((16, 3, 3), (12, 2, 3), (12, 3, 4), (8, 2, 4)):
+    for warps, groups, stages in ((16, 3, 3), (12, 2, 3), (12, 3, 4), (8, 2, 4), (8, 3, 6)):
         ap.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, warps)
         ap.ap_debug_set(ap.AP_DBG_CONSUMER_GROUPS, groups)
         with pytest.raises(ap.APError) as e:
