@@ -169,3 +169,40 @@ def test_tensor_map_ring_wait_times_out_and_recovers(ap, orc):
     ap.ap_row_roll(A, B, rows, cols, 1)
     assert ap.ap_check() == ap.AP_OK
     assert_bits(to_np(B), orc.row_roll(to_np(A).reshape(rows, cols), 1), "tensor roll after recovery")
+
+
+@pytest.mark.parametrize("call", ["ring", "exchange", "all_to_all"])
+def test_failed_wait_ends_the_launch_promptly(ap, call):
+    """Once one wait gives up, every other role stops: the drains do not wait
+    out the limit again for each copy still owed, so a faulted launch ends a
+    small multiple of the limit after it starts (0.2 s here; the ring's seven
+    stages in flight, or four pusher lanes with several pieces each, would
+    otherwise add seconds)."""
+    import time
+
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n = 4 * 4096 * 64 // 4
+    x = synth.uniform_pm1_torch(7, n, dev)
+    y = torch.empty_like(x)
+    ap.ap_debug_set(ap.AP_DBG_TIMEOUT_NS, 200_000_000)
+    ap.ap_debug_set(ap.AP_DBG_EXPECT_TX_EXTRA, 16)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    if call == "ring":
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 4096)
+        ap.ap_scale(x, y, n, 1, 2.0, 6)
+    elif call == "exchange":
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, 4)
+        ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, 1024)
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, 3)
+        ap.ap_cluster_exchange(x, y, n, 4, 4096)
+    else:
+        ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, 4)
+        ap.ap_cluster_all_to_all(x, y, n, 4, 4096)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    elapsed = time.perf_counter() - t0
+    assert elapsed < 1.5, f"{call}: the faulted launch took {elapsed:.2f} s with a 0.2 s wait limit"
+    reset_debug(ap)
