@@ -65,47 +65,55 @@ ap_status autotune_ring(const DeviceInfo& di, const Options& base, OpKind kind, 
     }
     double best_ms = -1.0;
     ap_status result = AP_OK;
-    // Schedules: a persistent grid of cps = 1..4 CTAs per SM, or (cps 0)
-    // runs of `runs[r]` consecutive stages per CTA.
+    // Time one shape (median of three launches after a warm-up); a shape
+    // whose ring does not fit in shared memory is skipped.
+    auto try_shape = [&](const RingShape& sh) {
+        Options o = base;
+        o.stage_bytes = sh.payload;
+        o.ctas_per_sm = sh.ctas_per_sm;
+        o.ring_run = sh.run > 0 ? sh.run : 1;  // 1: the persistent grid
+        o.consumer_warps = sh.consumer_warps;
+        o.consumer_groups = sh.groups;
+        ap_status st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);  // warm-up
+        if (st == AP_ERR_SMEM) return;
+        if (st != AP_OK) {
+            result = st;
+            return;
+        }
+        float ms_rep[3];
+        for (int r = 0; r < 3 && result == AP_OK; ++r) {
+            if (cudaEventRecord(e0, stream) != cudaSuccess) result = AP_ERR_CUDA;
+            st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);
+            if (st != AP_OK) result = st;
+            if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                cudaEventElapsedTime(&ms_rep[r], e0, e1) != cudaSuccess)
+                result = AP_ERR_CUDA;
+        }
+        if (result != AP_OK) return;
+        std::sort(ms_rep, ms_rep + 3);
+        if (best_ms < 0.0 || ms_rep[1] < best_ms) {
+            best_ms = ms_rep[1];
+            *best = sh;
+        }
+    };
+    // The built-in shape first (so the choice is never slower than it),
+    // then every stage size under both schedules: a persistent grid of
+    // cps = 1..4 CTAs per SM, or (cps 0) runs of `runs[r]` consecutive
+    // stages per CTA.
+    try_shape(auto_ring_shape(kind, stages, kind == OP_POLY ? op.degree : 0));
     const int64_t runs[3] = {stages, 2 * static_cast<int64_t>(stages), 4 * static_cast<int64_t>(stages)};
     for (int wi = 0; wi < 2 && result == AP_OK; ++wi) {
         const int warps = warp_choices[wi];
         if (kind != OP_POLY && warps != 8) continue;  // data movement: 8 consumer warps
         for (int64_t kib : kPayloadKiB) {
-            for (int64_t sched = 1; sched <= 7; ++sched) {
+            for (int64_t sched = 1; sched <= 7 && result == AP_OK; ++sched) {
                 const int64_t cps = sched <= 4 ? sched : 0;
                 const int64_t run = sched <= 4 ? 0 : runs[sched - 5];
                 // the ring of one CTA, and cps of them per SM, must fit in shared memory
                 const int64_t per_cta = static_cast<int64_t>(stages) * (kib * 1024 + 176) + 16 * stages + 4096;
                 if (per_cta > di.smem_optin || cps * (per_cta + 1024) > kSmemPerSM) continue;
                 if (kind == OP_POLY && cps > 1) continue;  // 16 warps x 92 registers: one CTA per SM
-                Options o = base;
-                o.stage_bytes = kib * 1024;
-                o.ctas_per_sm = cps > 0 ? cps : 1;
-                o.ring_run = run > 0 ? run : 1;  // 1: the persistent grid
-                o.consumer_warps = warps;
-                ap_status st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);  // warm-up
-                if (st == AP_ERR_SMEM) continue;
-                if (st != AP_OK) {
-                    result = st;
-                    break;
-                }
-                float ms_rep[3];
-                for (int r = 0; r < 3 && result == AP_OK; ++r) {
-                    if (cudaEventRecord(e0, stream) != cudaSuccess) result = AP_ERR_CUDA;
-                    st = launch_ring(di, o, in, out, n, off, unit, stages, op, false, stream);
-                    if (st != AP_OK) result = st;
-                    if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
-                        cudaEventElapsedTime(&ms_rep[r], e0, e1) != cudaSuccess)
-                        result = AP_ERR_CUDA;
-                }
-                if (result != AP_OK) break;
-                std::sort(ms_rep, ms_rep + 3);
-                const double ms = ms_rep[1];
-                if (best_ms < 0.0 || ms < best_ms) {
-                    best_ms = ms;
-                    *best = RingShape{kib * 1024, cps > 0 ? cps : 1, warps, run};
-                }
+                try_shape(RingShape{kib * 1024, cps > 0 ? cps : 1, warps, run});
             }
             if (result != AP_OK) break;
         }

@@ -249,8 +249,9 @@ ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const in
  * the operation over in/out for every stage size from 8 to 96 KiB, under
  * both schedules: a persistent grid of 1-4 CTAs per SM (whose shared memory
  * fits), and CTAs that each take a run of depth, 2 x depth or 4 x depth
- * consecutive stages. Three timed launches each (CUDA events on `stream`,
- * median); it keeps the fastest and installs it:
+ * consecutive stages, and the built-in shape for that operation and depth.
+ * Three timed launches each (CUDA events on `stream`, median); it keeps the
+ * fastest and installs it:
  * later calls of that operation with that depth on this device use it
  * instead of the built-in defaults (explicit ap_debug_set settings still
  * win). Blocks until the timing is done.
@@ -271,7 +272,8 @@ typedef struct ap_ring_shape {
     int ctas_per_sm;     /* persistent grid: resident CTAs per SM the grid is sized for */
     int consumer_warps;  /* consumer warps per CTA */
     int stages_per_cta;  /* 0: persistent grid; r: every CTA takes r consecutive stages */
-    int consumer_groups; /* ap_poly: consumer groups taking stages in turn (1 or 2) */
+    int consumer_groups; /* ap_poly: consumer groups taking stages in turn (1-3; 0: two for 16
+                            warps at even depths of 4 or more, else one) */
     double gbs;          /* measured rate of the chosen shape, GB/s */
 } ap_ring_shape;
 

@@ -51,7 +51,7 @@ def test_autotune_poly_and_roll(ap, orc):
     x = synth.uniform_pm1_torch(synth.SEED_POLY, n, dev)
     scratch = torch.empty_like(x)
     shape = ap.ap_autotune(ap.AP_TUNE_POLY, x, scratch, n, 3, degree=32)
-    assert shape["consumer_warps"] in (8, 16)
+    assert shape["consumer_warps"] in (8, 12, 16)
     c = synth.coeffs_np(32)
     m = 1 << 20
     y = torch.empty(m, device=dev)

@@ -219,3 +219,53 @@ def test_scale_pages_async_baseline(ap, orc, n_tiles, tile):
     assert ap.ap_debug_get(ap.AP_DBG_LAST_PATH) == 6
     assert_bits(to_np(out.view), orc.scale(to_np(x), 2.0), f"pages async {n_tiles}x{tile}")
     assert out.intact()
+
+
+@pytest.mark.parametrize("op", ["scale", "roll", "poly"])
+def test_beyond_2p32_elements(ap, orc, op):
+    """The largest buffers exercised: 2^32 + 1028 floats (16 GiB in and 16 GiB
+    out, an input 4 bytes past a 16-byte boundary), so element indices and
+    byte offsets pass 2^32 and 2^34 inside the planner, the regular-stage
+    shortcut and the consumers. Checked against the oracle at the first and
+    last 1 Mi elements and 1 Mi random positions (each computed one by one by
+    the oracle); the row shift wraps its last stage to row 0."""
+    import torch
+
+    dev = device()
+    n = (1 << 32) + 1028
+    base = torch.empty(n + 1, dtype=torch.float32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xA5A5)
+    base.uniform_(-1.0, 1.0, generator=g)
+    x = base[1:]  # 4 bytes past the allocation's 16-byte boundary
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    rng = np.random.default_rng(3)
+    idx_h = np.unique(np.concatenate([np.arange(1 << 20), np.arange(n - (1 << 20), n),
+                                      rng.integers(0, n, 1 << 20)]))
+    idx = torch.from_numpy(idx_h).to(dev)
+    if op == "scale":
+        ap.ap_scale(x, y, n, 1, -3.0, 4)
+        want = orc.scale(to_np(x[idx]), -3.0)
+    elif op == "roll":
+        rows, cols = n // 4, 4
+        shift = 7
+        ap.ap_row_roll(x, y, rows, cols, shift)
+        assert ap.ap_check() == ap.AP_OK
+        # Output rows [r0, r0 + k) need input rows r0 .. r0 + k + shift - 1
+        # (mod rows): the oracle shifts that window, and its first k rows are
+        # the expected output rows. Windows at the start, across the wrap at
+        # the end, and at random rows.
+        starts = [0, rows - 4096] + [int(r) for r in rng.integers(0, rows - 16, 256)]
+        for r0 in starts:
+            k = 4096 if r0 in (0, rows - 4096) else 16
+            src_rows = torch.remainder(torch.arange(r0, r0 + k + shift, device=dev), rows)
+            window = to_np(x.view(rows, cols)[src_rows])
+            want = orc.row_roll(window, shift)[:k]
+            assert_bits(to_np(y.view(rows, cols)[r0:r0 + k]), want, f"roll beyond 2^32, rows {r0}..{r0 + k}")
+        return
+    else:
+        c = synth.coeffs_np(8)
+        ap.ap_poly(x, y, n, c.tolist(), 8, 3)
+        want = orc.poly(to_np(x[idx]), c)
+    assert ap.ap_check() == ap.AP_OK
+    assert_bits(to_np(y[idx]), want, f"{op} over 2^32 + 1028 elements")
