@@ -367,7 +367,8 @@ ap_status ap_masked_copy(const float* in, float* out, int64_t n_chunks, const in
     DeviceInfo di;
     const ap_status st = current_device(&di);
     if (st != AP_OK) return st;
-    return launch_masked_copy(di, in, out, n_chunks, reinterpret_cast<const signed char*>(codes), stages, stream);
+    return launch_masked_copy(di, options(), in, out, n_chunks, reinterpret_cast<const signed char*>(codes), stages,
+                              stream);
 }
 
 ap_status ap_autotune(ap_tune_op op, const float* in, float* out, int64_t n, int stages, int degree,

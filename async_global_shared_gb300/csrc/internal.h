@@ -118,7 +118,7 @@ ap_status launch_scale_sync(const DeviceInfo& di, const float* in, float* out, i
 ap_status launch_scale_pages_async(const DeviceInfo& di, const float* in, float* out, int64_t n_tiles, int64_t tile,
                                    float alpha, cudaStream_t stream);
 
-ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, int64_t n_chunks,
+ap_status launch_masked_copy(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n_chunks,
                              const signed char* codes, int stages, cudaStream_t stream);
 
 ap_status launch_fma_probe(const DeviceInfo& di, float* out, int64_t out_elems, int64_t iters, cudaStream_t stream);

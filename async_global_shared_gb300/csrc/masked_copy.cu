@@ -31,16 +31,19 @@ struct McParams {
     const signed char* codes;
     int64_t n_chunks;
     uint32_t* status;
+    int64_t run_chunks;  // 0: persistent grid (CTA b takes stages b, b + grid, ...); else chunks a CTA takes
 };
 
 // This thread's codes of the stage at `base` (chunk base + tid + u * kMcThreads
-// for u < kMcChunks), -1 past the end; loaded one iteration before they are
-// needed so the load latency hides behind the current stage.
-__device__ __forceinline__ void load_codes(const McParams& P, int64_t base, int tid, int (&c)[kMcChunks]) {
+// for u < kMcChunks), -1 past `limit` (the end of the CTA's chunks); loaded one
+// iteration before they are needed so the load latency hides behind the
+// current stage.
+__device__ __forceinline__ void load_codes(const McParams& P, int64_t base, int64_t limit, int tid,
+                                           int (&c)[kMcChunks]) {
 #pragma unroll
     for (int u = 0; u < kMcChunks; ++u) {
         const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
-        c[u] = k < P.n_chunks ? static_cast<int>(P.codes[k]) : -1;
+        c[u] = k < limit ? static_cast<int>(P.codes[k]) : -1;
     }
 }
 
@@ -68,27 +71,37 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
     const uint32_t base_addr = ptx::smem_addr(smem);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kMcStageChunks;
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * kMcStageChunks;
+    // This CTA's stages: a persistent grid's b, b + grid, ..., or the run of
+    // consecutive stages in [first, limit).
+    int64_t stride, first, limit;
+    if (P.run_chunks == 0) {
+        stride = static_cast<int64_t>(gridDim.x) * kMcStageChunks;
+        first = static_cast<int64_t>(blockIdx.x) * kMcStageChunks;
+        limit = P.n_chunks;
+    } else {
+        stride = kMcStageChunks;
+        first = static_cast<int64_t>(blockIdx.x) * P.run_chunks;
+        limit = first + P.run_chunks < P.n_chunks ? first + P.run_chunks : P.n_chunks;
+    }
     signed char* codes = reinterpret_cast<signed char*>(smem + static_cast<size_t>(S) * kMcStageChunks * 16);
 
     // prologue: stages 0 .. S-2 in flight (empty groups keep the count right)
     int c[kMcChunks];
 #pragma unroll
     for (int t = 0; t < S - 1; ++t) {
-        load_codes(P, first + t * stride, tid, c);
+        load_codes(P, first + t * stride, limit, tid, c);
         issue_stage(P, base_addr + t * kMcStageChunks * 16u, codes + t * kMcStageChunks, first + t * stride, tid, c);
         ptx::cp_async_commit();
     }
-    load_codes(P, first + (S - 1) * stride, tid, c);
+    load_codes(P, first + (S - 1) * stride, limit, tid, c);
     int slot = 0;  // stage t's slot, t mod S
-    for (int64_t base = first; base < P.n_chunks; base += stride, slot = slot + 1 == S ? 0 : slot + 1) {
+    for (int64_t base = first; base < limit; base += stride, slot = slot + 1 == S ? 0 : slot + 1) {
         const int next = slot == 0 ? S - 1 : slot - 1;  // (t + S - 1) mod S
         // acquire + commit the stage S - 1 ahead (its slot was released last iteration)
         issue_stage(P, base_addr + next * kMcStageChunks * 16u, codes + next * kMcStageChunks, base + (S - 1) * stride,
                     tid, c);
         ptx::cp_async_commit();
-        load_codes(P, base + S * stride, tid, c);  // for the next iteration
+        load_codes(P, base + S * stride, limit, tid, c);  // for the next iteration
         // wait: at most S - 1 groups pending, so this thread's copies of stage t have landed
         ptx::cp_async_wait_group<S - 1>();
         const unsigned char* sl = smem + static_cast<size_t>(slot) * kMcStageChunks * 16;
@@ -96,7 +109,7 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
         for (int u = 0; u < kMcChunks; ++u) {
             const int code = codes[slot * kMcStageChunks + tid + u * kMcThreads];
             const int64_t k = base + tid + static_cast<int64_t>(u) * kMcThreads;
-            if (k >= P.n_chunks || code == -1) continue;
+            if (k >= limit || code == -1) continue;
             if (code < -2 || code > 16) {
                 atomicCAS(P.status, 0u, 11u /* AP_ERR_ARG */ | (SITE_MASKED_CODE << 8));
                 continue;
@@ -110,13 +123,23 @@ __global__ void __launch_bounds__(kMcThreads) masked_copy_kernel(const __grid_co
 }
 
 template <int S>
-ap_status launch_masked_s(const DeviceInfo& di, const McParams& P, cudaStream_t stream) {
+ap_status launch_masked_s(const DeviceInfo& di, McParams P, int64_t run, cudaStream_t stream) {
     const int64_t stages_total = (P.n_chunks + kMcStageChunks - 1) / kMcStageChunks;
-    // Two CTAs per SM at every depth: measured on 2^26 plain chunks, one CTA
-    // per SM reached 0.73 of the copy, two 0.95, three 0.86-0.92 and four (the
-    // earlier choice at depths 2-3) 0.93.
-    int64_t grid = static_cast<int64_t>(di.sms) * 2;
-    if (grid > stages_total) grid = stages_total;
+    int64_t grid;
+    if (run > 0) {
+        // runs of `run` consecutive stages per CTA, as many CTAs as that takes
+        const int64_t cap = int64_t(1) << 30;
+        if ((stages_total + run - 1) / run > cap) run = (stages_total + cap - 1) / cap;
+        grid = (stages_total + run - 1) / run;
+        P.run_chunks = run * kMcStageChunks;
+    } else {
+        // persistent: two CTAs per SM at every depth (measured on 2^26 plain
+        // chunks: one CTA per SM 0.73 of the copy, two 0.95, three 0.86-0.92,
+        // four 0.93)
+        grid = static_cast<int64_t>(di.sms) * 2;
+        if (grid > stages_total) grid = stages_total;
+        P.run_chunks = 0;
+    }
     if (grid < 1) grid = 1;
     const size_t smem = static_cast<size_t>(S) * kMcStageChunks * 17;  // data + one code byte per chunk
     static std::atomic<int> configured[64];  // attribute set on this device (setting twice is harmless)
@@ -128,22 +151,31 @@ ap_status launch_masked_s(const DeviceInfo& di, const McParams& P, cudaStream_t 
         configured[di.device] = 1;
     }
     record_launch(PATH_MASKED, grid, kMcStageChunks * 4, static_cast<int64_t>(smem), S, 0);
+    record_ring_shape(P.run_chunks / kMcStageChunks, kMcThreads / 32, 1, 0);
     masked_copy_kernel<S><<<static_cast<unsigned>(grid), kMcThreads, smem, stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? AP_OK : AP_ERR_CUDA;
 }
 
 }  // namespace
 
-ap_status launch_masked_copy(const DeviceInfo& di, const float* in, float* out, int64_t n_chunks,
+ap_status launch_masked_copy(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t n_chunks,
                              const signed char* codes, int stages, cudaStream_t stream) {
     McParams P{reinterpret_cast<const unsigned char*>(in), reinterpret_cast<unsigned char*>(out), codes, n_chunks,
-               di.status};
+               di.status, 0};
+    // Schedule (AP_DBG_RING_RUN: 1 persistent, r >= 2 runs of r stages).
+    // Automatic: at depths 2-4 (up to 68 KiB of shared memory a CTA, three
+    // CTAs a SM) runs of one pipeline's worth of stages, so the grid streams
+    // one narrow window of memory: plain chunks 0.976 -> 1.031-1.042 of the
+    // copy, mixed codes 0.63 -> 0.67 (2^26 chunks). At depths 5-6 (two CTAs
+    // a SM) a run's start is exposed and the persistent grid stays faster
+    // (0.973 against 0.88-0.94).
+    const int64_t run = o.ring_run >= 2 ? o.ring_run : (o.ring_run == 1 || stages > 4 ? 0 : stages);
     switch (stages) {
-        case 2: return launch_masked_s<2>(di, P, stream);
-        case 3: return launch_masked_s<3>(di, P, stream);
-        case 4: return launch_masked_s<4>(di, P, stream);
-        case 5: return launch_masked_s<5>(di, P, stream);
-        default: return launch_masked_s<6>(di, P, stream);
+        case 2: return launch_masked_s<2>(di, P, run, stream);
+        case 3: return launch_masked_s<3>(di, P, run, stream);
+        case 4: return launch_masked_s<4>(di, P, run, stream);
+        case 5: return launch_masked_s<5>(di, P, run, stream);
+        default: return launch_masked_s<6>(di, P, run, stream);
     }
 }
 

@@ -230,7 +230,9 @@ ap_status ap_cluster_all_to_all(const float* in, float* out, int64_t n, int clus
  * Copy, which names exactly these three forms of the 16-byte copy (a false
  * predicate, a source size, an ignored source). The chunks stream through a
  * per-thread cp.async pipeline of `stages` commit groups into shared memory
- * and out with 16-byte stores.
+ * and out with 16-byte stores; at depths 2-4 each CTA takes one pipeline's
+ * worth of consecutive stages (1024 chunks a stage), at 5-6 a persistent
+ * grid of two CTAs a SM walks them.
  *  in, out     device arrays of 4 * n_chunks floats, 16-byte aligned
  *              (AP_ERR_ALIGN); in == out is allowed, other overlap is not.
  *  n_chunks    >= 0.

@@ -73,10 +73,12 @@ typedef enum ap_debug_key {
                                    all-to-all; where none fits, one ring depth); 1 never split;
                                    0 automatic (the all-to-all splits where its ring depth is a power
                                    of two, with that many send buffers) */
-    AP_DBG_RING_RUN = 18,       /* ring schedule: 0 automatic; 1 a persistent grid (SMs x CTAs per SM
-                                   CTAs, CTA b taking stages b, b + grid, ...); r = 2 .. 2^20 every
-                                   CTA takes r consecutive stages and as many CTAs launch as that
-                                   takes. AP_DBG_GRID, when set, implies the persistent grid */
+    AP_DBG_RING_RUN = 18,       /* schedule of the ring calls and of ap_masked_copy: 0 automatic; 1 a
+                                   persistent grid (SMs x CTAs per SM CTAs, CTA b taking stages b,
+                                   b + grid, ...); r = 2 .. 2^20 every CTA takes r consecutive stages
+                                   (masked copy: of 1024 chunks) and as many CTAs launch as that
+                                   takes. AP_DBG_GRID, when set, implies the persistent grid for the
+                                   ring calls */
     AP_DBG_CONSUMER_GROUPS = 19, /* ap_poly: consumer groups that take stages in turn (group g the
                                    stages g, g + groups, ...): 0 automatic, or 1, 2, 3 where the count
                                    divides the consumer warps (16: 1 or 2; 12: 1, 2 or 3; 8: 1) and the

@@ -41,6 +41,28 @@ def test_masked_copy_random_codes(ap, orc, stages, n_chunks):
     assert out.intact()
 
 
+@pytest.mark.parametrize("stages", [2, 3, 6])
+@pytest.mark.parametrize("run", [1, 2, 3, 7, 12])
+@pytest.mark.parametrize("n_chunks", [1, 1025, 100003])
+def test_masked_copy_stage_runs(ap, orc, stages, run, n_chunks):
+    """Both schedules: the persistent grid (run 1) and CTAs that each take a
+    run of consecutive stages of 1024 chunks, with a short last run, runs
+    shorter and longer than the pipeline's depth, and random codes."""
+    dev = device()
+    rng = np.random.default_rng(7 * n_chunks + run)
+    x = synth.uniform_pm1_torch(n_chunks + run, 4 * n_chunks, dev)
+    before = synth.uniform_pm1_torch(n_chunks + 2, 4 * n_chunks, dev)
+    c_h, c_d = _codes(rng, n_chunks, dev)
+    ap.ap_debug_set(ap.AP_DBG_RING_RUN, run)
+    out = Guarded(4 * n_chunks, 0, dev, fill=before)
+    ap.ap_masked_copy(x, out.view, n_chunks, c_d, stages)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_RUN) == (0 if run == 1 else run)
+    assert_bits(to_np(out.view), orc.masked_copy(to_np(x), to_np(before), c_h),
+                f"masked n={n_chunks} S={stages} run={run}")
+    assert out.intact()
+
+
 def test_masked_copy_worked_example(ap):
     import torch
 
