@@ -194,6 +194,21 @@ def test_debug_settings_roundtrip(ap):
     for removed in (10, 12):  # the cache-hint and stage-order keys gained nothing and were removed
         assert lib.ap_debug_set(removed, 0) == ap.AP_ERR_ARG
         assert lib.ap_debug_get(removed) == -1
+    for good in (0, 1, 2, 12, 1 << 20):
+        assert lib.ap_debug_set(ap.AP_DBG_RING_RUN, good) == ap.AP_OK
+        assert ap.ap_debug_get(ap.AP_DBG_RING_RUN) == good
+    assert lib.ap_debug_set(ap.AP_DBG_RING_RUN, (1 << 20) + 1) == ap.AP_ERR_ARG
+    ap.ap_debug_set(ap.AP_DBG_RING_RUN, 0)
+    for good in (0, 1, 2, 3):
+        assert lib.ap_debug_set(ap.AP_DBG_CONSUMER_GROUPS, good) == ap.AP_OK
+    assert lib.ap_debug_set(ap.AP_DBG_CONSUMER_GROUPS, 4) == ap.AP_ERR_ARG
+    for good in (0, 8, 12, 16):
+        assert lib.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, good) == ap.AP_OK
+    for bad in (4, 15, 32):  # 15 warps left one SMSP a warp short and was replaced by 12
+        assert lib.ap_debug_set(ap.AP_DBG_CONSUMER_WARPS, bad) == ap.AP_ERR_ARG
+    for key in (ap.AP_DBG_LAST_RUN, ap.AP_DBG_LAST_WARPS, ap.AP_DBG_LAST_GROUPS, ap.AP_DBG_LAST_CHAINS):
+        assert ap.ap_debug_get(key) >= 0  # read-only, known
+        assert lib.ap_debug_set(key, 1) == ap.AP_ERR_ARG
 
 
 @pytest.mark.skipif(
