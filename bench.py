@@ -579,13 +579,26 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     for cs in (4, 8, 16):
         put(f"cluster all-to-all cs={cs}, 32 KiB chunks", 8 * n,
             lambda: ap.ap_cluster_all_to_all(x, y, n, cs, 32768, stream))
+    # The mixed pattern, then the same codes taken apart: a chunk left
+    # unchanged (code -1) beside a written one leaves its 32-byte sector half
+    # written, and the L2 fetches such a sector from DRAM before writing it
+    # back; half and zeroed chunks, or chunks left in whole sectors, do not.
+    plain_ms = None
     for name, pattern in (("all chunks copied", [16]),
-                          ("1/8 off, 1/8 half, 1/8 zeroed, 5/8 copied", [-1, 8, -2, 16, 16, 16, 16, 16])):
+                          ("1/8 off, 1/8 half, 1/8 zeroed, 5/8 copied", [-1, 8, -2, 16, 16, 16, 16, 16]),
+                          ("1/8 half, 1/8 zeroed, 6/8 copied (no chunk left)", [8, -2, 16, 16, 16, 16, 16, 16]),
+                          ("1/8 off, 7/8 copied (a half-written sector in four)", [-1, 16, 16, 16, 16, 16, 16, 16]),
+                          ("2/8 off in whole sectors, 6/8 copied", [-1, -1, 16, 16, 16, 16, 16, 16])):
         codes = torch.tensor(pattern, dtype=torch.int8).repeat(n // 4 // len(pattern)).to(dev)
         # per 16-byte chunk: the bytes it reads, the 16 it writes unless predicated off, 1 code byte
         rd = sum(max(c, 0) for c in pattern) / len(pattern)
         wr = sum(16 for c in pattern if c != -1) / len(pattern)
-        put(f"masked copy, {name}", (n // 4) * (rd + wr + 1), lambda: ap.ap_masked_copy(x, y, n // 4, codes, 4, stream))
+        key = f"masked copy, {name}"
+        ms = put(key, (n // 4) * (rd + wr + 1), lambda: ap.ap_masked_copy(x, y, n // 4, codes, 4, stream))
+        if plain_ms is None:
+            plain_ms = ms
+        else:
+            out[key]["time_vs_all_copied"] = round(ms / plain_ms, 4)
         del codes
     xp = synth.uniform_pm1_torch(synth.SEED_POLY, 1 << 30, dev)
     yp = torch.empty_like(xp)
