@@ -110,6 +110,35 @@ def test_all_to_all_split_rings(ap, orc, cs, store, group, lanes, send):
         assert out.intact()
 
 
+@pytest.mark.parametrize("chunk_bytes,groups", [(32768, 1), (32768, 300), (65536, 97), (40960, 61)])
+def test_all_to_all_three_ctas_per_sm(ap, orc, chunk_bytes, groups):
+    """Clusters of 8 with sub-blocks of 4 KiB or more run three CTAs per SM
+    (8 send and 8 receive slots of 4 KiB, the register-capped instantiation):
+    more CTAs than two a SM are resident, and the result is bit-exact, from
+    one group to many rounds of the ring; an explicit CTAs-per-SM setting of
+    two plans the two-CTA ring instead."""
+    import torch
+
+    dev = device()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cs = 8
+    n = groups * cs * chunk_bytes // 4
+    x = synth.uniform_pm1_torch(n + 3, n, dev)
+    want = orc.cluster_all_to_all(to_np(x), cs, chunk_bytes)
+    for cps in (0, 2):
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, cps)
+        out = Guarded(n, 0, dev)
+        ap.ap_cluster_all_to_all(x, out.view, n, cs, chunk_bytes)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), want, f"a2a cs=8 chunk={chunk_bytes} groups={groups} cps={cps}")
+        assert out.intact()
+        if chunk_bytes in (32768, 65536):  # 4 KiB pieces either way; 40 KiB chunks take 1280-byte pieces
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS) == 1024
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGES) == (8 if cps == 0 else 16)
+        if cps == 0 and groups >= 60:
+            assert ap.ap_debug_get(ap.AP_DBG_LAST_GRID) > 2 * sms, "three CTAs a SM expected"
+
+
 @pytest.mark.parametrize("cs", [2, 4, 8, 16])
 def test_all_to_all_full_size(ap, orc, cs):
     """2**28 floats in 32 KiB chunks (32768 chunks)."""

@@ -117,6 +117,26 @@ def test_all_to_all_wait_times_out_and_recovers(ap, orc, store, group, lanes, se
     assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), 4, 4096), "all-to-all after recovery")
 
 
+def test_all_to_all_three_ctas_wait_times_out_and_recovers(ap, orc):
+    """The same for clusters of 8 with 4 KiB sub-blocks, which run the
+    register-capped three-CTAs-per-SM instantiation."""
+    import torch
+
+    dev = device()
+    assert ap.ap_check() == ap.AP_OK
+    n = 8 * 32768 * 6 // 4
+    x = synth.uniform_pm1_torch(6, n, dev)
+    y = torch.empty_like(x)
+    _inject(ap)
+    ap.ap_cluster_all_to_all(x, y, n, 8, 32768)
+    assert ap.ap_check() == ap.AP_ERR_DEVICE_TIMEOUT
+    reset_debug(ap)
+    ap.ap_cluster_all_to_all(x, y, n, 8, 32768)
+    assert ap.ap_check() == ap.AP_OK
+    assert ap.ap_debug_get(ap.AP_DBG_LAST_STAGES) == 8
+    assert_bits(to_np(y), orc.cluster_all_to_all(to_np(x), 8, 32768), "all-to-all after recovery")
+
+
 def test_batched_exchange_wait_times_out_and_recovers(ap, orc):
     """The batched form's bounded waits (its loader barrier never completes)."""
     import torch
