@@ -716,12 +716,14 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     // way), one warp per piece from 9 (16: 0.85, against 0.76). All-to-all
     // (pieces from every sender, in no fixed order, so in-order draining waits
     // on the slowest sender): bulk stores for clusters of 1-2 (1.01-1.02), one
-    // warp per piece from 3 up (0.91-1.01; eight warps per piece: 0.53-0.56).
+    // warp per piece from 3 up (0.91-1.01; eight warps per piece: 0.53-0.56),
+    // two with 4 KiB pieces at three CTAs per SM (clusters of 8, 32 and 64 KiB
+    // chunks: 0.977 against 0.960 with one and 0.89-0.90 with four).
     const bool fixed_bulk = !a2a && (cs == 3 || cs == 4 || cs == 5 || cs == 8);
     const bool tma_store =
         batch > 0 || o.ex_tma_store == 1 || (o.ex_tma_store == 0 && ((a2a && cs <= 2) || fixed_bulk));
     const int64_t rgroup = o.ex_group > 0        ? o.ex_group
-                           : a2a                 ? 1
+                           : a2a                 ? (cps >= 3 && piece >= 4096 ? 2 : 1)
                            : (cs <= 5 || cs == 8) ? kExConsumerWarps
                            : cs <= 7             ? 4
                                                  : 1;
