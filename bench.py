@@ -1029,7 +1029,8 @@ def sweep(which: str, args):
 
 PROFILE_CASES = ("scale", "scale_s6", "sync", "poly0", "poly8", "poly32", "poly32_s4", "poly32_s6", "poly128",
                  "poly128_s6", "roll", "roll_mis", "roll_tensor", "exchange2", "exchange4", "exchange8", "exchange16",
-                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "masked_mixed", "masked_all", "torch_mul_2p28")
+                 "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "masked_mixed", "masked_all", "masked_off1",
+                 "masked_offpair", "masked_halfzero", "torch_mul_2p28")
 
 
 def profile_case(name: str, args):
@@ -1058,6 +1059,11 @@ def profile_case(name: str, args):
     y = torch.empty_like(x)
     codes = torch.tensor([-1, 8, -2, 16, 16, 16, 16, 16], dtype=torch.int8).repeat(n // 32).to(dev)
     codes16 = torch.full((n // 4,), 16, dtype=torch.int8, device=dev)
+
+    def pattern(p):  # per-chunk codes repeating p over the case's n / 4 chunks
+        return torch.tensor(p, dtype=torch.int8).repeat(n // 4 // len(p)).to(dev)
+
+    rest = [16] * 6
     calls = {
         "scale": lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, 2),
         "sync": lambda: ap.ap_scale_sync(x[:n], y[:n], n // 256, 256, 2.0),
@@ -1084,6 +1090,13 @@ def profile_case(name: str, args):
         "masked_mixed": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
         "masked_all": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes16, 4),
     }
+    # the mixed pattern taken apart: one chunk left in eight, two adjacent
+    # chunks left (whole sectors), a half and a zeroed chunk in eight
+    for key, p in (("masked_off1", [-1, 16] + rest), ("masked_offpair", [-1, -1] + rest),
+                   ("masked_halfzero", [8, -2] + rest)):
+        if name == key:
+            pc = pattern(p)
+            calls[key] = lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, pc, 4)
     if name == "roll_tensor":
         ap.ap_debug_set(ap.AP_DBG_FORCE_PATH, 3)
     fn = calls[name]
