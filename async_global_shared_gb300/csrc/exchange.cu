@@ -555,11 +555,11 @@ __global__ void __launch_bounds__(kExThreads, kMinBlocks) exchange_kernel(const 
 ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* in, float* out, int64_t groups, int cs,
                           int64_t chunk_bytes, int64_t shift, bool a2a, cudaStream_t stream) {
     // Piece: the largest multiple of 16 dividing chunk_bytes that is at most
-    // the target (8 KiB, or the stage-bytes setting), and two CTAs per SM.
-    // Measured on GB300 with 32 KiB chunks: the loader and pusher are single
-    // threads with a fixed cost per piece, so pieces much below 8 KiB starve
-    // them, and a second CTA per SM doubles those threads; whole 32 KiB chunks
-    // leave too few slots in flight.
+    // the target (8 KiB, or the stage-bytes setting), and two CTAs per SM
+    // (three for the all-to-all below). Measured on GB300 with 32 KiB chunks:
+    // the loader and pusher are single threads with a fixed cost per piece,
+    // so pieces much below 8 KiB starve them, and a second CTA per SM doubles
+    // those threads; whole 32 KiB chunks leave too few slots in flight.
     const int64_t target = o.stage_bytes > 0 ? o.stage_bytes : 8192;
     // Shared memory per CTA when `cps` CTAs share an SM (228 KiB per SM, 1 KiB
     // reserved per CTA): more resident CTAs let clusters of 8 fill more SMs.
@@ -569,7 +569,8 @@ ap_status launch_exchange(const DeviceInfo& di, const Options& o, const float* i
     // receive slots of 4 KiB a CTA, and the loads in flight per SM go from 64
     // to 96 KiB (2^28 floats, 32 KiB chunks: 0.935 -> 0.966 of the copy;
     // 64 KiB chunks: 0.934 -> 0.972); clusters of 16 with 64 KiB chunks
-    // (2 KiB pieces) 0.68 -> 0.74. The other forms lost up to 4 % with that
+    // (2 KiB pieces) 0.68 -> 0.74. Two receiver warps per 4 KiB piece then
+    // take it to 0.977 (below). The other forms lost up to 4 % with that
     // register cap, and the all-to-all at 4 CTAs gained nothing from a third
     // CTA.
     const bool a2a_three =
