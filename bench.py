@@ -219,6 +219,24 @@ def time_steps(fn, steps: int, warmup: int, stream, dist_ctx=None) -> float:
     return start.elapsed_time(end)
 
 
+def time_each(fn, steps: int, warmup: int, stream) -> list:
+    """Milliseconds of each of `steps` back-to-back calls of fn(): one CUDA
+    event recorded on `stream` between consecutive calls, after `warmup`
+    untimed calls."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for k in range(steps):
+        fn()
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+
+
 class Dist:
     def __init__(self):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -540,8 +558,9 @@ def bench_scale(args, d: Dist) -> dict:
 
 def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     """Every kernel of the path at its workload's full size, 20 timed launches
-    after 3 warm-up (CUDA events), as GB/s (read + write bytes) and the
-    fraction of the measured copy. Timed separately from the headline: the
+    after 3 warm-up (a CUDA event between launches), as GB/s (read + write
+    bytes) over the mean launch and the fraction of the measured copy, with
+    the median and best single launch beside them. Timed separately from the headline: the
     synchronous and the pages' asynchronous scale, the ring's scale and row
     shift at every ring depth, the cluster calls, the masked copy, all 16
     (degree, depth) cells of the polynomial sweep and the two FP32 roofs."""
@@ -550,9 +569,13 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     out = {}
 
     def put(name, nbytes, fn, **extra):
-        ms = time_steps(fn, 20, 3, stream) / 20
+        # 20 launches back to back after 3 warm-up: the mean (the rates
+        # below), and the median and best single launch
+        each = sorted(time_each(fn, 20, 3, stream))
+        ms = sum(each) / len(each)
         gb = nbytes / (ms * 1e-3) / 1e9
-        out[name] = {"GB/s": round(gb, 1), "frac": round(gb / peak, 4), "ms": round(ms, 4), **extra}
+        out[name] = {"GB/s": round(gb, 1), "frac": round(gb / peak, 4), "ms": round(ms, 4),
+                     "ms_median": round((each[9] + each[10]) / 2, 4), "ms_best": round(each[0], 4), **extra}
         return ms
 
     n = x.numel()  # 2^28 floats
@@ -608,6 +631,10 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
             key = f"poly K={K}, 2^30, S={S}"
             ms = put(key, 8 * (1 << 30), lambda: ap.ap_poly(xp, yp, 1 << 30, c, K, S, stream))
             out[key]["fp32_tflops"] = round(2.0 * K * (1 << 30) / (ms * 1e-3) / 1e12, 2)
+            if K == 0:
+                # degree 0 needs only the writes: its rate over the 4 B an element
+                # that minimum moves, beside the 8 B the ring streams
+                out[key]["write_only_GB/s"] = round(4 * (1 << 30) / (ms * 1e-3) / 1e9, 1)
     del xp, yp
     # The FP32 roofs under the same clocks: register-only fma chains, and the
     # operand pattern of the Horner loop (a coefficient read from shared memory
