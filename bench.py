@@ -558,9 +558,9 @@ def bench_scale(args, d: Dist) -> dict:
 
 def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     """Every kernel of the path at its workload's full size, 20 timed launches
-    after 3 warm-up (a CUDA event between launches), as GB/s (read + write
-    bytes) over the mean launch and the fraction of the measured copy, with
-    the median and best single launch beside them. Timed separately from the headline: the
+    after 3 warm-up (CUDA events), as GB/s (read + write bytes) over the mean
+    launch and the fraction of the measured copy, with the median and best
+    single launch of 20 more beside them. Timed separately from the headline: the
     synchronous and the pages' asynchronous scale, the ring's scale and row
     shift at every ring depth, the cluster calls, the masked copy, all 16
     (degree, depth) cells of the polynomial sweep and the two FP32 roofs."""
@@ -569,10 +569,13 @@ def per_kernel_lines(ap, synth, dev, stream, peak, x, y) -> dict:
     out = {}
 
     def put(name, nbytes, fn, **extra):
-        # 20 launches back to back after 3 warm-up: the mean (the rates
-        # below), and the median and best single launch
-        each = sorted(time_each(fn, 20, 3, stream))
-        ms = sum(each) / len(each)
+        # 20 launches back to back after 3 warm-up, timed as one region (the
+        # mean launch: the rates below); then 20 more with an event between
+        # launches for the median and best single launch (an event between
+        # two launches keeps the second from starting under the first's tail,
+        # which costs a 0.3 ms launch about 2 us)
+        ms = time_steps(fn, 20, 3, stream) / 20
+        each = sorted(time_each(fn, 20, 0, stream))
         gb = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"GB/s": round(gb, 1), "frac": round(gb / peak, 4), "ms": round(ms, 4),
                      "ms_median": round((each[9] + each[10]) / 2, 4), "ms_best": round(each[0], 4), **extra}
