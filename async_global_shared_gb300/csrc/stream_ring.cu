@@ -350,8 +350,7 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         // 17 warps (16 consumers + producer) leave at most 96 registers a
         // thread, too few for 32 chains: 16 chains there, or 24 (six groups)
         // where the op asks for them (a polynomial of degree 64 or more whose
-        // stages are whole rounds of six groups a thread, or of degree 32 or
-        // more whose stages are exactly one such round: 1.5-4 % faster;
+        // stages are whole rounds of six groups a thread: 1.5-4 % faster;
         // the 16-chain loop stays faster at low degree and for a six-plus-two
         // split). The choice is the host's: a per-stage test here cost the
         // low-degree loop 2 %.
