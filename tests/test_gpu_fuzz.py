@@ -100,7 +100,7 @@ def test_exchange_fuzz(ap, orc, seed):
         x = synth.uniform_pm1_torch(seed * 100 + case, n, dev)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, int(rng.choice([0, 16, 1024, 8192, 16384])))
         ap.ap_debug_set(ap.AP_DBG_GRID, int(rng.choice([0, 0, cs, 3 * cs])))
-        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2])))
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2, 3])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, int(rng.choice([0, 1, 2])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
@@ -124,14 +124,14 @@ def test_all_to_all_fuzz(ap, orc, seed):
     rng = np.random.default_rng(3000 + seed)
     for case in range(25):
         cs = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16]))
-        sub = 16 * int(rng.integers(1, 257))
+        sub = 16 * int(rng.choice([int(rng.integers(1, 257)), 256, 512]))  # up to 8 KiB: the three-CTA form too
         chunk = cs * sub
         groups = int(rng.integers(1, 60))
         n = groups * cs * chunk // 4
         x = synth.uniform_pm1_torch(seed * 1000 + case, n, dev)
         ap.ap_debug_set(ap.AP_DBG_STAGE_BYTES, int(rng.choice([0, 0, 512, 2048, 8192])))
         ap.ap_debug_set(ap.AP_DBG_GRID, int(rng.choice([0, 0, cs, 2 * cs])))
-        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2])))
+        ap.ap_debug_set(ap.AP_DBG_CTAS_PER_SM, int(rng.choice([0, 1, 2, 3])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_STORE, int(rng.choice([0, 1, 2])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_GROUP, int(rng.choice([0, 1, 2, 4, 8])))
         ap.ap_debug_set(ap.AP_DBG_EXCHANGE_LANES, int(rng.choice([0, 1, 2, 4])))
