@@ -888,7 +888,10 @@ def sweep(which: str, args):
         x = synth.uniform_pm1_torch(synth.SEED_SCALE, 4 * n_chunks, dev)
         y = torch.empty_like(x)
         for name, pattern in (("all 16 (plain copy)", [16]),
-                              ("1/8 off, 1/8 half, 1/8 zeroed, 5/8 copies", [-1, 8, -2, 16, 16, 16, 16, 16])):
+                              ("1/8 off, 1/8 half, 1/8 zeroed, 5/8 copies", [-1, 8, -2, 16, 16, 16, 16, 16]),
+                              ("1/8 half, 1/8 zeroed, 6/8 copies (no chunk left)", [8, -2, 16, 16, 16, 16, 16, 16]),
+                              ("1/8 off, 7/8 copies", [-1, 16, 16, 16, 16, 16, 16, 16]),
+                              ("2/8 off in whole sectors, 6/8 copies", [-1, -1, 16, 16, 16, 16, 16, 16])):
             pat = torch.tensor(pattern, dtype=torch.int8)
             codes = pat.repeat(n_chunks // len(pattern)).to(dev)
             rd = sum(max(c, 0) for c in pattern) / len(pattern)
