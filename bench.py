@@ -740,10 +740,14 @@ def sweep(which: str, args):
 
     window = {}
 
+    single = {}  # the median and best single launch of the last run()
+
     def line(workload, kernel, nbytes, ms, **extra):
         gb = _gbs(nbytes, ms)
         d = {"workload": workload, "kernel": kernel, "ms": round(ms, 5), "GB/s": round(gb, 1),
              "frac_of_measured_hbm": round(gb / peak, 4)}
+        d.update(single)
+        single.clear()
         d.update(extra)
         if ap.ap_check() != 0:
             d["device_status"] = "error"
@@ -756,7 +760,11 @@ def sweep(which: str, args):
         torch.cuda.synchronize()
         window["t0"] = datetime.datetime.now()
         ms = time_steps(fn, steps, 0, stream) / steps
+        # then up to 20 launches with an event between them, for the median
+        # and best single launch (rates stay those of the back-to-back region)
+        each = sorted(time_each(fn, min(steps, 20), 0, stream))
         window["t1"] = datetime.datetime.now()
+        single.update(ms_median=round(each[len(each) // 2], 5), ms_best=round(each[0], 5))
         return ms
 
     if "scale" in groups:
