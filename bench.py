@@ -1068,8 +1068,11 @@ def sweep(which: str, args):
 
 # ----------------------------------------------------------------------------- profiling cases
 
-PROFILE_CASES = ("scale", "scale_s6", "sync", "poly0", "poly8", "poly32", "poly32_s4", "poly32_s6", "poly128",
-                 "poly128_s6", "roll", "roll_mis", "roll_tensor", "exchange2", "exchange4", "exchange8", "exchange16",
+PROFILE_CASES = ("scale", "scale_s3", "scale_s4", "scale_s5", "scale_s6", "sync", "pages_async",
+                 "poly0", "poly0_s3", "poly0_s4", "poly0_s6", "poly8", "poly8_s3", "poly8_s4", "poly8_s6",
+                 "poly32_s2", "poly32", "poly32_s4", "poly32_s6", "poly128", "poly128_s3", "poly128_s4", "poly128_s6",
+                 "roll", "roll_s3", "roll_s4", "roll_s5", "roll_s6", "roll_mis", "roll_tensor",
+                 "exchange2", "exchange4", "exchange8", "exchange16",
                  "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "masked_mixed", "masked_all", "masked_off1",
                  "masked_offpair", "masked_halfzero", "torch_mul_2p28")
 
@@ -1131,6 +1134,22 @@ def profile_case(name: str, args):
         "masked_mixed": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes, 4),
         "masked_all": lambda: ap.ap_masked_copy(x[:n], y[:n], n // 4, codes16, 4),
     }
+    calls["pages_async"] = lambda: ap.ap_debug_scale_pages_async(x[:n], y[:n], n // 256, 256, 2.0)
+    # every (degree, depth) cell of the polynomial sweep and every depth of the
+    # scale and the row shift: polyK_sS, scale_sS, roll_sS (the row shift's
+    # depth through AP_DBG_ROLL_STAGES)
+    m = re.fullmatch(r"poly(\d+)_s(\d)", name)
+    if m and name not in calls:
+        deg, depth = int(m.group(1)), int(m.group(2))
+        calls[name] = lambda: ap.ap_poly(x[:n], y[:n], n, synth.coeffs_np(deg).tolist(), deg, depth)
+    m = re.fullmatch(r"(scale|roll)_s(\d)", name)
+    if m and name not in calls:
+        depth = int(m.group(2))
+        if m.group(1) == "scale":
+            calls[name] = lambda: ap.ap_scale(x[:n], y[:n], n // 256, 256, 2.0, depth)
+        else:
+            ap.ap_debug_set(ap.AP_DBG_ROLL_STAGES, depth)
+            calls[name] = lambda: ap.ap_row_roll(x[:n], y[:n], n // 4, 4, 1)
     # the mixed pattern taken apart: one chunk left in eight, two adjacent
     # chunks left (whole sectors), a half and a zeroed chunk in eight
     for key, p in (("masked_off1", [-1, 16] + rest), ("masked_offpair", [-1, -1] + rest),
