@@ -695,39 +695,62 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
     // (a run's first load is exposed with one 16-warp CTA per SM).
     if (kind == OP_POLY) {
         const int64_t r = 2 * static_cast<int64_t>(stages);  // runs: every slot filled twice
+        // Bands by degree at each depth, chosen from sweeps at degrees 0-32
+        // (every few degrees), 64, 80, 96 and 128; the best shape moves
+        // jaggedly with the degree near the crossover, so each band is the
+        // measured best of its neighbourhood.
         switch (stages) {
             case 2:
-                // degrees 0-24: 1.054 of the copy falling to 0.94 at 24 (persistent 0.93-0.97)
-                if (degree <= 24) return RingShape{64 * 1024, 1, 16, 4};
+                // 0-15: 1.05 of the copy; 16-26: 96 KiB runs 1.00-1.045 (64 KiB
+                // runs fell to 0.93 at 26); 27-31: 64 KiB persistent 1.01-1.03
+                // (96 KiB 0.92-1.0); from 32 96 KiB persistent (1.038 at 32,
+                // 0.874 of the register-only fma rate at 128)
+                if (degree <= 15) return RingShape{64 * 1024, 1, 16, 4};
+                if (degree <= 26) return RingShape{96 * 1024, 1, 16, 4};
+                if (degree <= 31) return RingShape{64 * 1024, 1, 16};
                 return RingShape{96 * 1024, 1, 16};
             case 3:
-                // degrees 0-10: 1.06 falling to 1.0; above, persistent stages
-                // of 32-64 KiB (0.92-1.0 of the copy up to degree 32); from
-                // degree 80 one 24-chain round a stage (48 KiB: 0.852 of the
-                // register-only fma rate at degree 128, 0.839 with 64 KiB)
-                if (degree <= 10) return RingShape{32 * 1024, 1, 16, r};
-                if (degree <= 16) return RingShape{32 * 1024, 1, 16};
-                if (degree <= 28) return RingShape{48 * 1024, 1, 16};
+                // 0-1: 32 KiB runs (1.06); 2-14: 48 KiB runs (1.05, where 32
+                // KiB runs fell to 0.97 at 14); 15-26: 64 KiB runs (0.99-1.044);
+                // 27-29: 48 KiB persistent (1.0-1.046); then persistent stages of
+                // 64 KiB (0.98-1.01 at 30-32); from degree 80 one 24-chain round
+                // a stage (48 KiB: 0.860 of the register-only fma rate at
+                // degree 128, 0.839 with 64 KiB)
+                if (degree <= 1) return RingShape{32 * 1024, 1, 16, r};
+                if (degree <= 14) return RingShape{48 * 1024, 1, 16, r};
+                if (degree <= 26) return RingShape{64 * 1024, 1, 16, r};
+                if (degree <= 29) return RingShape{48 * 1024, 1, 16};
                 if (degree < 80) return RingShape{64 * 1024, 1, 16};
                 return RingShape{48 * 1024, 1, 16};
             case 4:
-                // degrees 0-22: 1.055 falling to 0.98 (persistent 0.95-1.0)
-                if (degree <= 22) return RingShape{32 * 1024, 1, 16, r};
-                return RingShape{degree <= 26 ? 32 * 1024 : 48 * 1024, 1, 16};
+                // 0-16: 32 KiB runs (1.047-1.055); 17-26: 48 KiB runs (1.01-1.045,
+                // where 32 KiB runs fell to 0.92); 27-31: 32 KiB persistent in two
+                // consumer groups (0.99-1.03); from 32 48 KiB persistent in two
+                // groups (1.042 at 32, 0.872 of the register-only rate at 128)
+                if (degree <= 16) return RingShape{32 * 1024, 1, 16, r};
+                if (degree <= 26) return RingShape{48 * 1024, 1, 16, r};
+                return RingShape{degree <= 31 ? 32 * 1024 : 48 * 1024, 1, 16};
             case 5:
-                // degrees 0-18: 1.053 falling to 1.02
+                // 0-18: 32 KiB runs (1.05 falling to 1.0); 19-22: 12 consumer
+                // warps persistent (1.0-1.025, runs 0.96-0.98); 23-25: 40 KiB
+                // persistent (1.04 at 24); above 32 KiB persistent (1.0 at 26,
+                // 0.92 at 32)
                 if (degree <= 18) return RingShape{32 * 1024, 1, 16, r};
-                if (degree <= 22) return RingShape{32 * 1024, 1, 8};
+                if (degree <= 22) return RingShape{32 * 1024, 1, 12};
+                if (degree <= 25) return RingShape{40 * 1024, 1, 16};
                 return RingShape{32 * 1024, 1, 16};
             default:
-                // degrees 0-10: 24 KiB runs (1.05); 11-26: 32 KiB runs (1.044
-                // falling to 0.99); from 27 the persistent grid with 12
-                // consumer warps in three groups, each taking every third
-                // stage in two rounds of 32 chains (degree 32: 0.99-1.03 of
-                // the copy; degree 128: 0.847-0.856 of the register-only fma
-                // rate, against 0.836 with 16 warps in two groups)
-                if (degree <= 10) return RingShape{24 * 1024, 1, 16, r};
+                // 0-12: 24 KiB runs (1.05); 13-26: 32 KiB runs (1.044 falling
+                // to 0.98); 27-30: 24 KiB persistent, 16 warps in two groups
+                // (0.97-1.036, against 0.90-0.95 for the shapes either side);
+                // from 31 the persistent grid with 12 consumer warps in three
+                // groups, each taking every third stage in two rounds of 32
+                // chains (degree 32: 1.02 of the copy; degree 128: 0.853 of
+                // the register-only fma rate, against 0.836 with 16 warps in
+                // two groups)
+                if (degree <= 12) return RingShape{24 * 1024, 1, 16, r};
                 if (degree <= 26) return RingShape{32 * 1024, 1, 16, r};
+                if (degree <= 30) return RingShape{24 * 1024, 1, 16, 0, 2};
                 return RingShape{32 * 1024, 1, 12, 0, 3};
         }
     }

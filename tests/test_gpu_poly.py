@@ -127,12 +127,13 @@ def test_poly_two_consumer_groups(ap, orc, degree, stages):
 def test_poly_six_group_rounds(ap, orc, degree):
     """Stages that are whole rounds of six 16-byte groups per consumer thread
     (16 consumer warps: 48 KiB and 96 KiB) take 24 Horner chains a thread
-    from degree 64 on, and from degree 32 where a stage is one round (48 KiB);
-    five whole stages and a ragged sixth, element by element."""
+    from degree 64 on, 16 below; the automatic stage (96 KiB, or 64 KiB at
+    degrees 27-31) and both whole-round sizes; five whole stages and a
+    ragged sixth, element by element."""
     dev = device()
     c = synth.coeffs_np(degree)
     for stage_bytes in (0, 48 * 1024, 96 * 1024):
-        per = (stage_bytes or 96 * 1024) // 4
+        per = (stage_bytes or _auto_shape(degree, 2)[0] * 1024) // 4
         n = 5 * per + 1234
         x = synth.uniform_pm1_torch(n + degree + 7, n, dev)
         want = orc.poly(to_np(x), c)
@@ -149,48 +150,60 @@ def test_poly_six_group_rounds(ap, orc, degree):
 
 def _auto_shape(degree: int, stages: int) -> tuple:
     """The documented automatic shapes of ap_poly, band by band: (stage KiB,
-    stages per CTA (0: persistent grid), consumer warps)."""
+    stages per CTA (0: persistent grid), consumer warps, consumer groups)."""
     if stages == 2:
-        return (64, 4, 16) if degree <= 24 else (96, 0, 16)
+        if degree <= 15:
+            return (64, 4, 16, 1)
+        if degree <= 26:
+            return (96, 4, 16, 1)
+        return (64, 0, 16, 1) if degree <= 31 else (96, 0, 16, 1)
     if stages == 3:
-        if degree <= 10:
-            return (32, 6, 16)
-        if degree <= 16:
-            return (32, 0, 16)
-        if degree <= 28:
-            return (48, 0, 16)
-        return (64, 0, 16) if degree < 80 else (48, 0, 16)
+        if degree <= 1:
+            return (32, 6, 16, 1)
+        if degree <= 14:
+            return (48, 6, 16, 1)
+        if degree <= 26:
+            return (64, 6, 16, 1)
+        if degree <= 29:
+            return (48, 0, 16, 1)
+        return (64, 0, 16, 1) if degree < 80 else (48, 0, 16, 1)
     if stages == 4:
-        if degree <= 22:
-            return (32, 8, 16)
-        return (32, 0, 16) if degree <= 26 else (48, 0, 16)
+        if degree <= 16:
+            return (32, 8, 16, 2)
+        if degree <= 26:
+            return (48, 8, 16, 2)
+        return (32, 0, 16, 2) if degree <= 31 else (48, 0, 16, 2)
     if stages == 5:
         if degree <= 18:
-            return (32, 10, 16)
-        return (32, 0, 8) if degree <= 22 else (32, 0, 16)
-    if degree <= 10:
-        return (24, 12, 16)
-    return (32, 12, 16) if degree <= 26 else (32, 0, 12)
+            return (32, 10, 16, 1)
+        if degree <= 22:
+            return (32, 0, 12, 1)
+        return (40, 0, 16, 1) if degree <= 25 else (32, 0, 16, 1)
+    if degree <= 12:
+        return (24, 12, 16, 2)
+    if degree <= 26:
+        return (32, 12, 16, 2)
+    return (24, 0, 16, 2) if degree <= 30 else (32, 0, 12, 3)
 
 
 def test_poly_automatic_stage_sizes(ap, orc):
     """Automatic shapes across the degree bands at every depth: runs of
     stages where memory bounds the kernel, the persistent grid where the fma
-    work does (stage size, schedule and consumer warps as documented)."""
+    work does (stage size, schedule, consumer warps and groups as documented)."""
     dev = device()
     n = 3 * 24576 + 5
     x = synth.uniform_pm1_torch(n, n, dev)
-    for degree in (0, 3, 4, 8, 9, 10, 11, 16, 17, 18, 19, 20, 21, 22, 23, 24, 25, 26, 27, 28, 29, 79, 80, 128):
+    for degree in (0, 1, 2, 3, 4, 8, 12, 13, 14, 15, 16, 17, 18, 19, 22, 23, 25, 26, 27, 29, 30, 31, 32, 79, 80, 128):
         c = synth.coeffs_np(degree)
         want = orc.poly(to_np(x), c)
         for stages in (2, 3, 4, 5, 6):
             out = Guarded(n, 0, dev)
             ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
             assert ap.ap_check() == ap.AP_OK
-            kib, run, warps = _auto_shape(degree, stages)
+            kib, run, warps, groups = _auto_shape(degree, stages)
             got = (ap.ap_debug_get(ap.AP_DBG_LAST_STAGE_ELEMS), ap.ap_debug_get(ap.AP_DBG_LAST_RUN),
-                   ap.ap_debug_get(ap.AP_DBG_LAST_WARPS))
-            assert got == (kib * 256, run, warps), f"K={degree} S={stages}: {got}"
+                   ap.ap_debug_get(ap.AP_DBG_LAST_WARPS), ap.ap_debug_get(ap.AP_DBG_LAST_GROUPS))
+            assert got == (kib * 256, run, warps, groups), f"K={degree} S={stages}: {got}"
             assert_bits(to_np(out.view), want, f"poly K={degree} S={stages} automatic shape")
             assert out.intact()
 
