@@ -349,8 +349,9 @@ __device__ __forceinline__ void consume_stage(const RingParams<Op>& P, const Slo
         int q = ct;
         // 17 warps (16 consumers + producer) leave at most 96 registers a
         // thread, too few for 32 chains: 16 chains there, or 24 (six groups)
-        // where the op asks for them (a polynomial of degree 64 or more whose
-        // stages are whole rounds of six groups a thread: 1.5-4 % faster;
+        // where the op asks for them (a polynomial of degree 44 or more, 34 in
+        // two consumer groups, whose stages are whole rounds of six groups a
+        // thread: 1.5-4 % faster;
         // the 16-chain loop stays faster at low degree and for a six-plus-two
         // split). The choice is the host's: a per-stage test here cost the
         // low-degree loop 2 %.
@@ -892,9 +893,14 @@ ap_status launch_ring(const DeviceInfo& di, const Options& o, const float* in, f
                 if (warps % gcount != 0 || stages % gcount != 0 || (warps == 8 && gcount > 1)) return AP_ERR_ARG;
                 P.groups = static_cast<uint32_t>(gcount);
             }
+            // 24 chains a thread where a group's share of a stage is whole
+            // rounds of six 16-byte groups, from the degree where they beat 16
+            // chains (2^30 floats: from 34 in two groups at depth 4, +2-3 % at
+            // degrees 34-63 but -2 % at 33; from 44 in one group at depth 2,
+            // +1.3-2.5 % at 48-63 but -0.4-1 % at 33-40)
             const int64_t round_groups = 6 * 32 * 16 / P.groups;
             const bool whole_rounds = warps == 16 && (se / 4) % round_groups == 0;
-            P.op.six_groups = whole_rounds && op.degree >= 64 ? 1 : 0;
+            P.op.six_groups = whole_rounds && op.degree >= (P.groups == 2 ? 34 : 44) ? 1 : 0;
             record_ring_shape(run, warps, P.groups, warps == 16 ? (P.op.six_groups ? 24 : 16) : 32);
             for (int k = 0; k <= AP_POLY_MAX_DEGREE; ++k) P.op.c[k] = k <= op.degree ? op.coeffs[k] : 0.0f;
             return launch_ring_warps(di, warps, o.device_checks != 0, P, grid, smem, stream);

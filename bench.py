@@ -1070,7 +1070,8 @@ def sweep(which: str, args):
 
 PROFILE_CASES = ("scale", "scale_s3", "scale_s4", "scale_s5", "scale_s6", "sync", "pages_async",
                  "poly0", "poly0_s3", "poly0_s4", "poly0_s6", "poly8", "poly8_s3", "poly8_s4", "poly8_s6",
-                 "poly32_s2", "poly32", "poly32_s4", "poly32_s6", "poly128", "poly128_s3", "poly128_s4", "poly128_s6",
+                 "poly32_s2", "poly32", "poly32_s4", "poly32_s6", "poly40_s2", "poly48_s2", "poly128", "poly128_s3",
+                 "poly128_s4", "poly128_s6",
                  "roll", "roll_s3", "roll_s4", "roll_s5", "roll_s6", "roll_mis", "roll_tensor",
                  "exchange2", "exchange4", "exchange8", "exchange16",
                  "a2a4", "a2a8", "a2a16", "exchange4_256B", "masked", "masked_mixed", "masked_all", "masked_off1",

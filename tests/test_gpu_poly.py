@@ -123,13 +123,13 @@ def test_poly_two_consumer_groups(ap, orc, degree, stages):
         assert out.intact()
 
 
-@pytest.mark.parametrize("degree", [31, 32, 48, 63, 64, 127, 128, 200])
+@pytest.mark.parametrize("degree", [31, 32, 43, 44, 48, 63, 64, 127, 128, 200])
 def test_poly_six_group_rounds(ap, orc, degree):
     """Stages that are whole rounds of six 16-byte groups per consumer thread
-    (16 consumer warps: 48 KiB and 96 KiB) take 24 Horner chains a thread
-    from degree 64 on, 16 below; the automatic stage (96 KiB, or 64 KiB at
-    degrees 27-31) and both whole-round sizes; five whole stages and a
-    ragged sixth, element by element."""
+    (16 consumer warps in one group: 48 KiB and 96 KiB) take 24 Horner chains
+    a thread from degree 44 on, 16 below; the automatic stage (96 KiB, or
+    64 KiB at degrees 27-31) and both whole-round sizes; five whole stages
+    and a ragged sixth, element by element."""
     dev = device()
     c = synth.coeffs_np(degree)
     for stage_bytes in (0, 48 * 1024, 96 * 1024):
@@ -314,6 +314,8 @@ AUTO_SHAPES = {
     (0, 3): (6, 16, 1, 16), (8, 3): (6, 16, 1, 16), (32, 3): (0, 16, 1, 16), (128, 3): (0, 16, 1, 24),
     (0, 4): (8, 16, 2, 16), (8, 4): (8, 16, 2, 16), (32, 4): (0, 16, 2, 16), (128, 4): (0, 16, 2, 24),
     (0, 6): (12, 16, 2, 16), (8, 6): (12, 16, 2, 16), (32, 6): (0, 12, 3, 32), (128, 6): (0, 12, 3, 32),
+    # where 24 chains start: degree 44 in one group (depth 2), 34 in two (depth 4)
+    (43, 2): (0, 16, 1, 16), (44, 2): (0, 16, 1, 24), (33, 4): (0, 16, 2, 16), (34, 4): (0, 16, 2, 24),
 }
 
 
@@ -321,8 +323,9 @@ AUTO_SHAPES = {
 def test_poly_automatic_shapes(ap, orc, degree, stages):
     """The automatic shape of each cell of the degree x depth sweep (runs of
     stages where memory bounds the kernel, the persistent grid where the fma
-    work does, 24 chains a round from degree 64 with 16 warps, 12 warps in
-    three groups at depth 6 from degree 27) is the one that runs, and its
+    work does, 24 chains a round with 16 warps from degree 44 in one group or
+    34 in two, 12 warps in three groups at depth 6 from degree 31) is the one
+    that runs, and its
     output matches the oracle element by element."""
     dev = device()
     n = (1 << 20) + 4099
