@@ -714,14 +714,14 @@ RingShape auto_ring_shape(OpKind kind, int stages, int degree) {
                 // 0-1: 32 KiB runs (1.06); 2-14: 48 KiB runs (1.05, where 32
                 // KiB runs fell to 0.97 at 14); 15-26: 64 KiB runs (0.99-1.044);
                 // 27-29: 48 KiB persistent (1.0-1.046); then persistent stages of
-                // 64 KiB (0.98-1.01 at 30-32); from degree 80 one 24-chain round
+                // 64 KiB (0.98-1.01 at 30-32); from degree 64 one 24-chain round
                 // a stage (48 KiB: 0.860 of the register-only fma rate at
-                // degree 128, 0.839 with 64 KiB)
+                // degree 128, 0.839 with 64 KiB; +0.3-1 % at 64-79)
                 if (degree <= 1) return RingShape{32 * 1024, 1, 16, r};
                 if (degree <= 14) return RingShape{48 * 1024, 1, 16, r};
                 if (degree <= 26) return RingShape{64 * 1024, 1, 16, r};
                 if (degree <= 29) return RingShape{48 * 1024, 1, 16};
-                if (degree < 80) return RingShape{64 * 1024, 1, 16};
+                if (degree < 64) return RingShape{64 * 1024, 1, 16};
                 return RingShape{48 * 1024, 1, 16};
             case 4:
                 // 0-16: 32 KiB runs (1.047-1.055); 17-26: 48 KiB runs (1.01-1.045,

@@ -166,7 +166,7 @@ def _auto_shape(degree: int, stages: int) -> tuple:
             return (64, 6, 16, 1)
         if degree <= 29:
             return (48, 0, 16, 1)
-        return (64, 0, 16, 1) if degree < 80 else (48, 0, 16, 1)
+        return (64, 0, 16, 1) if degree < 64 else (48, 0, 16, 1)
     if stages == 4:
         if degree <= 16:
             return (32, 8, 16, 2)
@@ -193,7 +193,7 @@ def test_poly_automatic_stage_sizes(ap, orc):
     dev = device()
     n = 3 * 24576 + 5
     x = synth.uniform_pm1_torch(n, n, dev)
-    for degree in (0, 1, 2, 3, 4, 8, 12, 13, 14, 15, 16, 17, 18, 19, 22, 23, 25, 26, 27, 29, 30, 31, 32, 79, 80, 128):
+    for degree in (0, 1, 2, 3, 4, 8, 12, 13, 14, 15, 16, 17, 18, 19, 22, 23, 25, 26, 27, 29, 30, 31, 32, 63, 64, 128):
         c = synth.coeffs_np(degree)
         want = orc.poly(to_np(x), c)
         for stages in (2, 3, 4, 5, 6):
