@@ -1,7 +1,8 @@
-// The streaming ring: a persistent, warp-specialised kernel in which one
-// producer thread keeps up to S stages of input in flight with bulk
-// asynchronous copies while the consumer warps (8, or 16 on request) compute
-// on the oldest landed stage and store it.
+// The streaming ring: a warp-specialised kernel in which one producer thread
+// keeps up to S stages of input in flight with bulk asynchronous copies while
+// the consumer warps (8 for the data-movement ops; 16 or 12 for the
+// polynomial, in one to three groups that take stages in turn) compute on the
+// oldest landed stage and store it.
 //
 // Protocol per ring slot s (two mbarriers, "Asynchronous Data Movement",
 // section Barriers and pipelines: acquire, commit, wait, release):
@@ -19,9 +20,11 @@
 //
 // GB300 choices that differ from the pages' 256-float, one-block sketch:
 // a stage holds tens of KiB (many of the pages' tiles) so that each SM keeps
-// enough bytes in flight to cover HBM latency; the grid is persistent (one
-// CTA per SM, CTA b takes tiles b, b + grid, ...); the copy is a single
-// bulk-copy instruction per tile issued by one thread (the TMA engine
+// enough bytes in flight to cover HBM latency; memory-bound work runs as CTAs
+// that each take a short run of consecutive stages, started in index order so
+// the grid streams one narrow window of memory, and fma-bound work as a
+// persistent grid (CTA b takes stages b, b + grid, ...); the copy is a single
+// bulk-copy instruction per stage issued by one thread (the TMA engine
 // generates the addresses, "Asynchronous Data Movement", section The Tensor
 // Memory Accelerator) instead of every thread copying a few bytes.
 #include <cuda.h>
