@@ -208,6 +208,24 @@ def test_poly_automatic_stage_sizes(ap, orc):
             assert out.intact()
 
 
+@pytest.mark.parametrize("stages", [2, 3, 4, 5, 6])
+def test_poly_every_degree_automatic(ap, orc, stages):
+    """Every degree 0-66 and a few about 128 under the automatic shape of each
+    depth (every band edge and both chain counts), over several stages and
+    CTAs with a ragged end, element by element against the oracle."""
+    dev = device()
+    n = 5 * 24576 + 4099  # at least two CTAs under every run schedule, several stages each
+    x = synth.uniform_pm1_torch(n + 17 * stages, n, dev)
+    xh = to_np(x)
+    for degree in list(range(0, 67)) + [79, 80, 126, 127, 128]:
+        c = synth.coeffs_np(degree)
+        out = Guarded(n, 0, dev)
+        ap.ap_poly(x, out.view, n, c.tolist(), degree, stages)
+        assert ap.ap_check() == ap.AP_OK
+        assert_bits(to_np(out.view), orc.poly(xh, c), f"poly K={degree} S={stages} automatic")
+        assert out.intact()
+
+
 @pytest.mark.parametrize("degree", [0, 3, 8, 128])
 def test_poly_tensor_map_producer(ap, orc, degree):
     """Horner over the tensor-map producer's boxes, ragged lengths; three whole
