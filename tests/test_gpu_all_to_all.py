@@ -174,3 +174,35 @@ def test_all_to_all_batched(ap, orc, cs, sub_bytes, groups, batch):
             assert not ap.ap_debug_get(ap.AP_DBG_LAST_FLAGS) & 4
         assert_bits(to_np(out.view), want, f"batched a2a cs={cs} sub={sub_bytes} groups={groups} batch={batch}")
         assert out.intact()
+
+
+@pytest.mark.parametrize("op,cs", [("exchange", 4), ("all_to_all", 8)])
+def test_beyond_2p32_elements(ap, orc, op, cs):
+    """2^32 + 65536 floats (16 GiB in and 16 GiB out) in 32 KiB chunks, so
+    chunk and byte offsets pass 2^32 and 2^34: the cluster hand-off, and the
+    all-to-all over clusters of 8 in its three-CTA form. Checked group by group
+    against the oracle (a group of cs chunks is self-contained) at the first
+    and last 64 groups and 256 random ones."""
+    import torch
+
+    dev = device()
+    chunk = 32768
+    e = chunk // 4
+    n = (1 << 32) + 65536
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xA5A6)
+    x = torch.empty(n, dtype=torch.float32, device=dev).uniform_(-1.0, 1.0, generator=g)
+    y = torch.full((n,), float("nan"), dtype=torch.float32, device=dev)
+    if op == "exchange":
+        ap.ap_cluster_exchange(x, y, n, cs, chunk)
+    else:
+        ap.ap_cluster_all_to_all(x, y, n, cs, chunk)
+    assert ap.ap_check() == ap.AP_OK
+    groups = n // (cs * e)
+    rng = np.random.default_rng(5)
+    pick = sorted(set(list(range(64)) + list(range(groups - 64, groups)) + [int(v) for v in rng.integers(0, groups, 256)]))
+    for grp in pick:
+        lo, hi = grp * cs * e, (grp + 1) * cs * e
+        xg = to_np(x[lo:hi])
+        want = orc.cluster_exchange(xg, cs, chunk) if op == "exchange" else orc.cluster_all_to_all(xg, cs, chunk)
+        assert_bits(to_np(y[lo:hi]), want, f"{op} cs={cs} beyond 2^32, group {grp} of {groups}")
