@@ -112,3 +112,29 @@ def test_masked_copy_full_size(ap, orc):
     ap.ap_masked_copy(x, y, n_chunks, c_d, 4)
     assert ap.ap_check() == ap.AP_OK
     assert_bits(to_np(y), orc.masked_copy(to_np(x), np.full(4 * n_chunks, 7.0, np.float32), c_h), "full masked")
+
+
+@pytest.mark.parametrize("stages", [3, 6])
+def test_masked_copy_beyond_2p32_bytes(ap, orc, stages):
+    """2^28 + 1029 chunks (4 GiB + 16 KiB in and out, random codes), so byte
+    offsets pass 2^32, under the run schedule (depth 3) and the persistent grid
+    (depth 6); checked against the oracle over the first and last 1 Mi chunks
+    and 4096 random windows of 64 chunks."""
+    import torch
+
+    dev = device()
+    n_chunks = (1 << 28) + 1029
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xA5A7 + stages)
+    x = torch.empty(4 * n_chunks, dtype=torch.float32, device=dev).uniform_(-1.0, 1.0, generator=g)
+    codes = torch.randint(-2, 17, (n_chunks,), dtype=torch.int8, device=dev, generator=g)
+    y = torch.full_like(x, 7.0)
+    ap.ap_masked_copy(x, y, n_chunks, codes, stages)
+    assert ap.ap_check() == ap.AP_OK
+    rng = np.random.default_rng(stages)
+    windows = [(0, 1 << 20), (n_chunks - (1 << 20), n_chunks)]
+    windows += [(int(s), int(s) + 64) for s in rng.integers(0, n_chunks - 64, 4096)]
+    for lo, hi in windows:
+        xs = to_np(x[4 * lo:4 * hi])
+        want = orc.masked_copy(xs, np.full(xs.size, 7.0, np.float32), to_np(codes[lo:hi]))
+        assert_bits(to_np(y[4 * lo:4 * hi]), want, f"masked beyond 2^32 bytes, chunks {lo}..{hi} S={stages}")
