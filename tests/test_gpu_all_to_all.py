@@ -176,13 +176,15 @@ def test_all_to_all_batched(ap, orc, cs, sub_bytes, groups, batch):
         assert out.intact()
 
 
-@pytest.mark.parametrize("op,cs", [("exchange", 4), ("all_to_all", 8)])
+@pytest.mark.parametrize("op,cs", [("exchange", 4), ("all_to_all", 8), ("exchange_ex", 16)])
 def test_beyond_2p32_elements(ap, orc, op, cs):
     """2^32 + 65536 floats (16 GiB in and 16 GiB out) in 32 KiB chunks, so
-    chunk and byte offsets pass 2^32 and 2^34: the cluster hand-off, and the
-    all-to-all over clusters of 8 in its three-CTA form. Checked group by group
-    against the oracle (a group of cs chunks is self-contained) at the first
-    and last 64 groups and 256 random ones."""
+    chunk and byte offsets pass 2^32 and 2^34: the cluster hand-off, the
+    all-to-all over clusters of 8 in its three-CTA form, and the generalised
+    hand-off over 16-CTA clusters with shift 5 and a short last group of 8
+    chunks (run as a second launch). Checked group by group against the oracle
+    (a group of cs chunks is self-contained) at the first and last 64 groups
+    and 256 random ones."""
     import torch
 
     dev = device()
@@ -195,14 +197,21 @@ def test_beyond_2p32_elements(ap, orc, op, cs):
     y = torch.full((n,), float("nan"), dtype=torch.float32, device=dev)
     if op == "exchange":
         ap.ap_cluster_exchange(x, y, n, cs, chunk)
-    else:
+    elif op == "all_to_all":
         ap.ap_cluster_all_to_all(x, y, n, cs, chunk)
+    else:
+        ap.ap_cluster_exchange_ex(x, y, n, cs, chunk, 5)
     assert ap.ap_check() == ap.AP_OK
-    groups = n // (cs * e)
+    groups = -(-n // (cs * e))  # the last one short for the 16-CTA hand-off
     rng = np.random.default_rng(5)
     pick = sorted(set(list(range(64)) + list(range(groups - 64, groups)) + [int(v) for v in rng.integers(0, groups, 256)]))
     for grp in pick:
-        lo, hi = grp * cs * e, (grp + 1) * cs * e
+        lo, hi = grp * cs * e, min(n, (grp + 1) * cs * e)
         xg = to_np(x[lo:hi])
-        want = orc.cluster_exchange(xg, cs, chunk) if op == "exchange" else orc.cluster_all_to_all(xg, cs, chunk)
+        if op == "exchange":
+            want = orc.cluster_exchange(xg, cs, chunk)
+        elif op == "all_to_all":
+            want = orc.cluster_all_to_all(xg, cs, chunk)
+        else:
+            want = orc.cluster_exchange_ex(xg, cs, chunk, 5)
         assert_bits(to_np(y[lo:hi]), want, f"{op} cs={cs} beyond 2^32, group {grp} of {groups}")
